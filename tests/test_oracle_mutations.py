@@ -1,0 +1,60 @@
+"""The pins must catch plausible mistakes.
+
+Each case plants one mistake in a private copy of the oracle's C source,
+builds it with gcc into a temporary library, swaps it in, and checks that
+at least one pin of ``test_oracle_pins`` fails against it.  Runs on the CPU
+only; the real oracle is left untouched.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "swa_oracle.c")
+
+MUTATIONS = {
+    # the window holds W+1 keys instead of W
+    "window_off_by_one": ("int64_t a = p - window + 1;", "int64_t a = p - window;"),
+    # draft rows see later draft rows
+    "no_causality": ("*hi = p < seq_len - 1 ? p : seq_len - 1;", "*hi = seq_len - 1;"),
+    # query head h reads KV head h mod Hkv instead of floor(h / G)
+    "gqa_modulo": ("const int64_t g = h / G;", "const int64_t g = h % J->Hkv;"),
+    # max dropped from the log-sum-exp
+    "lse_drops_max": ("J->lse[row] = m + log(z);", "J->lse[row] = log(z);"),
+    # merge rescales with the wrong sign
+    "merge_sign": ("const double w = exp(mk - M);", "const double w = exp(M - mk);"),
+    # q and k dims transposed in the score (reads k at the wrong stride)
+    "score_operand": ("dot += qr[d] * kr[d];", "dot += qr[d] * kr[(d * 7) % D];"),
+}
+
+PIN_CHECKS = [
+    lambda: [pins.test_hand_worked_examples(c) for c in pins._load_golden()],
+    lambda: pins.test_brute_force_tiny(8),
+    lambda: pins.test_brute_force_gqa_batch_ragged(),
+    lambda: pins.test_full_window_is_causal_attention(64, 2, 1, 40, 8),
+    lambda: [pins.test_split_merge_identity(n) for n in (2, 3)],
+    lambda: pins.test_zero_keys_closed_form(),
+]
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_is_caught(name, tmp_path, monkeypatch):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread", "-o",
+                    str(lib), str(mutated), "-lm"], check=True)
+    monkeypatch.setattr(oracle, "_lib", oracle._bind(str(lib)))
+    failures = 0
+    for check in PIN_CHECKS:
+        try:
+            check()
+        except (AssertionError, ValueError):
+            failures += 1
+    assert failures > 0, f"no pin caught mutation {name}"
