@@ -1,0 +1,533 @@
+"""Benchmark of sliding-window split-KV verify attention on GB300.
+
+Metric: verify-attention microseconds per call and KV-cache GB/s (as a
+fraction of HBM bandwidth) at window 188, q_len 8.  `value` is KV GB/s
+(higher is better); `us_per_call` is reported beside it.
+
+One step = one swa_verify_attn call over one batch of the workload.  The
+default workload is the single-stream Gemma-style verify (1 sequence, 8/2
+heads, head_dim 256, context 4096, W 188, q_len 8); `--workload` selects
+another (batched, stress_w{188,512,1024}_q{1,8,64}, window_vs_full_w{188,4096},
+tiny_q{1,8}).  Inputs are seeded synthetic bf16 (no dataset exists for this
+path).
+
+Timing: the K timed steps are replays of a CUDA graph of calls, bracketed by
+a barrier and torch.cuda.synchronize() on both sides and timed with CUDA
+events on the launching stream.  L2 is defeated by rotating input replicas
+whose combined footprint is at least twice the L2 size (or, when one call
+already reads more than L2, by the size of the inputs).
+
+Algorithmic bytes per call = sum over sequences of
+  Hkv * S_b * 2 * D * 2   (K and V rows of the window span, S_b keys)
++ 2 * q_len * Hq * D * 2  (q in, out)
++ 4 * q_len * Hq          (lse)
+with S_b = min(q_pos + q_len, seq_len) - max(0, q_pos - W + 1).
+
+--impl reference times the fp64 CPU oracle (the only reference this path
+has) on the host cores, same workload, metric and unit.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "verify-attn µs/call and KV GB/s (% of GB300 HBM peak) at W=188, q_len=8"
+UNIT = "GB/s"
+
+
+# ----------------------------------------------------------------- workloads
+
+def make_workload(name, device, seed=0):
+    from sliding_window_speculative_gb300 import inputs
+    if name == "single_stream":
+        return inputs.single_stream(device=device, seed=seed)
+    if name == "batched":
+        return inputs.batched(device=device, seed=seed)
+    if name.startswith("window_vs_full_w"):
+        return inputs.window_vs_full(int(name.rsplit("w", 1)[1]), device=device, seed=seed)
+    if name.startswith("tiny_q"):
+        return inputs.tiny(int(name[6:]), device=device, seed=seed)
+    if name.startswith("stress_w"):
+        # stress_w{W}_q{Q}[_l{L}]: the bandwidth-stress batch; _l shortens the
+        # cache (and the context range) for profiler captures.
+        parts = name.split("_")
+        W, Q = int(parts[1][1:]), int(parts[2][1:])
+        L = int(parts[3][1:]) if len(parts) > 3 else 32768
+        return inputs.stress(W, Q, device=device, max_len=L, seed=seed)
+    raise ValueError(f"unknown workload {name}")
+
+
+def workload_bytes(case):
+    d = case.dims
+    kv = 0
+    for sl, qp in zip(case.seq_lens_host, case.q_pos_host):
+        lo = max(0, qp - case.window + 1)
+        hi = min(qp + d["q_len"], sl)
+        kv += d["num_kv_heads"] * max(0, hi - lo) * 2 * d["head_dim"] * 2
+    qo = 2 * d["batch"] * d["q_len"] * d["num_q_heads"] * d["head_dim"] * 2
+    lse = 4 * d["batch"] * d["q_len"] * d["num_q_heads"]
+    return kv, kv + qo + lse
+
+
+def workload_flops(case):
+    d = case.dims
+    G = d["num_q_heads"] // d["num_kv_heads"]
+    f = 0
+    for sl, qp in zip(case.seq_lens_host, case.q_pos_host):
+        for i in range(d["q_len"]):
+            p = qp + i
+            n = max(0, min(p, sl - 1) - max(0, p - case.window + 1) + 1)
+            f += n * 4 * d["head_dim"] * G * d["num_kv_heads"]
+    return f
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, device_index):
+        self.proc = None
+        sel = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            sel = vis.split(",")[device_index] if vis else str(device_index)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100", "-i", sel],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        self.lines = []
+        self.t = None
+        if self.proc is not None:
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=2)
+        except Exception:
+            self.proc.kill()
+        if self.t is not None:
+            self.t.join(timeout=2)
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            rows.append((ts, parts))
+        window = [p for ts, p in rows if t0 - 0.15 <= ts <= t1 + 0.15] or [p for _, p in rows]
+        mhz = [float(p[0]) for p in window if p[0].replace(".", "").isdigit()]
+        mx = [float(p[1]) for p in window if p[1].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for p in window:
+            for n, val in zip(names, p[4:]):
+                if val.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(window)}
+
+
+# ------------------------------------------------------------- GPU timing
+
+class Replicas:
+    """Copies of a workload's tensors at distinct addresses, so consecutive
+    calls read cold data."""
+
+    def __init__(self, case, n):
+        self.n = n
+        self.case = case
+        B = case.q.shape[0]
+        self.q = case.q.unsqueeze(0).repeat(n, 1, 1, 1, 1) if n > 1 else case.q.unsqueeze(0)
+        if n > 1:
+            self.k = torch.empty((n,) + tuple(case.k_cache.shape), dtype=torch.bfloat16,
+                                 device=case.q.device)
+            self.v = torch.empty_like(self.k)
+            self.k[:] = case.k_cache
+            self.v[:] = case.v_cache
+        else:
+            self.k = case.k_cache.unsqueeze(0)
+            self.v = case.v_cache.unsqueeze(0)
+        self.out = torch.empty_like(self.q)
+        self.lse = torch.empty((n, B, case.q.shape[1], case.q.shape[2]), dtype=torch.float32,
+                               device=case.q.device)
+
+    def call(self, i, num_splits=0):
+        from sliding_window_speculative_gb300 import swa_verify_attn
+        r = i % self.n
+        c = self.case
+        swa_verify_attn(self.q[r], self.k[r], self.v[r], c.seq_lens, c.q_pos, c.window, c.scale,
+                        out=self.out[r], lse=self.lse[r], num_splits=num_splits)
+
+
+def replica_count(case, bytes_per_call):
+    l2 = getattr(torch.cuda.get_device_properties(case.q.device), "L2_cache_size", 0) or (126 << 20)
+    if bytes_per_call >= l2:
+        return 1, l2
+    n = math.ceil(2 * l2 / bytes_per_call)
+    slab = case.k_cache.numel() * 2 * 2 + case.q.numel() * 2 * 2
+    n = max(2, min(n, 2048, int((16 << 30) // max(slab, 1))))
+    return n, l2
+
+
+def time_device(case, steps, warmup, num_splits=0, graph_len=1000, dist=None):
+    """Device time of `steps` calls (graph replays), L2 defeated by replicas.
+    Returns dict with total seconds and per-call microseconds."""
+    kv, total = workload_bytes(case)
+    nrep, l2 = replica_count(case, total)
+    rep = Replicas(case, nrep)
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3)):
+            rep.call(i, num_splits)
+    stream.synchronize()
+    g_len = max(1, min(graph_len, steps))
+    graphs = {}
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                rep.call(i, num_splits)
+        return g
+
+    full, rest = divmod(steps, g_len)
+    if full:
+        graphs["full"] = capture(g_len)
+    if rest:
+        graphs["rest"] = capture(rest)
+    # warm the graphs themselves
+    with torch.cuda.stream(stream):
+        for g in graphs.values():
+            g.replay()
+    stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(full):
+            graphs["full"].replay()
+        if rest:
+            graphs["rest"].replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if dist is not None:
+        dist.barrier()
+    ms = start.elapsed_time(end)
+    del graphs, rep
+    return {"seconds": ms / 1e3, "us_per_call": ms * 1e3 / steps, "replicas": nrep,
+            "l2_bytes": l2, "wall": (t0, t1), "kv_bytes": kv, "bytes": total}
+
+
+def time_e2e(case, steps, warmup):
+    """Through the public call with host buffers: each step copies q,
+    seq_lens, q_pos and the q_len new K/V rows per (sequence, KV head) from
+    pinned host memory, calls swa_verify_attn, and copies out and lse back to
+    pinned host memory.  Timed with CUDA events around all steps."""
+    from sliding_window_speculative_gb300 import swa_verify_attn
+    B, q_len, Hq, D = case.q.shape
+    Hkv = case.k_cache.shape[1]
+    h_q = case.q.cpu().pin_memory()
+    h_sl = case.seq_lens.cpu().pin_memory()
+    h_qp = case.q_pos.cpu().pin_memory()
+    # new K/V rows: [B, Hkv, q_len, D] at positions q_pos .. q_pos + q_len
+    rows_k = torch.stack([case.k_cache[b, :, p:p + q_len] for b, p in
+                          enumerate(case.q_pos_host)]).cpu().pin_memory()
+    rows_v = torch.stack([case.v_cache[b, :, p:p + q_len] for b, p in
+                          enumerate(case.q_pos_host)]).cpu().pin_memory()
+    d_q = torch.empty_like(case.q)
+    d_sl = torch.empty_like(case.seq_lens)
+    d_qp = torch.empty_like(case.q_pos)
+    d_rows_k = torch.empty(rows_k.shape, dtype=rows_k.dtype, device=case.q.device)
+    d_rows_v = torch.empty_like(d_rows_k)
+    out = torch.empty_like(case.q)
+    lse = torch.empty((B, q_len, Hq), dtype=torch.float32, device=case.q.device)
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    stream = torch.cuda.Stream()
+    h2d = (h_q.numel() * 2 + h_sl.numel() * 4 + h_qp.numel() * 4 + rows_k.numel() * 2 * 2)
+    d2h = out.numel() * 2 + lse.numel() * 4
+
+    def step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_sl.copy_(h_sl, non_blocking=True)
+        d_qp.copy_(h_qp, non_blocking=True)
+        d_rows_k.copy_(rows_k, non_blocking=True)
+        d_rows_v.copy_(rows_v, non_blocking=True)
+        for b, p in enumerate(case.q_pos_host):
+            case.k_cache[b, :, p:p + q_len].copy_(d_rows_k[b], non_blocking=True)
+            case.v_cache[b, :, p:p + q_len].copy_(d_rows_v[b], non_blocking=True)
+        swa_verify_attn(d_q, case.k_cache, case.v_cache, d_sl, d_qp, case.window, case.scale,
+                        out=out, lse=lse)
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            step()
+    stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    return {"us_per_call": ms * 1e3 / steps, "h2d": h2d, "d2h": d2h, "steps": steps}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(case, budget_s=10.0, max_calls=None, threads=None):
+    """Times the fp64 oracle on whole calls of the workload (sequences
+    sampled if one call is too long).  Returns per-call seconds scaled to the
+    full batch, the sample description and the threads used."""
+    import oracle
+    from tests.helpers import host_slices
+    B = case.q.shape[0]
+    kv, _ = workload_bytes(case)
+    threads = threads or oracle.default_threads()
+    seqs = list(range(B))
+    # estimate cost per sequence from its window span to bound the sample
+    q, k, v, base, sl, qp = host_slices(case, seqs[:1], margin=0)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, sl, qp, case.window, case.scale, base=base, threads=threads)
+    per_seq = max(time.perf_counter() - t0, 1e-6)
+    n_seq = max(1, min(B, int(budget_s / 4 / per_seq)))
+    seqs = seqs[:n_seq]
+    q, k, v, base, sl, qp = host_slices(case, seqs, margin=0)
+    calls = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.attention(q, k, v, sl, qp, case.window, case.scale, base=base, threads=threads)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_calls and calls >= max_calls):
+            break
+    per_call_sample = el / calls
+    frac = n_seq / B
+    per_call_full = per_call_sample / frac
+    used = min(threads, n_seq * case.q.shape[2])
+    sample = (f"{calls} oracle calls over {n_seq} of {B} sequences (all rows and heads of "
+              f"each), {el:.1f} s, scaled to the full batch")
+    return {"seconds_per_call": per_call_full, "sample": sample, "cores": used,
+            "kv_gbs": kv / per_call_full / 1e9}
+
+
+# ------------------------------------------------------------------- main
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="single_stream")
+    ap.add_argument("--splits", type=int, default=0, help="force a split count (0 = heuristic)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--also", default="batched,stress_w188_q8",
+                    help="extra workloads measured the same way (rank 0, device time)")
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return main_reference(args, world, rank)
+
+    from sliding_window_speculative_gb300 import build as libbuild
+    if rank == 0:
+        libbuild.build()
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+        dist.barrier()
+        libbuild.build()
+    else:
+        torch.cuda.set_device(local)
+    import sliding_window_speculative_gb300 as swa
+    dev = torch.device("cuda", local)
+    case = make_workload(args.workload, dev, seed=rank)
+    kv, total = workload_bytes(case)
+    plan = swa.swa_plan(swa.dims_of(case.q, case.k_cache, args.splits), case.window,
+                        torch.cuda.get_device_properties(dev).multi_processor_count)
+
+    sampler = ClockSampler(local)
+    r = time_device(case, args.steps, args.warmup, args.splits, dist=dist)
+    clocks = sampler.stop(*r["wall"])
+    secs = torch.tensor([r["seconds"]], device=dev)
+    if dist is not None:
+        dist.all_reduce(secs, op=dist.ReduceOp.MAX)
+    seconds = float(secs.item())
+    value = kv * args.steps * world / seconds / 1e9
+    us = seconds * 1e6 / args.steps
+
+    peak, peak_src = peaks()
+    launches_per_call = 1 + plan["merge"]
+    achieved = total / (us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
+        "us_per_call": round(us, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, **case.dims, "window": case.window,
+                   "kv_bytes_per_call": kv, "bytes_per_call": total,
+                   "l2": f"defeated by {r['replicas']} input replicas"
+                         if r["replicas"] > 1 else "inputs larger than L2",
+                   "timing": "CUDA graph of calls, CUDA events on the launching stream",
+                   "plan": plan, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "kernel": "swa_simt_kernel" +
+                     (" + swa_merge_kernel" if plan["merge"] else ""),
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "traffic": None,
+                     "note": "achieved = algorithmic bytes per call / device time per call"},
+        "clocks": clocks,
+        "gpu_launches": launches_per_call * args.steps,
+    }
+    if rank == 0 and not args.no_e2e:
+        e = time_e2e(case, min(args.steps, 2000), args.warmup)
+        line["e2e"] = {"value": round(kv / (e["us_per_call"] * 1e-6) / 1e9, 3), "unit": UNIT,
+                       "us_per_call": round(e["us_per_call"], 3),
+                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
+    if rank == 0 and world == 1 and args.also:
+        also = {}
+        for name in [a for a in args.also.split(",") if a and a != args.workload]:
+            c2 = make_workload(name, dev)
+            k2, t2 = workload_bytes(c2)
+            steps2 = max(50, min(2000, int(0.3e9 / max(t2, 1))))
+            r2 = time_device(c2, steps2, 5)
+            p2 = swa.swa_plan(swa.dims_of(c2.q, c2.k_cache), c2.window,
+                              torch.cuda.get_device_properties(dev).multi_processor_count)
+            ach = t2 / (r2["us_per_call"] * 1e-6) / 1e9
+            also[name] = {"us_per_call": round(r2["us_per_call"], 3),
+                          "kv_gbs": round(k2 / (r2["us_per_call"] * 1e-6) / 1e9, 2),
+                          "achieved_gbs": round(ach, 2), "frac": round(ach / peak, 4),
+                          "steps": steps2, "replicas": r2["replicas"],
+                          "splits": p2["num_splits"]}
+            del c2
+            torch.cuda.empty_cache()
+        line["also"] = also
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cb = oracle_sample(case, args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(cb["kv_gbs"], 6), "unit": UNIT,
+                                "cores": cb["cores"], "kind": "oracle", "sample": cb["sample"]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main_reference(args, world, rank):
+    """The oracle as the reference arm: each step is one oracle call over a
+    bounded sample of the workload's sequences (all heads and rows of each),
+    sized so that warm-up plus K steps stay within about three minutes."""
+    if rank != 0:
+        return
+    import oracle
+    from oracle import build as oraclebuild
+    from tests.helpers import host_slices
+    oraclebuild.build()
+    case = make_workload(args.workload, "cpu")
+    B = case.q.shape[0]
+    threads = oracle.default_threads()
+    q, k, v, base, sl, qp = host_slices(case, [0], margin=0)
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, sl, qp, case.window, case.scale, base=base, threads=threads)
+    per_seq = max(time.perf_counter() - t0, 1e-6)
+    budget = 150.0 / max(args.steps + args.warmup, 1)
+    n_seq = max(1, min(B, int(budget / per_seq)))
+    seqs = list(range(n_seq))
+    q, k, v, base, sl, qp = host_slices(case, seqs, margin=0)
+    sub_kv = 0
+    d = case.dims
+    for b in seqs:
+        lo = max(0, case.q_pos_host[b] - case.window + 1)
+        hi = min(case.q_pos_host[b] + d["q_len"], case.seq_lens_host[b])
+        sub_kv += d["num_kv_heads"] * max(0, hi - lo) * 2 * d["head_dim"] * 2
+    for _ in range(args.warmup):
+        oracle.attention(q, k, v, sl, qp, case.window, case.scale, base=base, threads=threads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.attention(q, k, v, sl, qp, case.window, case.scale, base=base, threads=threads)
+    el = time.perf_counter() - t0
+    per_step = el / args.steps
+    value = sub_kv / per_step / 1e9
+    used = min(threads, n_seq * case.q.shape[2])
+    sample = (f"each step: one fp64 oracle call over {n_seq} of {B} sequences "
+              f"(all heads and draft rows), {threads} threads")
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": args.workload, **case.dims, "window": case.window,
+                   "sampled_sequences": n_seq},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": used,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

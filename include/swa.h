@@ -1,0 +1,151 @@
+/*
+ * swa.h - sliding-window split-KV verify attention for GB300 (sm_103a).
+ *
+ * One call computes, for a block of q_len query rows per sequence (one
+ * committed token plus the drafted tokens of a speculative-decoding step),
+ * grouped-query attention over a bf16 KV cache in which the query at
+ * absolute position p sees only the keys at positions (p - W, p]:
+ *
+ *   "The Fast Gemma Challenge: our verified-SOTA recipe, in full",
+ *   manifest keys SLIDING_WINDOW=188 / FA_SLIDING=1 (attend to the most
+ *   recent W tokens, section "What each piece does, and why"),
+ *   SPECULATIVE_CONFIG num_speculative_tokens=7 (q_len = 1 + 7 = 8),
+ *   SPLITKV_VERIFY=1 and SPLITKV_VERIFY_MAX_Q=64 (split-KV verify kernel,
+ *   at most 64 query rows per call).
+ *
+ * Definition (per sequence b, query head h, draft row i, p = q_pos[b] + i,
+ * KV head g = floor(h / (Hq / Hkv))):
+ *   K(p) = { j : max(0, p - W + 1) <= j <= p, j < seq_len[b], j < max_len }
+ *   s_j  = scale * <q[b,i,h,:], k_cache[b,g,j,:]>
+ *   lse  = ln sum_{j in K(p)} exp(s_j)
+ *   out  = sum_{j in K(p)} exp(s_j - lse) * v_cache[b,g,j,:]
+ * A row with an empty K(p) gets out = 0 and lse = -inf.
+ *
+ * All entry points are plain C: device pointers and host structs, no
+ * framework types.  Nothing here synchronises the device unless stated.
+ */
+#ifndef SWA_H
+#define SWA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *swa_stream_t;
+
+typedef enum {
+    SWA_OK = 0,
+    SWA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape or size      */
+    SWA_ERR_UNSUPPORTED = 2,  /* well-formed but outside what the kernels cover  */
+    SWA_ERR_WORKSPACE = 3,    /* split partials need more workspace than is set  */
+                              /* and it cannot be grown (stream capture active)  */
+    SWA_ERR_CUDA = 4          /* a CUDA runtime call failed; see swa_last_error  */
+} swa_status;
+
+/* Shapes of one call.  The pages give no shapes; these name the tensors'
+ * dimensions.  All tensors are contiguous row-major. */
+typedef struct {
+    int32_t batch;         /* B, number of sequences, 1..65535                  */
+    int32_t q_len;         /* query rows per sequence, 1..64 (SPLITKV_VERIFY_MAX_Q) */
+    int32_t num_q_heads;   /* Hq                                                */
+    int32_t num_kv_heads;  /* Hkv, Hq % Hkv == 0; G = Hq / Hkv query heads per KV head */
+    int32_t head_dim;      /* D, one of 64, 128, 256                            */
+    int32_t max_len;       /* L, cache rows per (sequence, KV head), >= 1       */
+    int32_t num_splits;    /* 0: the library picks the split count; n >= 1 forces n
+                              chunks per (sequence, KV head) (clamped to 1..64)   */
+} swa_dims;
+
+/* Windowed verify attention ("split-KV verify kernel", SPLITKV_VERIFY).
+ *
+ *   q        bf16 [B, q_len, Hq, D]   device, 16-byte aligned
+ *   k_cache  bf16 [B, Hkv, L, D]      device, 16-byte aligned
+ *   v_cache  bf16 [B, Hkv, L, D]      device, 16-byte aligned
+ *   seq_lens int32 [B]                device: valid cache rows per sequence
+ *   q_pos    int32 [B]                device: absolute position of query row 0;
+ *                                      row i sits at q_pos + i
+ *   window   W >= 1                   keys (p - W, p] are visible to row p
+ *   scale    finite                   multiplies q.k (1/sqrt(D) for plain attention)
+ *   out      bf16 [B, q_len, Hq, D]   device, 16-byte aligned, written
+ *   lse      fp32 [B, q_len, Hq]      device or NULL; natural-log log-sum-exp
+ *   dims     host struct, read during the call only
+ *   stream   work is enqueued on this stream; the call returns without waiting
+ *
+ * Device-side preconditions (not checked on the host because the values
+ * live on the device): 0 <= q_pos, q_pos + q_len <= seq_len <= L, and the
+ * caller has written the q_len new K/V rows before the call.  If they do not
+ * hold the kernels still never read a cache row outside [0, L) of the
+ * sequence's own slab, and rows without a visible key get out = 0,
+ * lse = -inf.
+ *
+ * Ownership: every pointer stays owned by the caller; nothing is retained
+ * after the call except through the workspace described below.
+ *
+ * Workspace: when the chosen split count needs split partials in global
+ * memory, they go to the workspace set with swa_set_workspace() for the
+ * current device, or else to a library-owned buffer grown on demand with
+ * cudaMalloc (never while `stream` is capturing: then SWA_ERR_WORKSPACE).
+ * All calls on one device share that buffer, so calls that may run at the
+ * same time on different streams race on it; order them on one stream or
+ * give each its own device.
+ *
+ * Errors: SWA_ERR_INVALID_ARG / SWA_ERR_UNSUPPORTED are returned before any
+ * CUDA call and leave the outputs untouched.  SWA_ERR_CUDA reports a failed
+ * launch or allocation.  swa_last_error() gives the message. */
+swa_status swa_verify_attn(const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *seq_lens, const int32_t *q_pos, int32_t window,
+                           float scale, void *out, float *lse, const swa_dims *dims,
+                           swa_stream_t stream);
+
+/* Upper bound, in bytes, of the split-partial workspace any call with these
+ * dims and window may need on any device (pure host arithmetic; 0 if the
+ * arguments are invalid).  Layout: fp32 acc [B, Hkv, splits, R, D] followed
+ * by fp32 (m, l) pairs [B, Hkv, splits, R, 2], R = q_len * Hq / Hkv. */
+size_t swa_workspace_bytes(const swa_dims *dims, int32_t window);
+
+/* Use caller-owned device memory [dev_ptr, dev_ptr + bytes) as the
+ * workspace of the current device (16-byte aligned).  The library frees any
+ * buffer it grew itself.  dev_ptr = NULL, bytes = 0 returns to the
+ * library-owned buffer.  The memory must stay valid until replaced. */
+swa_status swa_set_workspace(void *dev_ptr, size_t bytes);
+
+/* Release the library-owned workspace of the current device (synchronises
+ * the device through cudaFree). */
+swa_status swa_release_workspace(void);
+
+/* What the library would launch for these dims on a GPU with `num_sms`
+ * SMs (pure host arithmetic, no CUDA call). */
+typedef struct {
+    int32_t kernel;        /* 1 = CUDA-core (SIMT) chunk kernel                 */
+    int32_t num_splits;    /* chunks per (sequence, KV head)                    */
+    int32_t chunk_keys;    /* keys per chunk                                    */
+    int32_t row_tiles;     /* CTAs along the packed rows R = q_len * G          */
+    int32_t rows_per_tile; /* packed rows per CTA                               */
+    int32_t grid_ctas;     /* CTAs of the attention kernel                      */
+    int32_t merge;         /* 0 none, 1 separate log-sum-exp merge kernel       */
+    int64_t workspace_bytes; /* global scratch this plan uses                   */
+} swa_plan_info;
+
+swa_status swa_plan(const swa_dims *dims, int32_t window, int32_t num_sms,
+                    swa_plan_info *plan);
+
+/* Thread-local message of the last failing call on this thread ("" if none). */
+const char *swa_last_error(void);
+
+/* Device-side fault word of the current device: every bounded wait inside
+ * the kernels that gives up sets a bit here instead of hanging.  Reading it
+ * synchronises the device; the word is cleared after the read.
+ * Bit 0: a K/V tile copy did not complete within the wait limit. */
+swa_status swa_read_device_errors(uint32_t *flags);
+
+/* Library version, e.g. "swa 0.1.0 sm_103a". */
+const char *swa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWA_H */

@@ -1,0 +1,16 @@
+"""Sliding-window split-KV verify attention on GB300 (sm_103a).
+
+The compute lives in the CUDA library ``libswa.so`` (C ABI, include/swa.h);
+this package is its thin Python binding plus the seeded synthetic input
+generators (``inputs``).  The library is loaded on first use and a missing
+build raises: there is no CPU path.
+"""
+from ._binding import (SWA_ERR_CUDA, SWA_ERR_INVALID_ARG, SWA_ERR_UNSUPPORTED,  # noqa: F401
+                       SWA_ERR_WORKSPACE, SWA_OK, SwaDims, SwaError, dims_of, load_library,
+                       make_dims, swa_last_error, swa_plan, swa_read_device_errors,
+                       swa_release_workspace, swa_set_workspace, swa_verify_attn,
+                       swa_version, swa_workspace_bytes)
+
+__all__ = ["swa_verify_attn", "swa_workspace_bytes", "swa_set_workspace",
+           "swa_release_workspace", "swa_plan", "swa_last_error", "swa_read_device_errors",
+           "swa_version", "SwaDims", "SwaError", "make_dims", "dims_of", "load_library"]

@@ -1,0 +1,187 @@
+"""ctypes binding of libswa.so (include/swa.h), argument marshalling only.
+
+Every compute step runs in the CUDA library; this module checks tensor
+types, takes raw device pointers and the current CUDA stream, and calls the
+C entry point of the same name.  If the library has not been built the first
+call raises: there is no fallback.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libswa.so")
+
+SWA_OK = 0
+SWA_ERR_INVALID_ARG = 1
+SWA_ERR_UNSUPPORTED = 2
+SWA_ERR_WORKSPACE = 3
+SWA_ERR_CUDA = 4
+_STATUS = {0: "SWA_OK", 1: "SWA_ERR_INVALID_ARG", 2: "SWA_ERR_UNSUPPORTED",
+           3: "SWA_ERR_WORKSPACE", 4: "SWA_ERR_CUDA"}
+
+
+class SwaDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("q_len", ctypes.c_int32),
+                ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("max_len", ctypes.c_int32),
+                ("num_splits", ctypes.c_int32)]
+
+
+class SwaPlanInfo(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("num_splits", ctypes.c_int32),
+                ("chunk_keys", ctypes.c_int32), ("row_tiles", ctypes.c_int32),
+                ("rows_per_tile", ctypes.c_int32), ("grid_ctas", ctypes.c_int32),
+                ("merge", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64)]
+
+
+class SwaError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path=LIB_PATH):
+    """Load libswa.so and declare the C signatures.  Raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is not built; run sliding_window_speculative_gb300.build.build() "
+                          "(nvcc, sm_103a). There is no CPU fallback.")
+    lib = ctypes.CDLL(path)
+    vp, sz, i32 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32
+    lib.swa_verify_attn.argtypes = [vp, vp, vp, vp, vp, i32, ctypes.c_float, vp, vp,
+                                    ctypes.POINTER(SwaDims), vp]
+    lib.swa_verify_attn.restype = ctypes.c_int
+    lib.swa_workspace_bytes.argtypes = [ctypes.POINTER(SwaDims), i32]
+    lib.swa_workspace_bytes.restype = sz
+    lib.swa_set_workspace.argtypes = [vp, sz]
+    lib.swa_set_workspace.restype = ctypes.c_int
+    lib.swa_release_workspace.argtypes = []
+    lib.swa_release_workspace.restype = ctypes.c_int
+    lib.swa_plan.argtypes = [ctypes.POINTER(SwaDims), i32, i32, ctypes.POINTER(SwaPlanInfo)]
+    lib.swa_plan.restype = ctypes.c_int
+    lib.swa_last_error.argtypes = []
+    lib.swa_last_error.restype = ctypes.c_char_p
+    lib.swa_read_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.swa_read_device_errors.restype = ctypes.c_int
+    lib.swa_version.argtypes = []
+    lib.swa_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(status):
+    if status != SWA_OK:
+        raise SwaError(status, swa_last_error())
+
+
+def make_dims(batch, q_len, num_q_heads, num_kv_heads, head_dim, max_len, num_splits=0):
+    return SwaDims(batch, q_len, num_q_heads, num_kv_heads, head_dim, max_len, num_splits)
+
+
+def dims_of(q, k_cache, num_splits=0):
+    B, q_len, Hq, D = q.shape
+    Hkv, L = k_cache.shape[1], k_cache.shape[2]
+    return make_dims(B, q_len, Hq, Hkv, D, L, num_splits)
+
+
+def _dev_tensor(t, name, dtype, ndim):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be on a CUDA device (got {t.device})")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype} (got {t.dtype})")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions (got {tuple(t.shape)})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def swa_verify_attn(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out=None, lse=None,
+                    num_splits=0, stream=None, want_lse=True):
+    """Windowed verify attention through the C entry point swa_verify_attn.
+
+    q bf16 [B, q_len, Hq, D]; k_cache, v_cache bf16 [B, Hkv, L, D];
+    seq_lens, q_pos int32 [B] (device).  Returns (out, lse); out/lse are
+    allocated if not given (lse only if want_lse).  Enqueued on `stream`
+    (default: torch's current stream); does not synchronise.
+    """
+    lib = load_library()
+    B, q_len, Hq, D = q.shape
+    pq = _dev_tensor(q, "q", torch.bfloat16, 4)
+    pk = _dev_tensor(k_cache, "k_cache", torch.bfloat16, 4)
+    pv = _dev_tensor(v_cache, "v_cache", torch.bfloat16, 4)
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    if k_cache.shape[0] != B or k_cache.shape[3] != D:
+        raise ValueError("cache shape does not match q")
+    ps = _dev_tensor(seq_lens, "seq_lens", torch.int32, 1)
+    pp = _dev_tensor(q_pos, "q_pos", torch.int32, 1)
+    if seq_lens.numel() != B or q_pos.numel() != B:
+        raise ValueError("seq_lens and q_pos need one entry per sequence")
+    if out is None:
+        out = torch.empty_like(q)
+    po = _dev_tensor(out, "out", torch.bfloat16, 4)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if lse is None and want_lse:
+        lse = torch.empty((B, q_len, Hq), dtype=torch.float32, device=q.device)
+    pl = None
+    if lse is not None:
+        pl = _dev_tensor(lse, "lse", torch.float32, 3)
+        if tuple(lse.shape) != (B, q_len, Hq):
+            raise ValueError("lse must be [B, q_len, Hq]")
+    dims = dims_of(q, k_cache, num_splits)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _check(lib.swa_verify_attn(pq, pk, pv, ps, pp, int(window), float(scale), po, pl,
+                               ctypes.byref(dims), handle))
+    return out, lse
+
+
+def swa_workspace_bytes(dims, window):
+    return load_library().swa_workspace_bytes(ctypes.byref(dims), int(window))
+
+
+def swa_set_workspace(buffer=None):
+    """Use a caller-owned CUDA tensor as the current device's workspace
+    (None returns to the library-owned buffer)."""
+    lib = load_library()
+    if buffer is None:
+        _check(lib.swa_set_workspace(None, 0))
+    else:
+        _check(lib.swa_set_workspace(buffer.data_ptr(), buffer.numel() * buffer.element_size()))
+
+
+def swa_release_workspace():
+    _check(load_library().swa_release_workspace())
+
+
+def swa_plan(dims, window, num_sms):
+    info = SwaPlanInfo()
+    _check(load_library().swa_plan(ctypes.byref(dims), int(window), int(num_sms),
+                                   ctypes.byref(info)))
+    return {f: getattr(info, f) for f, _ in SwaPlanInfo._fields_}
+
+
+def swa_last_error():
+    return load_library().swa_last_error().decode()
+
+
+def swa_read_device_errors():
+    flags = ctypes.c_uint32(0)
+    _check(load_library().swa_read_device_errors(ctypes.byref(flags)))
+    return flags.value
+
+
+def swa_version():
+    return load_library().swa_version().decode()

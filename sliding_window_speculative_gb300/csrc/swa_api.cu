@@ -1,0 +1,391 @@
+// C-ABI of the sliding-window split-KV verify-attention library: argument
+// validation, the split heuristic, workspace management and kernel launch.
+// Every entry point is declared (with its contract) in include/swa.h.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/swa.h"
+#include "swa_simt.cuh"
+
+// Fault word of each device that loads the library; kernels receive its
+// address and OR bits into it when a bounded wait gives up.
+__device__ uint32_t g_fault_word = 0;
+
+namespace {
+
+constexpr int kMaxSplits = 64;
+constexpr int kMaxQLen = 64;      // SPLITKV_VERIFY_MAX_Q
+constexpr int kMaxDevices = 64;
+
+thread_local char t_last_error[512] = "";
+
+swa_status fail(swa_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof t_last_error, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+swa_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(SWA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+swa_status validate_dims(const swa_dims *d, int32_t window) {
+    if (d == nullptr) return fail(SWA_ERR_INVALID_ARG, "dims is NULL");
+    if (d->batch < 1 || d->batch > 65535)
+        return fail(SWA_ERR_INVALID_ARG, "batch %d outside [1, 65535]", d->batch);
+    if (d->q_len < 1 || d->q_len > kMaxQLen)
+        return fail(SWA_ERR_INVALID_ARG, "q_len %d outside [1, %d]", d->q_len, kMaxQLen);
+    if (d->num_q_heads < 1 || d->num_kv_heads < 1)
+        return fail(SWA_ERR_INVALID_ARG, "head counts must be >= 1 (Hq %d, Hkv %d)",
+                    d->num_q_heads, d->num_kv_heads);
+    if (d->num_q_heads % d->num_kv_heads != 0)
+        return fail(SWA_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d",
+                    d->num_q_heads, d->num_kv_heads);
+    if (d->num_kv_heads > 65535)
+        return fail(SWA_ERR_INVALID_ARG, "num_kv_heads %d too large", d->num_kv_heads);
+    if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256)
+        return fail(SWA_ERR_UNSUPPORTED, "head_dim %d not in {64, 128, 256}", d->head_dim);
+    if (d->max_len < 1) return fail(SWA_ERR_INVALID_ARG, "max_len %d < 1", d->max_len);
+    if (window < 1) return fail(SWA_ERR_INVALID_ARG, "window %d < 1", window);
+    if (d->num_splits < 0) return fail(SWA_ERR_INVALID_ARG, "num_splits %d < 0", d->num_splits);
+    const long long R = (long long)d->q_len * (d->num_q_heads / d->num_kv_heads);
+    if (R > 4096) return fail(SWA_ERR_UNSUPPORTED, "q_len * G = %lld rows per KV head > 4096", R);
+    // cache and query element counts must fit the kernels' size_t arithmetic
+    // and the grid: Hkv * row_tiles <= 65535
+    const long long row_tiles = (R + 31) / 32;
+    if ((long long)d->num_kv_heads * row_tiles > 65535)
+        return fail(SWA_ERR_UNSUPPORTED, "num_kv_heads * row tiles exceeds the grid limit");
+    return SWA_OK;
+}
+
+struct Plan {
+    int kernel;       // 1 = SIMT
+    int rpw, nrg;     // SIMT row layout
+    int rows_per_tile, row_tiles;
+    int splits, chunk;
+    long long workspace;
+    long long grid;
+};
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+// Split heuristic: enough CTAs to cover every SM about twice, never a chunk
+// shorter than one 32-key tile, at most kMaxSplits chunks.  Chunks are
+// multiples of 16 keys.  Host-only: seq_lens live on the device, so the
+// worst-case span W + q_len - 1 (bounded by the cache length) is used.
+Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
+    Plan p{};
+    const int G = d->num_q_heads / d->num_kv_heads;
+    const int R = d->q_len * G;
+    p.kernel = 1;
+    if (R <= 4) { p.rpw = 4; p.nrg = 1; }
+    else if (R <= 8) { p.rpw = 8; p.nrg = 1; }
+    else if (R <= 16) { p.rpw = 8; p.nrg = 2; }
+    else { p.rpw = 8; p.nrg = 4; }
+    p.rows_per_tile = p.rpw * p.nrg;
+    p.row_tiles = ceil_div(R, p.rows_per_tile);
+    long long span = (long long)window + d->q_len - 1;
+    if (span > d->max_len) span = d->max_len;
+    if (span < 1) span = 1;
+    const long long units = (long long)d->batch * d->num_kv_heads * p.row_tiles;
+    int splits;
+    if (d->num_splits > 0) {
+        splits = d->num_splits;
+    } else {
+        const long long target = 2LL * (num_sms > 0 ? num_sms : 148);
+        long long s = (target + units - 1) / units;
+        const long long by_len = (span + swa::kSimtTileKeys - 1) / swa::kSimtTileKeys;
+        if (s > by_len) s = by_len;
+        splits = (int)s;
+    }
+    if (splits < 1) splits = 1;
+    if (splits > kMaxSplits) splits = kMaxSplits;
+    long long chunk = (span + splits - 1) / splits;
+    if (d->num_splits == 0) chunk = (chunk + 15) / 16 * 16;
+    if (chunk < 1) chunk = 1;
+    splits = ceil_div(span, chunk);
+    p.splits = splits;
+    p.chunk = (int)chunk;
+    p.grid = (long long)splits * d->num_kv_heads * p.row_tiles * d->batch;
+    p.workspace = splits > 1 ? (long long)d->batch * d->num_kv_heads * splits * R *
+                                   ((long long)d->head_dim + 2) * 4
+                             : 0;
+    return p;
+}
+
+// ------------------------------------------------------------- workspace
+
+struct Workspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+    bool owned = false;
+};
+std::mutex g_ws_mutex;
+Workspace g_ws[kMaxDevices];
+
+swa_status ensure_workspace(int dev, size_t need, cudaStream_t stream, void **out) {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    Workspace &w = g_ws[dev];
+    if (w.bytes >= need) {
+        *out = w.ptr;
+        return SWA_OK;
+    }
+    if (!w.owned && w.ptr != nullptr)
+        return fail(SWA_ERR_WORKSPACE, "workspace set by the caller holds %zu bytes, %zu needed",
+                    w.bytes, need);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+    if (cap != cudaStreamCaptureStatusNone)
+        return fail(SWA_ERR_WORKSPACE,
+                    "stream is capturing and the workspace (%zu bytes) is below the %zu needed; "
+                    "run one call outside capture first or set a workspace",
+                    w.bytes, need);
+    if (w.ptr) {
+        e = cudaFree(w.ptr);
+        w.ptr = nullptr;
+        w.bytes = 0;
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+    }
+    size_t grow = need + need / 4;
+    e = cudaMalloc(&w.ptr, grow);
+    if (e != cudaSuccess) {
+        w.ptr = nullptr;
+        return cuda_fail(e, "cudaMalloc(workspace)");
+    }
+    w.bytes = grow;
+    w.owned = true;
+    *out = w.ptr;
+    return SWA_OK;
+}
+
+template <int D, int RPW, int NRG>
+cudaError_t launch_simt(const swa::AttnParams &P, cudaStream_t stream) {
+    using C = swa::SimtCfg<D, RPW, NRG>;
+    auto kern = swa::swa_simt_kernel<D, RPW, NRG>;
+    static bool attr_done[kMaxDevices] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (!attr_done[dev]) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    dim3 grid(P.splits, P.Hkv * P.row_tiles, P.B);
+    kern<<<grid, swa::kSimtThreads, C::SMEM_BYTES, stream>>>(P);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_simt_d(const Plan &pl, const swa::AttnParams &P, cudaStream_t s) {
+    if (pl.rpw == 4) return launch_simt<D, 4, 1>(P, s);
+    if (pl.nrg == 1) return launch_simt<D, 8, 1>(P, s);
+    if (pl.nrg == 2) return launch_simt<D, 8, 2>(P, s);
+    return launch_simt<D, 8, 4>(P, s);
+}
+
+template <int D>
+cudaError_t launch_merge(const swa::AttnParams &P, cudaStream_t s) {
+    const long long threads = (long long)P.B * P.Hkv * P.R * (D / 8);
+    const long long blocks = (threads + 255) / 256;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    swa::swa_merge_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(P);
+    return cudaGetLastError();
+}
+
+uint32_t *fault_word_ptr(int dev) {
+    static uint32_t *cache[kMaxDevices] = {};
+    if (cache[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_fault_word) != cudaSuccess) return nullptr;
+        cache[dev] = static_cast<uint32_t *>(p);
+    }
+    return cache[dev];
+}
+
+int device_sms(int dev) {
+    static int cache[kMaxDevices] = {};
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+swa_status swa_verify_attn(const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *seq_lens, const int32_t *q_pos, int32_t window,
+                           float scale, void *out, float *lse, const swa_dims *dims,
+                           swa_stream_t stream) {
+    swa_status st = validate_dims(dims, window);
+    if (st != SWA_OK) return st;
+    if (!q || !k_cache || !v_cache || !seq_lens || !q_pos || !out)
+        return fail(SWA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return fail(SWA_ERR_INVALID_ARG, "q, k_cache, v_cache and out must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(seq_lens) & 3u) || (reinterpret_cast<uintptr_t>(q_pos) & 3u) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(SWA_ERR_INVALID_ARG, "seq_lens, q_pos and lse must be 4-byte aligned");
+    if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
+        return fail(SWA_ERR_INVALID_ARG, "scale must be finite");
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev >= kMaxDevices) return fail(SWA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+
+    uint32_t *fault = fault_word_ptr(dev);
+    if (fault == nullptr) return fail(SWA_ERR_CUDA, "cannot resolve the device fault word");
+    const Plan pl = make_plan(dims, window, device_sms(dev));
+    swa::AttnParams P{};
+    P.q = static_cast<const __nv_bfloat16 *>(q);
+    P.k = static_cast<const __nv_bfloat16 *>(k_cache);
+    P.v = static_cast<const __nv_bfloat16 *>(v_cache);
+    P.seq_lens = seq_lens;
+    P.q_pos = q_pos;
+    P.out = static_cast<__nv_bfloat16 *>(out);
+    P.lse = lse;
+    P.B = dims->batch;
+    P.q_len = dims->q_len;
+    P.Hq = dims->num_q_heads;
+    P.Hkv = dims->num_kv_heads;
+    P.G = dims->num_q_heads / dims->num_kv_heads;
+    P.L = dims->max_len;
+    P.window = window;
+    P.R = P.q_len * P.G;
+    P.splits = pl.splits;
+    P.chunk = pl.chunk;
+    P.row_tiles = pl.row_tiles;
+    P.rows_per_tile = pl.rows_per_tile;
+    P.qk_scale = scale * swa::kLog2e;
+    P.fault = fault;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (pl.splits > 1) {
+        void *ws = nullptr;
+        st = ensure_workspace(dev, (size_t)pl.workspace, s, &ws);
+        if (st != SWA_OK) return st;
+        P.part_acc = static_cast<float *>(ws);
+        P.part_ml = P.part_acc + (size_t)P.B * P.Hkv * P.splits * P.R * dims->head_dim;
+    }
+    switch (dims->head_dim) {
+        case 64: e = launch_simt_d<64>(pl, P, s); break;
+        case 128: e = launch_simt_d<128>(pl, P, s); break;
+        default: e = launch_simt_d<256>(pl, P, s); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
+    if (pl.splits > 1) {
+        switch (dims->head_dim) {
+            case 64: e = launch_merge<64>(P, s); break;
+            case 128: e = launch_merge<128>(P, s); break;
+            default: e = launch_merge<256>(P, s); break;
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+    }
+    t_last_error[0] = '\0';
+    return SWA_OK;
+}
+
+size_t swa_workspace_bytes(const swa_dims *dims, int32_t window) {
+    if (validate_dims(dims, window) != SWA_OK) return 0;
+    // the largest split count any device could get: the plan for a 1-SM part
+    // is not larger than kMaxSplits chunks of one tile each
+    const int G = dims->num_q_heads / dims->num_kv_heads;
+    const long long R = (long long)dims->q_len * G;
+    long long span = (long long)window + dims->q_len - 1;
+    if (span > dims->max_len) span = dims->max_len;
+    long long splits;
+    if (dims->num_splits > 0) {
+        splits = dims->num_splits > kMaxSplits ? kMaxSplits : dims->num_splits;
+    } else {
+        splits = (span + swa::kSimtTileKeys - 1) / swa::kSimtTileKeys;
+        if (splits > kMaxSplits) splits = kMaxSplits;
+    }
+    if (splits <= 1) return 0;
+    return (size_t)dims->batch * dims->num_kv_heads * splits * R * (dims->head_dim + 2) * 4;
+}
+
+swa_status swa_set_workspace(void *dev_ptr, size_t bytes) {
+    if ((dev_ptr == nullptr) != (bytes == 0))
+        return fail(SWA_ERR_INVALID_ARG, "dev_ptr and bytes must be both set or both zero");
+    if (dev_ptr && !aligned16(dev_ptr))
+        return fail(SWA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev >= kMaxDevices) return fail(SWA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    Workspace &w = g_ws[dev];
+    if (w.owned && w.ptr) {
+        e = cudaFree(w.ptr);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+    }
+    w.ptr = dev_ptr;
+    w.bytes = bytes;
+    w.owned = false;
+    return SWA_OK;
+}
+
+swa_status swa_release_workspace(void) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev >= kMaxDevices) return fail(SWA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    Workspace &w = g_ws[dev];
+    if (w.owned && w.ptr) {
+        e = cudaFree(w.ptr);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+        w = Workspace{};
+    }
+    return SWA_OK;
+}
+
+swa_status swa_plan(const swa_dims *dims, int32_t window, int32_t num_sms, swa_plan_info *plan) {
+    swa_status st = validate_dims(dims, window);
+    if (st != SWA_OK) return st;
+    if (plan == nullptr) return fail(SWA_ERR_INVALID_ARG, "plan is NULL");
+    if (num_sms < 1) return fail(SWA_ERR_INVALID_ARG, "num_sms %d < 1", num_sms);
+    const Plan p = make_plan(dims, window, num_sms);
+    plan->kernel = p.kernel;
+    plan->num_splits = p.splits;
+    plan->chunk_keys = p.chunk;
+    plan->row_tiles = p.row_tiles;
+    plan->rows_per_tile = p.rows_per_tile;
+    plan->grid_ctas = (int32_t)p.grid;
+    plan->merge = p.splits > 1 ? 1 : 0;
+    plan->workspace_bytes = p.workspace;
+    return SWA_OK;
+}
+
+const char *swa_last_error(void) { return t_last_error; }
+
+swa_status swa_read_device_errors(uint32_t *flags) {
+    if (flags == nullptr) return fail(SWA_ERR_INVALID_ARG, "flags is NULL");
+    uint32_t v = 0, zero = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    e = cudaMemcpyFromSymbol(&v, g_fault_word, sizeof v);
+    if (e != cudaSuccess) return cuda_fail(e, "read fault word");
+    e = cudaMemcpyToSymbol(g_fault_word, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "clear fault word");
+    *flags = v;
+    return SWA_OK;
+}
+
+const char *swa_version(void) { return "swa 0.1.0 sm_103a"; }
+
+}  // extern "C"

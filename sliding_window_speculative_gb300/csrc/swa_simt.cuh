@@ -1,0 +1,417 @@
+// CUDA-core split-KV chunk kernel for sliding-window verify attention.
+//
+// One CTA = one (chunk of the window span, KV head, row tile, sequence).
+// The K and V rows of the chunk stream through a ring of shared-memory
+// stages, each filled by two bulk copies on the TMA engine (a sequence's
+// rows of one KV head are contiguous, so a tile of keys is one contiguous
+// block).  Four warps split the CTA's packed query rows (the G query heads
+// of the KV head times the q_len draft rows, so each K/V byte is read once
+// per KV head) and/or the keys of each tile.  Scores, an online softmax in
+// the log2 domain and the PV accumulation run in fp32 on the CUDA cores:
+//
+//   lanes split head_dim; a lane holds RPW query rows x D/32 dims in
+//   registers; for every group of 32/RPW keys the 32 (key, row) partial
+//   dot products are summed across the warp with a reduce-scatter
+//   butterfly (31 shuffles) that leaves one finished score per lane.
+//
+// The chunk's result is either the final output (one chunk per sequence)
+// or a partial (m, l, acc) for the log-sum-exp merge kernel.
+#pragma once
+
+#include "swa_common.cuh"
+
+namespace swa {
+
+constexpr int kSimtThreads = 128;
+constexpr int kSimtTileKeys = 32;
+
+struct AttnParams {
+    const __nv_bfloat16 *q;
+    const __nv_bfloat16 *k;
+    const __nv_bfloat16 *v;
+    const int32_t *seq_lens;
+    const int32_t *q_pos;
+    __nv_bfloat16 *out;
+    float *lse;
+    float *part_acc;  // [B*Hkv, splits, R, D]  (splits > 1)
+    float *part_ml;   // [B*Hkv, splits, R, 2]
+    uint32_t *fault;  // device fault word (bounded waits that gave up)
+    int B, q_len, Hq, Hkv, G, L, window, R;
+    int splits, chunk, row_tiles, rows_per_tile;
+    float qk_scale;   // scale * log2(e)
+};
+
+// Key range [c_lo, c_hi) of chunk `split` of sequence b's window span,
+// clamped to the sequence's own slab [0, L).
+struct ChunkRange {
+    int lo, hi;   // whole span, hi exclusive
+    int c_lo, c_hi;
+    int qp;       // q_pos of the sequence
+};
+
+__device__ __forceinline__ ChunkRange chunk_range(const AttnParams &P, int b, int split) {
+    ChunkRange c;
+    const long long qp = P.q_pos[b];
+    const long long sl = P.seq_lens[b];
+    long long hi = qp + P.q_len;
+    if (hi > sl) hi = sl;
+    if (hi > P.L) hi = P.L;
+    if (hi < 0) hi = 0;
+    long long lo = qp - P.window + 1;
+    if (lo < 0) lo = 0;
+    if (lo > hi) lo = hi;
+    long long clo = lo + (long long)split * P.chunk;
+    long long chi = clo + P.chunk;
+    if (clo > hi) clo = hi;
+    if (chi > hi) chi = hi;
+    c.lo = (int)lo;
+    c.hi = (int)hi;
+    c.c_lo = (int)clo;
+    c.c_hi = (int)chi;
+    c.qp = (int)(qp < -(1LL << 30) ? -(1LL << 30) : (qp > (1LL << 30) ? (1LL << 30) : qp));
+    return c;
+}
+
+template <int D>
+__device__ __forceinline__ void load_row_f32(const __nv_bfloat16 *src, float *dst) {
+    // D/32 consecutive bf16 of one row owned by this lane.
+    constexpr int DPL = D / 32;
+    if constexpr (DPL == 8) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(src);
+        dst[0] = bf16lo(w.x); dst[1] = bf16hi(w.x);
+        dst[2] = bf16lo(w.y); dst[3] = bf16hi(w.y);
+        dst[4] = bf16lo(w.z); dst[5] = bf16hi(w.z);
+        dst[6] = bf16lo(w.w); dst[7] = bf16hi(w.w);
+    } else if constexpr (DPL == 4) {
+        const uint2 w = *reinterpret_cast<const uint2 *>(src);
+        dst[0] = bf16lo(w.x); dst[1] = bf16hi(w.x);
+        dst[2] = bf16lo(w.y); dst[3] = bf16hi(w.y);
+    } else {
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(src);
+        dst[0] = bf16lo(w); dst[1] = bf16hi(w);
+    }
+}
+
+// Reduce-scatter of 32 per-lane values: afterwards lane l holds
+// sum over all lanes of v[l].  v is consumed.
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int half = 16; half >= 1; half >>= 1) {
+        const bool upper = (lane & half) != 0;
+#pragma unroll
+        for (int e = 0; e < half; ++e) {
+            const float keep = upper ? v[e + half] : v[e];
+            const float give = upper ? v[e] : v[e + half];
+            v[e] = keep + __shfl_xor_sync(0xffffffffu, give, half);
+        }
+    }
+    return v[0];
+}
+
+template <int D, int RPW, int NRG>
+struct SimtCfg {
+    static constexpr int NKG = 4 / NRG;                 // key groups (warps per row group)
+    static constexpr int RPT = RPW * NRG;               // packed rows per CTA
+    static constexpr int DPL = D / 32;                  // dims per lane
+    static constexpr int KPG = 32 / RPW;                // keys per butterfly group
+    static constexpr int KB = kSimtTileKeys / NKG;      // keys per warp per tile
+    static constexpr int NG = KB / KPG;                 // butterfly groups per warp per tile
+    static constexpr int STAGES = D == 256 ? 3 : 4;
+    static constexpr int TILE_BYTES = kSimtTileKeys * D * 2;         // one of K or V
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int COMB_BYTES = NKG * RPT * D * 4 + NKG * RPT * 2 * 4;
+    static constexpr int MAIN_BYTES = RING_BYTES > COMB_BYTES ? RING_BYTES : COMB_BYTES;
+    static constexpr int PBUF_BYTES = 4 * KB * RPW * 4;
+    static constexpr int SMEM_BYTES = MAIN_BYTES + PBUF_BYTES + STAGES * 8;
+    static_assert(KB % KPG == 0, "key block must hold whole butterfly groups");
+};
+
+template <int D, int RPW, int NRG>
+__global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams P) {
+    using C = SimtCfg<D, RPW, NRG>;
+    constexpr int DPL = C::DPL;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *ring = smem;
+    float *pbuf_all = reinterpret_cast<float *>(smem + C::MAIN_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::MAIN_BYTES + C::PBUF_BYTES);
+
+    const int split = blockIdx.x;
+    const int h = blockIdx.y / P.row_tiles;
+    const int rt = blockIdx.y % P.row_tiles;
+    const int b = blockIdx.z;
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int rg = warp % NRG, kg = warp / NRG;
+    float *pbuf = pbuf_all + warp * (C::KB * RPW);
+
+    const ChunkRange cr = chunk_range(P, b, split);
+    const int n_keys = cr.c_hi - cr.c_lo;
+    const int n_tiles = n_keys > 0 ? (n_keys + kSimtTileKeys - 1) / kSimtTileKeys : 0;
+
+    const size_t slab = ((size_t)b * P.Hkv + h) * (size_t)P.L;  // first row of this (b, h)
+    const __nv_bfloat16 *kslab = P.k + slab * D;
+    const __nv_bfloat16 *vslab = P.v + slab * D;
+
+    if (tid == 0) {
+        for (int s = 0; s < C::STAGES; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    auto issue = [&](int t) {
+        const int s = t % C::STAGES;
+        const int j0 = cr.c_lo + t * kSimtTileKeys;
+        const int n = min(kSimtTileKeys, cr.c_hi - j0);
+        const uint32_t bytes = (uint32_t)n * D * 2;
+        uint8_t *dst = ring + s * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full[s], 2 * bytes);
+        bulk_copy_g2s(dst, kslab + (size_t)j0 * D, bytes, &full[s]);
+        bulk_copy_g2s(dst + C::TILE_BYTES, vslab + (size_t)j0 * D, bytes, &full[s]);
+    };
+    if (tid == 0) {
+        for (int t = 0; t < C::STAGES - 1 && t < n_tiles; ++t) issue(t);
+    }
+
+    // ---- this lane's query rows (pre-scaled into the log2 domain)
+    const int row0 = rt * C::RPT + rg * RPW;  // first packed row of this warp
+    float qf[RPW][DPL];
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) {
+        const int r = row0 + rr;
+        if (r < P.R) {
+            const int i = r / P.G, gg = r - (r / P.G) * P.G;
+            const __nv_bfloat16 *src =
+                P.q + (((size_t)b * P.q_len + i) * P.Hq + (size_t)h * P.G + gg) * D + lane * DPL;
+            load_row_f32<D>(src, qf[rr]);
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) qf[rr][d] *= P.qk_scale;
+        } else {
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) qf[rr][d] = 0.f;
+        }
+    }
+
+    // ---- the row whose finished scores this lane holds after a butterfly
+    const int r_own = row0 + (lane % RPW);
+    int jlo_own = 1, jhi_own = 0;  // inclusive, empty by default
+    if (r_own < P.R) {
+        const int p = cr.qp + r_own / P.G;
+        jlo_own = max(max(cr.c_lo, p - P.window + 1), 0);
+        jhi_own = min(p, cr.c_hi - 1);
+    }
+
+    float m_own = NEG_INF, l_own = 0.f;
+    float acc[RPW][DPL];
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) acc[rr][d] = 0.f;
+
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+        if (tid == 0 && t + C::STAGES - 1 < n_tiles) {
+            fence_proxy_async_smem();
+            issue(t + C::STAGES - 1);
+        }
+        const int s = t % C::STAGES;
+        if (!mbar_wait_bounded(&full[s], (t / C::STAGES) & 1, P.fault, kFaultCopyTimeout)) {
+            ok = false;
+            break;
+        }
+        const __nv_bfloat16 *Ks = reinterpret_cast<const __nv_bfloat16 *>(ring + s * C::STAGE_BYTES);
+        const __nv_bfloat16 *Vs = Ks + kSimtTileKeys * D;
+        const int j0 = cr.c_lo + t * kSimtTileKeys;
+        const int n = min(kSimtTileKeys, cr.c_hi - j0);
+        const int kb0 = kg * C::KB;
+
+        // scores of this warp's key block: one finished (key, row) per lane per group
+        float sc[C::NG];
+#pragma unroll
+        for (int grp = 0; grp < C::NG; ++grp) {
+            float v[32];
+#pragma unroll
+            for (int kk = 0; kk < C::KPG; ++kk) {
+                float kf[DPL];
+                load_row_f32<D>(Ks + (size_t)(kb0 + grp * C::KPG + kk) * D + lane * DPL, kf);
+#pragma unroll
+                for (int rr = 0; rr < RPW; ++rr) {
+                    float a = 0.f;
+#pragma unroll
+                    for (int d = 0; d < DPL; ++d) a = fmaf(qf[rr][d], kf[d], a);
+                    v[kk * RPW + rr] = a;
+                }
+            }
+            const float red = warp_reduce_scatter32(v);
+            const int j = j0 + kb0 + grp * C::KPG + lane / RPW;
+            sc[grp] = (j >= jlo_own && j <= jhi_own) ? red : NEG_INF;
+        }
+
+        // online softmax for the row this lane holds
+        float tmax = sc[0];
+#pragma unroll
+        for (int grp = 1; grp < C::NG; ++grp) tmax = fmaxf(tmax, sc[grp]);
+#pragma unroll
+        for (int off = RPW; off < 32; off <<= 1)
+            tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+        const float m_new = fmaxf(m_own, tmax);
+        const float m_use = m_new == NEG_INF ? 0.f : m_new;
+        const float alpha = fast_exp2(m_own - m_use);
+        float psum = 0.f;
+#pragma unroll
+        for (int grp = 0; grp < C::NG; ++grp) {
+            const float pv = fast_exp2(sc[grp] - m_use);
+            psum += pv;
+            pbuf[grp * 32 + lane] = pv;  // = pbuf[key_in_block * RPW + row]
+        }
+#pragma unroll
+        for (int off = RPW; off < 32; off <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+        l_own = l_own * alpha + psum;
+        m_own = m_new;
+        __syncwarp();
+
+        // rescale and accumulate P V
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr) {
+            const float a = __shfl_sync(0xffffffffu, alpha, rr);
+#pragma unroll
+            for (int d = 0; d < DPL; ++d) acc[rr][d] *= a;
+        }
+        const int kmax = min(C::KB, n - kb0);  // keys past the tile's end hold stale data
+        for (int kk = 0; kk < kmax; ++kk) {
+            float vf[DPL];
+            load_row_f32<D>(Vs + (size_t)(kb0 + kk) * D + lane * DPL, vf);
+            float pr[RPW];
+            if constexpr (RPW == 4) {
+                const float4 p4 = *reinterpret_cast<const float4 *>(pbuf + kk * 4);
+                pr[0] = p4.x; pr[1] = p4.y; pr[2] = p4.z; pr[3] = p4.w;
+            } else {
+                const float4 a4 = *reinterpret_cast<const float4 *>(pbuf + kk * 8);
+                const float4 b4 = *reinterpret_cast<const float4 *>(pbuf + kk * 8 + 4);
+                pr[0] = a4.x; pr[1] = a4.y; pr[2] = a4.z; pr[3] = a4.w;
+                pr[4] = b4.x; pr[5] = b4.y; pr[6] = b4.z; pr[7] = b4.w;
+            }
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+                for (int d = 0; d < DPL; ++d) acc[rr][d] = fmaf(pr[rr], vf[d], acc[rr][d]);
+        }
+        __syncthreads();  // stage s and pbuf free for reuse
+    }
+    if (!ok) return;  // a copy never landed; the fault word is set
+
+    // ---- combine the key groups of each row group, then write out
+    float *comb_acc = reinterpret_cast<float *>(ring);
+    float *comb_ml = comb_acc + C::NKG * C::RPT * D;
+    __syncthreads();
+#pragma unroll
+    for (int rr = 0; rr < RPW; ++rr) {
+        float *dst = comb_acc + ((size_t)kg * C::RPT + rg * RPW + rr) * D + lane * DPL;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) dst[d] = acc[rr][d];
+    }
+    if (lane < RPW) {
+        float *ml = comb_ml + ((size_t)kg * C::RPT + rg * RPW + lane) * 2;
+        ml[0] = m_own;
+        ml[1] = l_own;
+    }
+    __syncthreads();
+
+    constexpr int CPR = D / 8;  // 8-dim chunks per row
+    for (int idx = tid; idx < C::RPT * CPR; idx += kSimtThreads) {
+        const int rloc = idx / CPR, dc = idx % CPR;
+        const int r = rt * C::RPT + rloc;
+        if (r >= P.R) continue;
+        float M = NEG_INF;
+#pragma unroll
+        for (int q = 0; q < C::NKG; ++q) M = fmaxf(M, comb_ml[((size_t)q * C::RPT + rloc) * 2]);
+        float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float Lam = 0.f;
+        if (M != NEG_INF) {
+#pragma unroll
+            for (int q = 0; q < C::NKG; ++q) {
+                const float mq = comb_ml[((size_t)q * C::RPT + rloc) * 2];
+                const float w = fast_exp2(mq - M);
+                Lam += w * comb_ml[((size_t)q * C::RPT + rloc) * 2 + 1];
+                const float *a = comb_acc + ((size_t)q * C::RPT + rloc) * D + dc * 8;
+#pragma unroll
+                for (int d = 0; d < 8; ++d) o[d] = fmaf(w, a[d], o[d]);
+            }
+        }
+        const int i = r / P.G, gg = r - (r / P.G) * P.G;
+        const size_t orow = ((size_t)b * P.q_len + i) * P.Hq + (size_t)h * P.G + gg;
+        if (P.splits == 1) {
+            const float inv = Lam > 0.f ? 1.f / Lam : 0.f;
+            uint4 w;
+            w.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+            w.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+            w.z = pack_bf16x2(o[4] * inv, o[5] * inv);
+            w.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+            *reinterpret_cast<uint4 *>(P.out + orow * D + dc * 8) = w;
+            if (dc == 0 && P.lse != nullptr)
+                P.lse[orow] = Lam > 0.f ? (M + __log2f(Lam)) * kLn2 : NEG_INF;
+        } else {
+            const size_t prow = (((size_t)b * P.Hkv + h) * P.splits + split) * P.R + r;
+            float4 *dst = reinterpret_cast<float4 *>(P.part_acc + prow * D + dc * 8);
+            dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+            if (dc == 0) {
+                P.part_ml[prow * 2] = M;
+                P.part_ml[prow * 2 + 1] = Lam;
+            }
+        }
+    }
+}
+
+// Log-sum-exp merge of the split partials of every packed row:
+//   M = max_s m_s, Lambda = sum_s l_s 2^(m_s - M),
+//   out = sum_s acc_s 2^(m_s - M) / Lambda, lse = (M + log2 Lambda) ln 2.
+// One thread per (row, 8 dims).
+template <int D>
+__global__ void __launch_bounds__(256) swa_merge_kernel(const AttnParams P) {
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    constexpr int CPR = D / 8;
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long rows = (long long)P.B * P.Hkv * P.R;
+    if (idx >= rows * CPR) return;
+    const long long grow = idx / CPR;  // (b*Hkv + h) * R + r
+    const int dc = (int)(idx % CPR);
+    const long long bh = grow / P.R;
+    const int r = (int)(grow % P.R);
+    const int b = (int)(bh / P.Hkv), h = (int)(bh % P.Hkv);
+    const size_t base = (size_t)bh * P.splits * P.R + r;  // split s at base + s*R
+    float M = NEG_INF;
+    for (int s = 0; s < P.splits; ++s) M = fmaxf(M, P.part_ml[(base + (size_t)s * P.R) * 2]);
+    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float Lam = 0.f;
+    if (M != NEG_INF) {
+        for (int s = 0; s < P.splits; ++s) {
+            const size_t prow = base + (size_t)s * P.R;
+            const float ms = P.part_ml[prow * 2];
+            if (ms == NEG_INF) continue;
+            const float w = fast_exp2(ms - M);
+            Lam += w * P.part_ml[prow * 2 + 1];
+            const float4 *a = reinterpret_cast<const float4 *>(P.part_acc + prow * D + dc * 8);
+            const float4 a0 = a[0], a1 = a[1];
+            o[0] = fmaf(w, a0.x, o[0]); o[1] = fmaf(w, a0.y, o[1]);
+            o[2] = fmaf(w, a0.z, o[2]); o[3] = fmaf(w, a0.w, o[3]);
+            o[4] = fmaf(w, a1.x, o[4]); o[5] = fmaf(w, a1.y, o[5]);
+            o[6] = fmaf(w, a1.z, o[6]); o[7] = fmaf(w, a1.w, o[7]);
+        }
+    }
+    const float inv = Lam > 0.f ? 1.f / Lam : 0.f;
+    const int i = r / P.G, gg = r % P.G;
+    const size_t orow = ((size_t)b * P.q_len + i) * P.Hq + (size_t)h * P.G + gg;
+    uint4 w;
+    w.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+    w.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+    w.z = pack_bf16x2(o[4] * inv, o[5] * inv);
+    w.w = pack_bf16x2(o[6] * inv, o[7] * inv);
+    *reinterpret_cast<uint4 *>(P.out + orow * D + dc * 8) = w;
+    if (dc == 0 && P.lse != nullptr) P.lse[orow] = Lam > 0.f ? (M + __log2f(Lam)) * kLn2 : NEG_INF;
+}
+
+}  // namespace swa

@@ -1,0 +1,136 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry
+point include/swa.h declares, rejects bad arguments before touching CUDA,
+and its split plan / workspace arithmetic hold their invariants."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sliding_window_speculative_gb300 as swa
+from sliding_window_speculative_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "swa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return swa.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(swa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("swa_verify_attn", "swa_workspace_bytes", "swa_set_workspace",
+                     "swa_last_error"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in swa.h but not exported"
+
+
+def test_binding_uses_the_c_names():
+    for name in declared_functions():
+        assert hasattr(swa, name), f"binding lacks {name}"
+
+
+def test_version(lib):
+    assert "sm_103a" in swa.swa_version()
+
+
+def _call_raw(lib, dims, window=188, q=16, k=32, v=48, sl=64, qp=128, out=256, lse=None,
+              scale=0.0625):
+    d = swa.make_dims(*dims) if isinstance(dims, tuple) else dims
+    return lib.swa_verify_attn(q, k, v, sl, qp, window, scale, out, lse,
+                               ctypes.byref(d) if d is not None else None, None)
+
+
+GOOD = (2, 8, 8, 2, 256, 4096, 0)
+
+
+@pytest.mark.parametrize("dims,window,code", [
+    ((0, 8, 8, 2, 256, 4096, 0), 188, swa.SWA_ERR_INVALID_ARG),     # batch 0
+    ((2, 0, 8, 2, 256, 4096, 0), 188, swa.SWA_ERR_INVALID_ARG),     # q_len 0
+    ((2, 65, 8, 2, 256, 4096, 0), 188, swa.SWA_ERR_INVALID_ARG),    # q_len > 64
+    ((2, 8, 8, 3, 256, 4096, 0), 188, swa.SWA_ERR_INVALID_ARG),     # Hq % Hkv
+    ((2, 8, 8, 0, 256, 4096, 0), 188, swa.SWA_ERR_INVALID_ARG),     # Hkv 0
+    ((2, 8, 8, 2, 96, 4096, 0), 188, swa.SWA_ERR_UNSUPPORTED),      # head_dim
+    ((2, 8, 8, 2, 256, 0, 0), 188, swa.SWA_ERR_INVALID_ARG),        # max_len
+    ((2, 8, 8, 2, 256, 4096, -1), 188, swa.SWA_ERR_INVALID_ARG),    # splits
+    (GOOD, 0, swa.SWA_ERR_INVALID_ARG),                              # window 0
+    ((2, 64, 512, 1, 256, 4096, 0), 188, swa.SWA_ERR_UNSUPPORTED),  # R > 4096
+])
+def test_invalid_dims_rejected_before_cuda(lib, dims, window, code):
+    assert _call_raw(lib, dims, window) == code
+    assert swa.swa_last_error() != ""
+
+
+def test_null_and_misaligned_pointers(lib):
+    assert _call_raw(lib, None) == swa.SWA_ERR_INVALID_ARG
+    assert _call_raw(lib, GOOD, q=None) == swa.SWA_ERR_INVALID_ARG
+    assert _call_raw(lib, GOOD, out=None) == swa.SWA_ERR_INVALID_ARG
+    assert _call_raw(lib, GOOD, k=40) == swa.SWA_ERR_INVALID_ARG     # 8-byte aligned only
+    assert _call_raw(lib, GOOD, sl=66) == swa.SWA_ERR_INVALID_ARG    # int32 misaligned
+    assert _call_raw(lib, GOOD, scale=float("nan")) == swa.SWA_ERR_INVALID_ARG
+    assert _call_raw(lib, GOOD, scale=float("inf")) == swa.SWA_ERR_INVALID_ARG
+
+
+def test_workspace_bytes(lib):
+    d = swa.make_dims(*GOOD)
+    assert swa.swa_workspace_bytes(d, 188) > 0
+    assert swa.swa_workspace_bytes(swa.make_dims(0, 8, 8, 2, 256, 4096), 188) == 0
+    one = swa.make_dims(2, 8, 8, 2, 256, 4096, 1)
+    assert swa.swa_workspace_bytes(one, 188) == 0
+
+
+@pytest.mark.parametrize("B,q_len,Hq,Hkv,D,L,W", [
+    (1, 8, 8, 2, 256, 4096, 188), (1, 1, 8, 2, 256, 4096, 188), (1, 1, 8, 2, 256, 4096, 4096),
+    (64, 8, 8, 2, 256, 4096, 188), (512, 64, 8, 2, 256, 32768, 1024), (1, 1, 2, 1, 64, 40, 16),
+    (3, 64, 16, 2, 256, 1024, 188), (7, 5, 6, 2, 128, 300, 5000),
+])
+@pytest.mark.parametrize("sms", [1, 148, 152])
+def test_plan_invariants(lib, B, q_len, Hq, Hkv, D, L, W, sms):
+    dims = swa.make_dims(B, q_len, Hq, Hkv, D, L)
+    p = swa.swa_plan(dims, W, sms)
+    span = min(W + q_len - 1, L)
+    R = q_len * Hq // Hkv
+    assert 1 <= p["num_splits"] <= 64
+    assert p["num_splits"] * p["chunk_keys"] >= span               # chunks cover the span
+    assert (p["num_splits"] - 1) * p["chunk_keys"] < span          # no empty trailing chunk
+    assert p["row_tiles"] * p["rows_per_tile"] >= R
+    assert p["grid_ctas"] == p["num_splits"] * Hkv * p["row_tiles"] * B
+    assert p["merge"] == (1 if p["num_splits"] > 1 else 0)
+    assert p["workspace_bytes"] <= swa.swa_workspace_bytes(dims, W)
+    if p["num_splits"] > 1:
+        assert p["workspace_bytes"] == B * Hkv * p["num_splits"] * R * (D + 2) * 4
+
+
+def test_plan_forced_splits(lib):
+    dims = swa.make_dims(1, 8, 8, 2, 256, 4096, 5)
+    p = swa.swa_plan(dims, 188, 152)
+    assert p["num_splits"] == 5 and p["chunk_keys"] == 39
+    dims = swa.make_dims(1, 8, 8, 2, 256, 4096, 500)
+    assert swa.swa_plan(dims, 188, 152)["num_splits"] <= 64
+
+
+def test_plan_fills_the_gpu_for_one_sequence(lib):
+    p = swa.swa_plan(swa.make_dims(1, 8, 8, 2, 256, 4096), 188, 152)
+    assert p["num_splits"] > 1
+
+
+def test_binding_rejects_cpu_tensors(lib):
+    import torch
+    q = torch.zeros(1, 8, 8, 256, dtype=torch.bfloat16)
+    k = torch.zeros(1, 2, 64, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        swa.swa_verify_attn(q, k, k, torch.zeros(1, dtype=torch.int32),
+                            torch.zeros(1, dtype=torch.int32), 188, 0.0625)
