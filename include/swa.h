@@ -144,6 +144,42 @@ swa_status swa_read_device_errors(uint32_t *flags);
 /* Library version, e.g. "swa 0.1.0 sm_103a". */
 const char *swa_version(void);
 
+/* Bytes of the fixed device scratch used by swa_verify_attn_noalloc. */
+#define SWA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/* Allocation-free variant of swa_verify_attn (no counterpart on the pages:
+ * it serves callers, not the method).
+ *
+ * Some callers must not allocate device memory at call time: an engine that
+ * reserves (nearly) all GPU memory for its own pool at start-up, a plugin
+ * that is only handed pointers by a host framework owning every allocation,
+ * or a latency-critical path that cannot afford cudaMalloc's implicit device
+ * synchronisation.  This entry point never calls cudaMalloc, cudaFree or any
+ * allocating routine.  When the plan splits the keys into several chunks,
+ * the split partials go to a fixed scratch array of
+ * SWA_NOALLOC_SCRATCH_BYTES (16 MiB) that the library declares statically;
+ * every GPU on which the library's kernels are loaded holds that array until
+ * the process exits.
+ *
+ * Arguments, layouts, preconditions and results are those of
+ * swa_verify_attn; the caller still owns and passes every input and output.
+ * Differences:
+ *  - If the chosen plan needs more scratch than SWA_NOALLOC_SCRATCH_BYTES
+ *    (see swa_plan(): workspace_bytes), the call returns SWA_ERR_WORKSPACE
+ *    with a message naming both sizes and launches nothing; a smaller
+ *    dims->num_splits (1 needs no scratch) brings it under the limit.
+ *  - The first call on a device resolves the scratch array's device address
+ *    with cudaGetSymbolAddress (with that device current) and caches it; make
+ *    that first call before any stream capture.
+ *  - All calls on one device share the one array, and it keeps the last
+ *    call's contents (nothing in it needs to start at zero: every partial is
+ *    written before it is read within a call).  Calls that may overlap on the
+ *    GPU, e.g. on different streams without ordering, race on it. */
+swa_status swa_verify_attn_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *seq_lens, const int32_t *q_pos,
+                                   int32_t window, float scale, void *out, float *lse,
+                                   const swa_dims *dims, swa_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

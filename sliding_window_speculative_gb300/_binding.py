@@ -72,6 +72,8 @@ def load_library(path=LIB_PATH):
     lib.swa_read_device_errors.restype = ctypes.c_int
     lib.swa_version.argtypes = []
     lib.swa_version.restype = ctypes.c_char_p
+    lib.swa_verify_attn_noalloc.argtypes = lib.swa_verify_attn.argtypes
+    lib.swa_verify_attn_noalloc.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -106,7 +108,7 @@ def _dev_tensor(t, name, dtype, ndim):
 
 
 def swa_verify_attn(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out=None, lse=None,
-                    num_splits=0, stream=None, want_lse=True):
+                    num_splits=0, stream=None, want_lse=True, _entry="swa_verify_attn"):
     """Windowed verify attention through the C entry point swa_verify_attn.
 
     q bf16 [B, q_len, Hq, D]; k_cache, v_cache bf16 [B, Hkv, L, D];
@@ -143,9 +145,26 @@ def swa_verify_attn(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out=Non
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    _check(lib.swa_verify_attn(pq, pk, pv, ps, pp, int(window), float(scale), po, pl,
-                               ctypes.byref(dims), handle))
+    _check(getattr(lib, _entry)(pq, pk, pv, ps, pp, int(window), float(scale), po, pl,
+                                ctypes.byref(dims), handle))
     return out, lse
+
+
+def swa_verify_attn_noalloc(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out, lse=None,
+                            num_splits=0, stream=None):
+    """The allocation-free C entry point swa_verify_attn_noalloc: same
+    arguments as swa_verify_attn, but `out` (and `lse`, if wanted) must be
+    given, and split partials use the library's fixed 16 MiB device scratch
+    instead of a cudaMalloc'd workspace.  For callers that may not allocate
+    device memory while serving (a pre-reserved memory pool, a framework that
+    owns every allocation, a path that cannot take cudaMalloc's device
+    synchronisation).  Overlapping calls on one device share the scratch and
+    race; make the first call on a device outside stream capture."""
+    if out is None:
+        raise ValueError("swa_verify_attn_noalloc writes into a caller-given out tensor")
+    return swa_verify_attn(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out=out,
+                           lse=lse, num_splits=num_splits, stream=stream, want_lse=False,
+                           _entry="swa_verify_attn_noalloc")
 
 
 def swa_workspace_bytes(dims, window):

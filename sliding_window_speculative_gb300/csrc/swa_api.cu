@@ -389,3 +389,111 @@ swa_status swa_read_device_errors(uint32_t *flags) {
 const char *swa_version(void) { return "swa 0.1.0 sm_103a"; }
 
 }  // extern "C"
+
+// ------------------------------------------------- allocation-free variant
+//
+// Split partials of swa_verify_attn_noalloc live in this fixed array instead
+// of a cudaMalloc'd workspace.  In host code `g_noalloc_scratch` only names
+// the symbol; its device address comes from cudaGetSymbolAddress.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SWA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on device `dev` (which must be the
+// current device), resolved once per device.
+swa_status noalloc_scratch(int dev, void **ptr) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return SWA_OK;
+}
+
+}  // namespace
+
+extern "C" swa_status swa_verify_attn_noalloc(const void *q, const void *k_cache,
+                                              const void *v_cache, const int32_t *seq_lens,
+                                              const int32_t *q_pos, int32_t window, float scale,
+                                              void *out, float *lse, const swa_dims *dims,
+                                              swa_stream_t stream) {
+    swa_status st = validate_dims(dims, window);
+    if (st != SWA_OK) return st;
+    if (!q || !k_cache || !v_cache || !seq_lens || !q_pos || !out)
+        return fail(SWA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return fail(SWA_ERR_INVALID_ARG, "q, k_cache, v_cache and out must be 16-byte aligned");
+    if ((reinterpret_cast<uintptr_t>(seq_lens) & 3u) || (reinterpret_cast<uintptr_t>(q_pos) & 3u) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u))
+        return fail(SWA_ERR_INVALID_ARG, "seq_lens, q_pos and lse must be 4-byte aligned");
+    if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
+        return fail(SWA_ERR_INVALID_ARG, "scale must be finite");
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev >= kMaxDevices) return fail(SWA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+    uint32_t *fault = fault_word_ptr(dev);
+    if (fault == nullptr) return fail(SWA_ERR_CUDA, "cannot resolve the device fault word");
+    const Plan pl = make_plan(dims, window, device_sms(dev));
+    if (pl.workspace > (long long)SWA_NOALLOC_SCRATCH_BYTES)
+        return fail(SWA_ERR_WORKSPACE,
+                    "this call's %d-way split needs %lld bytes of scratch, above the fixed "
+                    "%zu-byte maximum of swa_verify_attn_noalloc; pass fewer splits "
+                    "(num_splits = 1 needs none)",
+                    pl.splits, pl.workspace, (size_t)SWA_NOALLOC_SCRATCH_BYTES);
+    void *scratch = nullptr;
+    st = noalloc_scratch(dev, &scratch);
+    if (st != SWA_OK) return st;
+
+    swa::AttnParams P{};
+    P.q = static_cast<const __nv_bfloat16 *>(q);
+    P.k = static_cast<const __nv_bfloat16 *>(k_cache);
+    P.v = static_cast<const __nv_bfloat16 *>(v_cache);
+    P.seq_lens = seq_lens;
+    P.q_pos = q_pos;
+    P.out = static_cast<__nv_bfloat16 *>(out);
+    P.lse = lse;
+    P.B = dims->batch;
+    P.q_len = dims->q_len;
+    P.Hq = dims->num_q_heads;
+    P.Hkv = dims->num_kv_heads;
+    P.G = dims->num_q_heads / dims->num_kv_heads;
+    P.L = dims->max_len;
+    P.window = window;
+    P.R = P.q_len * P.G;
+    P.splits = pl.splits;
+    P.chunk = pl.chunk;
+    P.row_tiles = pl.row_tiles;
+    P.rows_per_tile = pl.rows_per_tile;
+    P.qk_scale = scale * swa::kLog2e;
+    P.fault = fault;
+    if (pl.splits > 1) {
+        P.part_acc = static_cast<float *>(scratch);
+        P.part_ml = P.part_acc + (size_t)P.B * P.Hkv * P.splits * P.R * dims->head_dim;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    switch (dims->head_dim) {
+        case 64: e = launch_simt_d<64>(pl, P, s); break;
+        case 128: e = launch_simt_d<128>(pl, P, s); break;
+        default: e = launch_simt_d<256>(pl, P, s); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
+    if (pl.splits > 1) {
+        switch (dims->head_dim) {
+            case 64: e = launch_merge<64>(P, s); break;
+            case 128: e = launch_merge<128>(P, s); break;
+            default: e = launch_merge<256>(P, s); break;
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+    }
+    t_last_error[0] = '\0';
+    return SWA_OK;
+}
