@@ -8,8 +8,11 @@
 #include <cstring>
 #include <mutex>
 
+#include <cstdlib>
+
 #include "../../include/swa.h"
 #include "swa_simt.cuh"
+#include "swa_tc_host.h"
 
 // Fault word of each device that loads the library; kernels receive its
 // address and OR bits into it when a bounded wait gives up.
@@ -67,57 +70,120 @@ swa_status validate_dims(const swa_dims *d, int32_t window) {
 }
 
 struct Plan {
-    int kernel;       // 1 = SIMT
+    int kernel;       // 1 = CUDA-core (SIMT) chunk kernel, 2 = tensor-core kernel
     int rpw, nrg;     // SIMT row layout
     int rows_per_tile, row_tiles;
+    int q_rows_per_tile;  // tensor-core path: draft rows per item
+    int tc_n;             // tensor-core path: padded rows per item (MMA N)
     int splits, chunk;
     long long workspace;
-    long long grid;
+    long long grid;   // CTAs of the attention kernel
+    long long items;  // tensor-core path: work items
 };
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
-// Split heuristic: enough CTAs to cover every SM about twice, never a chunk
-// shorter than one 32-key tile, at most kMaxSplits chunks.  Chunks are
-// multiples of 16 keys.  Host-only: seq_lens live on the device, so the
+// Kernel override for sweeps and tests: SWA_FORCE_KERNEL=simt or =tc.
+int forced_kernel() {
+    const char *v = getenv("SWA_FORCE_KERNEL");
+    if (v == nullptr) return 0;
+    if (strcmp(v, "simt") == 0) return 1;
+    if (strcmp(v, "tc") == 0) return 2;
+    return 0;
+}
+
+// Split heuristic.  Host-only: seq_lens live on the device, so the
 // worst-case span W + q_len - 1 (bounded by the cache length) is used.
+//  - Tensor-core path (head_dim 128/256, >= 16 packed rows): one chunk per
+//    (sequence, KV head, row tile) once those units cover half the SMs;
+//    otherwise enough chunks of >= 64 keys to reach every SM.  Persistent
+//    grid of at most SMs x resident CTAs.
+//  - CUDA-core path: enough CTAs to cover every SM about twice, chunks of at
+//    least one 32-key tile.
+// Chunks are multiples of 16 keys; at most kMaxSplits chunks.
 Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
     Plan p{};
     const int G = d->num_q_heads / d->num_kv_heads;
     const int R = d->q_len * G;
-    p.kernel = 1;
-    if (R <= 4) { p.rpw = 4; p.nrg = 1; }
-    else if (R <= 8) { p.rpw = 8; p.nrg = 1; }
-    else if (R <= 16) { p.rpw = 8; p.nrg = 2; }
-    else { p.rpw = 8; p.nrg = 4; }
-    p.rows_per_tile = p.rpw * p.nrg;
-    p.row_tiles = ceil_div(R, p.rows_per_tile);
+    const int D = d->head_dim;
+    if (num_sms < 1) num_sms = 148;
     long long span = (long long)window + d->q_len - 1;
     if (span > d->max_len) span = d->max_len;
     if (span < 1) span = 1;
-    const long long units = (long long)d->batch * d->num_kv_heads * p.row_tiles;
+
+    const int force = forced_kernel();
+    const bool tc_shape = (D == 128 || D == 256) && G <= (D == 256 ? 64 : 128) &&
+                          (long long)d->batch * d->num_kv_heads * d->max_len < (1LL << 31) &&
+                          (long long)d->batch * d->q_len < (1LL << 31) &&
+                          (long long)d->batch * d->num_kv_heads * d->q_len * kMaxSplits <
+                              (1LL << 31);
+    const bool use_tc = tc_shape && (force == 2 || (force == 0 && R >= 16));
     int splits;
-    if (d->num_splits > 0) {
-        splits = d->num_splits;
+    if (use_tc) {
+        p.kernel = 2;
+        // rows per item: at most 64 for head_dim 256 (shared memory holds Q and
+        // two P tiles beside the ring), 128 for head_dim 128
+        const int max_rows = D == 256 ? 64 : 128;
+        p.rows_per_tile = R <= max_rows ? R : (max_rows / G) * G;
+        p.q_rows_per_tile = p.rows_per_tile / G;
+        p.row_tiles = ceil_div(d->q_len, p.q_rows_per_tile);
+        p.tc_n = p.rows_per_tile <= 16 ? 16 : p.rows_per_tile <= 32 ? 32
+                 : p.rows_per_tile <= 64 ? 64 : 128;
+        swa::TcConfInfo ci{};
+        swa::tc_conf(D, p.tc_n, &ci);
+        const long long units = (long long)d->batch * d->num_kv_heads * p.row_tiles;
+        if (d->num_splits > 0) {
+            splits = d->num_splits;
+        } else if (units * 2 >= num_sms) {
+            splits = 1;
+        } else {
+            long long s = (num_sms + units - 1) / units;
+            const long long by_len = (span + 63) / 64;
+            splits = (int)(s < by_len ? s : by_len);
+        }
+        if (splits < 1) splits = 1;
+        if (splits > kMaxSplits) splits = kMaxSplits;
+        long long chunk = (span + splits - 1) / splits;
+        if (d->num_splits == 0) chunk = (chunk + 15) / 16 * 16;
+        if (chunk < 1) chunk = 1;
+        splits = ceil_div(span, chunk);
+        p.splits = splits;
+        p.chunk = (int)chunk;
+        p.items = (long long)splits * units;
+        const long long slots = (long long)num_sms * ci.ctas_per_sm;
+        p.grid = p.items < slots ? p.items : slots;
     } else {
-        const long long target = 2LL * (num_sms > 0 ? num_sms : 148);
-        long long s = (target + units - 1) / units;
-        const long long by_len = (span + swa::kSimtTileKeys - 1) / swa::kSimtTileKeys;
-        if (s > by_len) s = by_len;
-        splits = (int)s;
+        p.kernel = 1;
+        if (R <= 4) { p.rpw = 4; p.nrg = 1; }
+        else if (R <= 8) { p.rpw = 8; p.nrg = 1; }
+        else if (R <= 16) { p.rpw = 8; p.nrg = 2; }
+        else { p.rpw = 8; p.nrg = 4; }
+        p.rows_per_tile = p.rpw * p.nrg;
+        p.row_tiles = ceil_div(R, p.rows_per_tile);
+        const long long units = (long long)d->batch * d->num_kv_heads * p.row_tiles;
+        if (d->num_splits > 0) {
+            splits = d->num_splits;
+        } else {
+            const long long target = 2LL * num_sms;
+            long long s = (target + units - 1) / units;
+            const long long by_len = (span + swa::kSimtTileKeys - 1) / swa::kSimtTileKeys;
+            if (s > by_len) s = by_len;
+            splits = (int)s;
+        }
+        if (splits < 1) splits = 1;
+        if (splits > kMaxSplits) splits = kMaxSplits;
+        long long chunk = (span + splits - 1) / splits;
+        if (d->num_splits == 0) chunk = (chunk + 15) / 16 * 16;
+        if (chunk < 1) chunk = 1;
+        splits = ceil_div(span, chunk);
+        p.splits = splits;
+        p.chunk = (int)chunk;
+        p.grid = (long long)splits * d->num_kv_heads * p.row_tiles * d->batch;
+        p.items = p.grid;
     }
-    if (splits < 1) splits = 1;
-    if (splits > kMaxSplits) splits = kMaxSplits;
-    long long chunk = (span + splits - 1) / splits;
-    if (d->num_splits == 0) chunk = (chunk + 15) / 16 * 16;
-    if (chunk < 1) chunk = 1;
-    splits = ceil_div(span, chunk);
-    p.splits = splits;
-    p.chunk = (int)chunk;
-    p.grid = (long long)splits * d->num_kv_heads * p.row_tiles * d->batch;
-    p.workspace = splits > 1 ? (long long)d->batch * d->num_kv_heads * splits * R *
-                                   ((long long)d->head_dim + 2) * 4
-                             : 0;
+    p.workspace = p.splits > 1 ? (long long)d->batch * d->num_kv_heads * p.splits * R *
+                                     ((long long)D + 2) * 4
+                               : 0;
     return p;
 }
 
@@ -202,6 +268,47 @@ cudaError_t launch_merge(const swa::AttnParams &P, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Launches the attention kernel of `pl` (and the merge kernel when the
+// plan splits the keys).  P carries every pointer, including the partials.
+swa_status launch_plan(const Plan &pl, const swa_dims *dims, const swa::AttnParams &P,
+                       const void *q, const void *k_cache, const void *v_cache, cudaStream_t s) {
+    cudaError_t e;
+    if (pl.kernel == 2) {
+        swa::TcLaunch L{};
+        L.T.a = P;
+        L.T.rows_per_tile = pl.rows_per_tile;
+        L.T.q_rows_per_tile = pl.q_rows_per_tile;
+        L.T.items = (int)pl.items;
+        L.D = dims->head_dim;
+        L.N = pl.tc_n;
+        L.grid = (int)pl.grid;
+        L.q = q;
+        L.k = k_cache;
+        L.v = v_cache;
+        char msg[256] = "";
+        e = swa::tc_launch(L, s, msg, sizeof msg);
+        if (e != cudaSuccess)
+            return msg[0] ? fail(SWA_ERR_CUDA, "%s", msg)
+                          : cuda_fail(e, "tensor-core kernel launch");
+    } else {
+        switch (dims->head_dim) {
+            case 64: e = launch_simt_d<64>(pl, P, s); break;
+            case 128: e = launch_simt_d<128>(pl, P, s); break;
+            default: e = launch_simt_d<256>(pl, P, s); break;
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
+    }
+    if (pl.splits > 1) {
+        switch (dims->head_dim) {
+            case 64: e = launch_merge<64>(P, s); break;
+            case 128: e = launch_merge<128>(P, s); break;
+            default: e = launch_merge<256>(P, s); break;
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+    }
+    return SWA_OK;
+}
+
 uint32_t *fault_word_ptr(int dev) {
     static uint32_t *cache[kMaxDevices] = {};
     if (cache[dev] == nullptr) {
@@ -281,20 +388,8 @@ swa_status swa_verify_attn(const void *q, const void *k_cache, const void *v_cac
         P.part_acc = static_cast<float *>(ws);
         P.part_ml = P.part_acc + (size_t)P.B * P.Hkv * P.splits * P.R * dims->head_dim;
     }
-    switch (dims->head_dim) {
-        case 64: e = launch_simt_d<64>(pl, P, s); break;
-        case 128: e = launch_simt_d<128>(pl, P, s); break;
-        default: e = launch_simt_d<256>(pl, P, s); break;
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
-    if (pl.splits > 1) {
-        switch (dims->head_dim) {
-            case 64: e = launch_merge<64>(P, s); break;
-            case 128: e = launch_merge<128>(P, s); break;
-            default: e = launch_merge<256>(P, s); break;
-        }
-        if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
-    }
+    st = launch_plan(pl, dims, P, q, k_cache, v_cache, s);
+    if (st != SWA_OK) return st;
     t_last_error[0] = '\0';
     return SWA_OK;
 }
@@ -480,20 +575,8 @@ extern "C" swa_status swa_verify_attn_noalloc(const void *q, const void *k_cache
         P.part_ml = P.part_acc + (size_t)P.B * P.Hkv * P.splits * P.R * dims->head_dim;
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    switch (dims->head_dim) {
-        case 64: e = launch_simt_d<64>(pl, P, s); break;
-        case 128: e = launch_simt_d<128>(pl, P, s); break;
-        default: e = launch_simt_d<256>(pl, P, s); break;
-    }
-    if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
-    if (pl.splits > 1) {
-        switch (dims->head_dim) {
-            case 64: e = launch_merge<64>(P, s); break;
-            case 128: e = launch_merge<128>(P, s); break;
-            default: e = launch_merge<256>(P, s); break;
-        }
-        if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
-    }
+    st = launch_plan(pl, dims, P, q, k_cache, v_cache, s);
+    if (st != SWA_OK) return st;
     t_last_error[0] = '\0';
     return SWA_OK;
 }

@@ -1,0 +1,39 @@
+// Internal interface between the C-ABI layer and the tensor-core path.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "swa_simt.cuh"
+
+namespace swa {
+
+// Kernel parameters of the tensor-core path (plain data).
+struct TcParams {
+    AttnParams a;
+    int rows_per_tile;    // packed rows per item (a multiple of G, <= N)
+    int q_rows_per_tile;  // draft rows per item
+    int items;            // splits * Hkv * row_tiles * B
+};
+
+struct TcConfInfo {
+    int nslot;        // ring slots of 16 KB
+    int smem_bytes;   // dynamic shared memory per CTA
+    int tmem_cols;    // TMEM columns per CTA
+    int ctas_per_sm;  // resident CTAs per SM the plan assumes
+};
+
+struct TcLaunch {
+    TcParams T;
+    int D, N;   // head_dim, padded rows per item
+    int grid;   // persistent CTAs
+    const void *k, *v, *q;
+};
+
+// Constants of the (head_dim, padded rows) configuration; false if none.
+bool tc_conf(int D, int N, TcConfInfo *c);
+
+// Encodes the TMA tensor maps and launches; on failure writes a message.
+cudaError_t tc_launch(const TcLaunch &L, cudaStream_t stream, char *err, size_t errlen);
+
+}  // namespace swa

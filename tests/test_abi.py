@@ -107,14 +107,37 @@ def test_plan_invariants(lib, B, q_len, Hq, Hkv, D, L, W, sms):
     assert p["num_splits"] * p["chunk_keys"] >= span               # chunks cover the span
     assert (p["num_splits"] - 1) * p["chunk_keys"] < span          # no empty trailing chunk
     assert p["row_tiles"] * p["rows_per_tile"] >= R
-    assert p["grid_ctas"] == p["num_splits"] * Hkv * p["row_tiles"] * B
+    units = p["num_splits"] * Hkv * p["row_tiles"] * B
+    if p["kernel"] == 1:
+        assert p["grid_ctas"] == units
+    else:                                   # persistent grid over the work items
+        assert p["kernel"] == 2 and 1 <= p["grid_ctas"] <= min(units, 2 * sms)
+        assert p["rows_per_tile"] <= (64 if D == 256 else 128)
+        assert p["rows_per_tile"] % (Hq // Hkv) == 0
     assert p["merge"] == (1 if p["num_splits"] > 1 else 0)
     assert p["workspace_bytes"] <= swa.swa_workspace_bytes(dims, W)
     if p["num_splits"] > 1:
         assert p["workspace_bytes"] == B * Hkv * p["num_splits"] * R * (D + 2) * 4
 
 
-def test_plan_forced_splits(lib):
+def test_plan_kernel_choice(lib, monkeypatch):
+    q8 = swa.make_dims(1, 8, 8, 2, 256, 4096)
+    assert swa.swa_plan(q8, 188, 152)["kernel"] == 2            # 32 packed rows: tensor cores
+    q1 = swa.make_dims(1, 1, 8, 2, 256, 4096)
+    assert swa.swa_plan(q1, 188, 152)["kernel"] == 1            # 4 rows: CUDA cores
+    d64 = swa.make_dims(1, 8, 2, 1, 64, 40)
+    assert swa.swa_plan(d64, 16, 152)["kernel"] == 1            # head_dim 64: CUDA cores
+    q64 = swa.swa_plan(swa.make_dims(512, 64, 8, 2, 256, 32768), 1024, 152)
+    assert q64["kernel"] == 2 and q64["row_tiles"] == 4 and q64["rows_per_tile"] == 64
+    monkeypatch.setenv("SWA_FORCE_KERNEL", "simt")
+    assert swa.swa_plan(q8, 188, 152)["kernel"] == 1
+    monkeypatch.setenv("SWA_FORCE_KERNEL", "tc")
+    assert swa.swa_plan(q1, 188, 152)["kernel"] == 2
+    assert swa.swa_plan(d64, 16, 152)["kernel"] == 1
+
+
+def test_plan_forced_splits(lib, monkeypatch):
+    monkeypatch.setenv("SWA_FORCE_KERNEL", "simt")
     dims = swa.make_dims(1, 8, 8, 2, 256, 4096, 5)
     p = swa.swa_plan(dims, 188, 152)
     assert p["num_splits"] == 5 and p["chunk_keys"] == 39

@@ -26,6 +26,15 @@ def _built():
     yield
 
 
+@pytest.fixture(params=["simt", "tc"])
+def kernel(request, monkeypatch):
+    """Runs the test once per kernel: the CUDA-core chunk kernel and the
+    tensor-core kernel (shapes the tensor-core kernel does not cover,
+    head_dim 64, fall back to the CUDA-core kernel)."""
+    monkeypatch.setenv("SWA_FORCE_KERNEL", request.param)
+    return request.param
+
+
 def _check(case, num_splits=0, seqs=None, what=None):
     out, lse = run_gpu(case, num_splits)
     ref_o, ref_l = oracle_reference(case, seqs)
@@ -38,21 +47,21 @@ def _check(case, num_splits=0, seqs=None, what=None):
 
 @pytest.mark.parametrize("q_len", [1, 8])
 @pytest.mark.parametrize("splits", [0, 1, 2, 3])
-def test_tiny(q_len, splits):
+def test_tiny(q_len, splits, kernel):
     _check(inputs.tiny(q_len, device="cuda"), splits)
 
 
 @pytest.mark.parametrize("splits", [0, 1, 2, 5, 13])
-def test_single_stream(splits):
+def test_single_stream(splits, kernel):
     _check(inputs.single_stream(device="cuda"), splits)
 
 
 @pytest.mark.parametrize("window", [188, 4096])
-def test_window_vs_full(window):
+def test_window_vs_full(window, kernel):
     _check(inputs.window_vs_full(window, device="cuda"))
 
 
-def test_batched():
+def test_batched(kernel):
     _check(inputs.batched(device="cuda"))
 
 
@@ -60,7 +69,7 @@ STRESS = [(w, q) for w in (188, 512, 1024) for q in (1, 8, 64)]
 
 
 @pytest.mark.parametrize("window,q_len", STRESS)
-def test_stress_full_size_sampled(window, q_len):
+def test_stress_full_size_sampled(window, q_len, kernel):
     """Full bandwidth-stress size (512 sequences, cache 32768); the oracle
     checks a seeded subset of 12 sequences (plus the shortest and longest)."""
     case = inputs.stress(window, q_len)
@@ -78,7 +87,7 @@ def test_stress_full_size_sampled(window, q_len):
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("Hq,Hkv", [(2, 2), (6, 2), (16, 2), (8, 1)])
 @pytest.mark.parametrize("q_len", [1, 3, 8, 17])
-def test_ragged_shapes(D, Hq, Hkv, q_len):
+def test_ragged_shapes(D, Hq, Hkv, q_len, kernel):
     lens = [q_len, 5 + q_len, 100, 301, 77]
     case = inputs.make_case("ragged", 5, Hq, Hkv, D, q_len, 37, lens, 320, seed=11,
                             outliers=True, device="cuda")
@@ -87,7 +96,7 @@ def test_ragged_shapes(D, Hq, Hkv, q_len):
 
 
 @pytest.mark.parametrize("Hq,Hkv", [(8, 2), (16, 2)])
-def test_max_draft_block(Hq, Hkv):
+def test_max_draft_block(Hq, Hkv, kernel):
     """q_len 64 (the verify maximum); 16/2 heads gives 512 packed rows."""
     case = inputs.make_case("maxq", 3, Hq, Hkv, 256, 64, 188, [64, 300, 1000], 1024, seed=12,
                             outliers=True, device="cuda")
@@ -95,20 +104,20 @@ def test_max_draft_block(Hq, Hkv):
 
 
 @pytest.mark.parametrize("window", [1, 2, 63, 64, 65, 5000])
-def test_window_sizes(window):
+def test_window_sizes(window, kernel):
     case = inputs.make_case("win", 2, 8, 2, 128, 8, window, [200, 33], 256, seed=13,
                             device="cuda")
     _check(case)
     _check(case, num_splits=3, what=f"W{window}/3 splits")
 
 
-def test_single_row_sequence():
+def test_single_row_sequence(kernel):
     case = inputs.make_case("one", 1, 8, 2, 256, 1, 188, [1], 16, q_pos=[0], seed=14,
                             device="cuda")
     _check(case)
 
 
-def test_nan_in_unseen_rows_never_reaches_output():
+def test_nan_in_unseen_rows_never_reaches_output(kernel):
     """Rows before the window and past seq_len hold NaN (an unwritten cache)."""
     case = inputs.make_case("nan", 4, 8, 2, 256, 8, 188, [100, 1000, 4000, 9], 4096, seed=15,
                             device="cuda", fill="window", margin=0, poison="nan")
@@ -118,7 +127,7 @@ def test_nan_in_unseen_rows_never_reaches_output():
     _check(case)
 
 
-def test_rows_past_seq_len_and_before_zero():
+def test_rows_past_seq_len_and_before_zero(kernel):
     """Device preconditions broken on purpose: q_pos < 0 gives rows with no
     key (out 0, lse -inf); rows past seq_len see keys up to seq_len - 1."""
     case = inputs.make_case("defensive", 3, 4, 2, 64, 8, 10, [20, 12, 6], 24,
@@ -128,7 +137,7 @@ def test_rows_past_seq_len_and_before_zero():
     _check(case)
 
 
-def test_deterministic():
+def test_deterministic(kernel):
     case = inputs.batched(device="cuda")
     a = run_gpu(case)
     b = run_gpu(case)
@@ -150,7 +159,7 @@ def test_lse_optional():
 
 @pytest.mark.parametrize("window,q_len", [(188, 8), (188, 1), (16, 8), (1, 4), (512, 64)])
 @pytest.mark.parametrize("splits", [0, 1, 3])
-def test_count_probe(window, q_len, splits):
+def test_count_probe(window, q_len, splits, kernel):
     """K = 0 makes every score 0, so lse = ln |K(p)| exactly: an off-by-one
     window (|K| = W + 1) moves lse by ln((W+1)/W) > 1e-3 for W <= 999."""
     lens = [window + q_len + 40, window // 2 + q_len, q_len]
@@ -168,7 +177,7 @@ def test_count_probe(window, q_len, splits):
 
 
 @pytest.mark.parametrize("offset,inside", [(-188, False), (-187, True), (0, True), (1, False)])
-def test_edge_probe(offset, inside):
+def test_edge_probe(offset, inside, kernel):
     """One spike key at p + offset carries a marker value; rows see it only
     when it lies in (p - W, p]."""
     W, q_len = 188, 8
@@ -221,7 +230,7 @@ def test_workspace_caller_owned_and_capture():
     assert e.value.status == swa.SWA_ERR_WORKSPACE
 
 
-def test_graph_replay_matches_eager():
+def test_graph_replay_matches_eager(kernel):
     import sliding_window_speculative_gb300 as swa
     case = inputs.single_stream(device="cuda")
     ref, ref_l = run_gpu(case)          # grows the workspace outside capture
