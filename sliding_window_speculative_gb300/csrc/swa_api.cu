@@ -112,7 +112,7 @@ Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
     if (span < 1) span = 1;
 
     const int force = forced_kernel();
-    const bool tc_shape = (D == 128 || D == 256) && G <= (D == 256 ? 64 : 128) &&
+    const bool tc_shape = (D == 128 || D == 256) && G <= 64 &&
                           (long long)d->batch * d->num_kv_heads * d->max_len < (1LL << 31) &&
                           (long long)d->batch * d->q_len < (1LL << 31) &&
                           (long long)d->batch * d->num_kv_heads * d->q_len * kMaxSplits <
@@ -121,14 +121,13 @@ Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
     int splits;
     if (use_tc) {
         p.kernel = 2;
-        // rows per item: at most 64 for head_dim 256 (shared memory holds Q and
-        // two P tiles beside the ring), 128 for head_dim 128
-        const int max_rows = D == 256 ? 64 : 128;
+        // rows per item: at most 64 (shared memory holds Q and P tiles beside
+        // the ring; the softmax keeps a row's reference maximum in registers)
+        const int max_rows = 64;
         p.rows_per_tile = R <= max_rows ? R : (max_rows / G) * G;
         p.q_rows_per_tile = p.rows_per_tile / G;
         p.row_tiles = ceil_div(d->q_len, p.q_rows_per_tile);
-        p.tc_n = p.rows_per_tile <= 16 ? 16 : p.rows_per_tile <= 32 ? 32
-                 : p.rows_per_tile <= 64 ? 64 : 128;
+        p.tc_n = p.rows_per_tile <= 16 ? 16 : p.rows_per_tile <= 32 ? 32 : 64;
         swa::TcConfInfo ci{};
         swa::tc_conf(D, p.tc_n, &ci);
         const long long units = (long long)d->batch * d->num_kv_heads * p.row_tiles;

@@ -49,10 +49,9 @@ struct ChunkRange {
     int qp;       // q_pos of the sequence
 };
 
-__device__ __forceinline__ ChunkRange chunk_range(const AttnParams &P, int b, int split) {
+__device__ __forceinline__ ChunkRange chunk_range_of(const AttnParams &P, long long qp,
+                                                     long long sl, int split) {
     ChunkRange c;
-    const long long qp = P.q_pos[b];
-    const long long sl = P.seq_lens[b];
     long long hi = qp + P.q_len;
     if (hi > sl) hi = sl;
     if (hi > P.L) hi = P.L;
@@ -70,6 +69,10 @@ __device__ __forceinline__ ChunkRange chunk_range(const AttnParams &P, int b, in
     c.c_hi = (int)chi;
     c.qp = (int)(qp < -(1LL << 30) ? -(1LL << 30) : (qp > (1LL << 30) ? (1LL << 30) : qp));
     return c;
+}
+
+__device__ __forceinline__ ChunkRange chunk_range(const AttnParams &P, int b, int split) {
+    return chunk_range_of(P, P.q_pos[b], P.seq_lens[b], split);
 }
 
 template <int D>

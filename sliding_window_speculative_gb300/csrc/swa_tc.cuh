@@ -1,34 +1,44 @@
 // Tensor-core (tcgen05) split-KV kernel for sliding-window verify attention.
 //
-// Persistent CTAs walk a list of work items (sequence, KV head, key chunk,
-// row tile).  Keys are the MMA's M dimension: for every tile of 128 keys
+// Persistent CTAs (one per SM) walk a list of work items (sequence, KV
+// head, key chunk, row tile).  Keys are the MMA's M dimension: for every
+// tile of 128 keys
 //
 //   S^T[128 keys x N rows] = K_tile[128 x D] . Q[N x D]^T      (TMEM, fp32)
 //   O^T[D x N]            += V_tile^T[D x 128] . P^T[N x 128]^T (TMEM, fp32)
+//
+// where the N rows are the packed query rows of one KV head (G query heads
+// times the draft rows, padded to a multiple of 16), so every K/V byte is
+// read once per KV head and small draft blocks cost no M padding.
 //
 // P is carried into the second MMA as two bf16 tiles, P = P_hi + P_lo with
 // P_hi = bf16(P) and P_lo = bf16(P - P_hi), so the weights keep about 16
 // significant bits instead of bf16's 8; the PV product is issued twice.
 //
-// where the N rows are the packed query rows of one KV head (G query heads
-// times the q_len draft rows, padded to a multiple of 16), so every K/V byte
-// is read once per KV head and small draft blocks cost no M padding.  K and
-// V tiles arrive by TMA in 16 KB slabs (128 keys x 64 dims, 128-byte
-// swizzle) through a ring of shared-memory slots; Q arrives once per item.
+// K and V arrive by TMA in 16 KB slabs (128 keys x 64 dims, 128-byte
+// swizzle) through a ring of shared-memory slots; a tile with fewer than 128
+// keys is fetched in 32-key boxes.  Q, P and O are double-buffered (where
+// shared memory allows) so consecutive tiles and items overlap: the MMA lane
+// issues the next tile's S (across item boundaries) before the current
+// tile's PV, and the epilogue of one item runs while the next item's loads
+// and scores proceed.
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM owner and MMA issuer (one lane)
-//   warps 2..5  softmax / correction / epilogue, one thread per TMEM lane:
-//               a thread owns one key of the S^T tile and one head-dim row
-//               of the O^T accumulator.
+//   warps 2..9  softmax / correction / epilogue in two warpgroups that split
+//               the packed rows in halves; within a group a thread owns one
+//               TMEM lane: one key of the S^T tile and one head-dim row of
+//               the O^T accumulator (warps w and w + 4 read the same lanes).
 //
 // Softmax runs in the log2 domain with a lazily raised reference maximum:
-// each row keeps m_ref; a tile whose scaled score exceeds m_ref + 8 (a
-// factor 256) for any row triggers an exact per-row tile maximum, a raise of
-// m_ref and, if O already holds data, a rescale of O^T in TMEM.  Otherwise
-// P = 2^(s - m_ref) <= 256, exact in the ratio the normaliser divides out.
-// Row sums are reduced across lanes with a reduce-scatter butterfly.
+// each row keeps m_ref (in registers, identical in every thread of the
+// group that owns the row);
+// a tile whose scaled score exceeds m_ref + 8 (a factor 256) for any row
+// triggers an exact per-row tile maximum, a raise of m_ref and, if O
+// already holds data, a rescale of O^T in TMEM.  Otherwise
+// P = 2^(s - m_ref) <= 256.  Row sums are reduced across lanes with a
+// reduce-scatter butterfly.
 //
 // Every wait on an mbarrier is bounded; a wait that gives up sets the fault
 // word, the roles leave their loops together, and TMEM is freed.
@@ -40,47 +50,51 @@
 
 namespace swa {
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;
 constexpr int kTcTileKeys = 128;
+constexpr int kTcTailBox = 32;    // keys per box of a partial tile
+constexpr int kTcMetaItems = 16;  // items per CTA whose metadata is cached in smem
 
-template <int D, int N, int NSLOT>
+template <int D, int N, int NSLOT, int QB, int PB>
 struct TcCfg {
     static constexpr int SLABS = D / 64;
     static constexpr int SLOT_BYTES = 16384;
     static constexpr int Q_SLAB = N * 128;
+    static constexpr int Q_BUF = SLABS * Q_SLAB;
     static constexpr int P_SLAB = N * 128;
+    static constexpr int P_LO = 2 * P_SLAB;   // P_lo after P_hi (2 key slabs each)
+    static constexpr int P_BUF = 4 * P_SLAB;  // hi + lo
     static constexpr int RING_OFF = 0;
     static constexpr int Q_OFF = RING_OFF + NSLOT * SLOT_BYTES;
-    static constexpr int P_OFF = Q_OFF + SLABS * Q_SLAB;
-    static constexpr int P_LO = 2 * P_SLAB;               // P_lo tile after P_hi
-    static constexpr int RED_OFF = P_OFF + 4 * P_SLAB;  // float [4][N]
-    static constexpr int MREF_OFF = RED_OFF + 4 * N * 4;  // float [N]
-    static constexpr int ALPHA_OFF = MREF_OFF + N * 4;    // float [N]
-    static constexpr int LSUM_OFF = ALPHA_OFF + N * 4;    // float [N]
-    static constexpr int BAR_OFF = LSUM_OFF + N * 4;
-    static constexpr int NBARS = 2 * NSLOT + 10;
-    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base, abort flag
+    static constexpr int P_OFF = Q_OFF + QB * Q_BUF;
+    static constexpr int RED_OFF = P_OFF + PB * P_BUF;        // float [2][4][N]
+    static constexpr int LINV_OFF = RED_OFF + 2 * 4 * N * 4;  // float [N]
+    static constexpr int ALPHA_OFF = LINV_OFF + N * 4;        // float [N]
+    static constexpr int META_OFF = ALPHA_OFF + N * 4;        // int [2][kTcMetaItems]
+    static constexpr int BAR_OFF = META_OFF + 2 * kTcMetaItems * 4;
+    // ring full/empty, q full/empty [QB], s full/free [2], p full [PB],
+    // pv done [PB], o free [2], drain
+    static constexpr int B_FULL = 0, B_EMPTY = NSLOT, B_QFULL = 2 * NSLOT,
+                         B_QEMPTY = B_QFULL + QB, B_SFULL = B_QEMPTY + QB, B_SFREE = B_SFULL + 2,
+                         B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + PB, B_OFREE = B_PVDONE + PB,
+                         B_DRAIN = B_OFREE + 2, NBARS = B_DRAIN + 1;
+    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base
     static constexpr int END = MISC_OFF + 16;
     static constexpr int SMEM_BYTES = END + 1024;  // slack for 1024-byte alignment
-    static constexpr int TMEM_USED = 2 * N + (D / 128) * N;
+    static constexpr int TMEM_USED = 2 * N + 2 * (D / 128) * N;
     static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
                                      : TMEM_USED <= 64  ? 64
                                      : TMEM_USED <= 128 ? 128
                                      : TMEM_USED <= 256 ? 256
                                                         : 512;
+    static constexpr int O_COL = 2 * N;           // O buffer ob at O_COL + ob * (D/128) * N
     static constexpr int CW = N >= 32 ? 32 : 16;  // TMEM columns per load
     static constexpr int NCH = N / CW;
-    static constexpr bool LOOKAHEAD = NSLOT >= 2 * SLABS;
-    // two CTAs share an SM when shared memory allows it
-    static constexpr int MIN_BLOCKS = SMEM_BYTES + 1024 <= 113 * 1024 ? 2 : 1;
-    static_assert(NSLOT % 2 == 0 && NSLOT >= SLABS, "ring holds whole K or V tiles in pairs");
-    static_assert(N % 16 == 0 && N >= 16 && N <= 128, "rows per tile");
+    static_assert(NSLOT % 2 == 0 && NSLOT >= 2 * SLABS, "ring holds a K and a V tile, V in pairs");
+    static_assert(N % 16 == 0 && N >= 16 && N <= 64, "rows per tile");
     static_assert(TMEM_USED <= 512, "TMEM");
-    // barrier indices
-    static constexpr int B_FULL = 0, B_EMPTY = NSLOT, B_QFULL = 2 * NSLOT, B_QEMPTY = 2 * NSLOT + 1,
-                         B_SFULL = 2 * NSLOT + 2, B_SFREE = 2 * NSLOT + 4,
-                         B_PFULL = 2 * NSLOT + 6, B_PVDONE = 2 * NSLOT + 7,
-                         B_OFREE = 2 * NSLOT + 8, B_DRAIN = 2 * NSLOT + 9;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static_assert(PB * P_BUF >= N * 512, "epilogue staging fits in the P buffers");
 };
 
 struct TcItem {
@@ -92,7 +106,10 @@ struct TcItem {
     int i0;    // first draft row
 };
 
-__device__ __forceinline__ TcItem tc_decode(const TcParams &T, int item) {
+// Work item `item`; `j` is its position in this CTA's item sequence (its
+// metadata may sit in shared memory).
+__device__ __forceinline__ TcItem tc_decode(const TcParams &T, int item, int j,
+                                            const int *meta_sl, const int *meta_qp) {
     const AttnParams &P = T.a;
     TcItem it;
     int rest = item;
@@ -102,7 +119,10 @@ __device__ __forceinline__ TcItem tc_decode(const TcParams &T, int item) {
     rest /= P.splits;
     it.h = rest % P.Hkv;
     it.b = rest / P.Hkv;
-    it.cr = chunk_range(P, it.b, it.split);
+    if (j < kTcMetaItems)
+        it.cr = chunk_range_of(P, meta_qp[j], meta_sl[j], it.split);
+    else
+        it.cr = chunk_range(P, it.b, it.split);
     const int nk = it.cr.c_hi - it.cr.c_lo;
     it.n_tiles = nk > 0 ? (nk + kTcTileKeys - 1) / kTcTileKeys : 0;
     it.row0 = it.rt * T.rows_per_tile;
@@ -111,26 +131,29 @@ __device__ __forceinline__ TcItem tc_decode(const TcParams &T, int item) {
     return it;
 }
 
-__device__ __forceinline__ void named_sync_softmax() {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
+// Barrier of one softmax warpgroup (128 threads), ids 1 / 3.
+__device__ __forceinline__ void group_sync(int wg) {
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + 2 * wg) : "memory");
 }
 
-// True on every softmax thread if `v` is true on any of them.
-__device__ __forceinline__ bool softmax_any(bool v) {
+// True on every thread of softmax warpgroup `wg` if `v` is true on any of
+// them (ids 2 / 4).
+__device__ __forceinline__ bool group_any(int wg, bool v) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.or.pred p, 2, 128, q;\n\t"
+        "bar.red.or.pred p, %2, 128, q;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(r)
-        : "r"((uint32_t)v)
+        : "r"((uint32_t)v), "r"(2 + 2 * wg)
         : "memory");
     return r != 0;
 }
 
-// Reduce-scatter of CW per-lane values across the warp with op `max` or
-// `sum`: afterwards lane l holds the reduction of element (l % CW).
+// Reduce-scatter of CW (8, 16 or 32) per-lane values across the warp with
+// op `max` or `sum`: afterwards lane l holds the reduction of element
+// (l % CW) over all 32 lanes.  v is consumed.
 template <int CW, bool MAX>
 __device__ __forceinline__ float lane_reduce(float (&v)[CW]) {
     const int lane = threadIdx.x & 31;
@@ -145,32 +168,47 @@ __device__ __forceinline__ float lane_reduce(float (&v)[CW]) {
             v[e] = MAX ? fmaxf(keep, got) : keep + got;
         }
     }
-    if constexpr (CW == 16) {
-        const float got = __shfl_xor_sync(0xffffffffu, v[0], 16);
+#pragma unroll
+    for (int off = CW; off < 32; off <<= 1) {
+        const float got = __shfl_xor_sync(0xffffffffu, v[0], off);
         v[0] = MAX ? fmaxf(v[0], got) : v[0] + got;
     }
     return v[0];
 }
 
-template <int CW>
-__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, uint32_t (&raw)[CW]) {
-    if constexpr (CW == 32) {
-        tc::tmem_ld32(taddr, raw);
+// W (8, 16 or 32) consecutive TMEM columns of this thread's lane.
+template <int W>
+__device__ __forceinline__ void tmem_load(uint32_t taddr, uint32_t *r) {
+    if constexpr (W == 32) {
+        tc::tmem_ld32(taddr, *reinterpret_cast<uint32_t(*)[32]>(r));
+    } else if constexpr (W == 16) {
+        tc::tmem_ld16(taddr, r);
     } else {
-        tc::tmem_ld16(taddr, raw);
+        tc::tmem_ld8(taddr, r);
     }
-    tc::tmem_wait_ld();
 }
 
-template <int D, int N, int NSLOT>
-__global__ void __launch_bounds__(kTcThreads, (TcCfg<D, N, NSLOT>::MIN_BLOCKS))
+template <int W>
+__device__ __forceinline__ void tmem_store(uint32_t taddr, const uint32_t *r) {
+    if constexpr (W == 16) {
+        tc::tmem_st16(taddr, r);
+    } else {
+        static_assert(W == 8, "store width");
+        tc::tmem_st8(taddr, r);
+    }
+}
+
+template <int D, int N, int NSLOT, int QB, int PB>
+__global__ void __launch_bounds__(kTcThreads, 1)
     swa_tc_kernel(const __grid_constant__ TcParams T, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v,
+                  const __grid_constant__ CUtensorMap map_k32,
+                  const __grid_constant__ CUtensorMap map_v32,
                   const __grid_constant__ CUtensorMap map_q) {
-    using C = TcCfg<D, N, NSLOT>;
+    using C = TcCfg<D, N, NSLOT, QB, PB>;
     using namespace tc;
     constexpr int SLABS = C::SLABS;
-    constexpr int CW = C::CW;
+    constexpr int MH = D / 128;
     const float NEG_INF = -__int_as_float(0x7f800000);
     const AttnParams &P = T.a;
 
@@ -181,15 +219,16 @@ __global__ void __launch_bounds__(kTcThreads, (TcCfg<D, N, NSLOT>::MIN_BLOCKS))
     uint8_t *qs = sm + C::Q_OFF;
     uint8_t *ps = sm + C::P_OFF;
     float *red = reinterpret_cast<float *>(sm + C::RED_OFF);
-    float *mref = reinterpret_cast<float *>(sm + C::MREF_OFF);
-    float *alpha = reinterpret_cast<float *>(sm + C::ALPHA_OFF);
-    float *lsum = reinterpret_cast<float *>(sm + C::LSUM_OFF);
+    float *linv = reinterpret_cast<float *>(sm + C::LINV_OFF);
+    float *alpha_sm = reinterpret_cast<float *>(sm + C::ALPHA_OFF);
+    int *meta_sl = reinterpret_cast<int *>(sm + C::META_OFF);
+    int *meta_qp = meta_sl + kTcMetaItems;
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::BAR_OFF);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::MISC_OFF);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::MISC_OFF + 4);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    const int per_b = P.row_tiles * P.splits * P.Hkv;  // items per sequence
 
     // ---------------------------------------------------------------- setup
     if (tid == 0) {
@@ -197,22 +236,34 @@ __global__ void __launch_bounds__(kTcThreads, (TcCfg<D, N, NSLOT>::MIN_BLOCKS))
             mbar_init(&bars[C::B_FULL + i], 1);
             mbar_init(&bars[C::B_EMPTY + i], 1);
         }
-        mbar_init(&bars[C::B_QFULL], 1);
-        mbar_init(&bars[C::B_QEMPTY], 1);
-        mbar_init(&bars[C::B_SFULL], 1);
-        mbar_init(&bars[C::B_SFULL + 1], 1);
-        mbar_init(&bars[C::B_SFREE], 128);
-        mbar_init(&bars[C::B_SFREE + 1], 128);
-        mbar_init(&bars[C::B_PFULL], 128);
-        mbar_init(&bars[C::B_PVDONE], 1);
-        mbar_init(&bars[C::B_OFREE], 128);
+        for (int i = 0; i < QB; ++i) {
+            mbar_init(&bars[C::B_QFULL + i], 1);
+            mbar_init(&bars[C::B_QEMPTY + i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[C::B_SFULL + i], 1);
+            mbar_init(&bars[C::B_SFREE + i], 256);
+            mbar_init(&bars[C::B_OFREE + i], 256);
+        }
+        for (int i = 0; i < PB; ++i) {
+            mbar_init(&bars[C::B_PFULL + i], 256);
+            mbar_init(&bars[C::B_PVDONE + i], 1);
+        }
         mbar_init(&bars[C::B_DRAIN], 1);
-        *abort_flag = 0;
         fence_barrier_init();
     }
-    // Q rows past the item's rows stay zero for the whole kernel (TMA
-    // writes only the first rows_per_tile rows of each slab).
-    for (int i = tid; i < SLABS * C::Q_SLAB / 16; i += kTcThreads)
+    // metadata of this CTA's first items
+    for (int j = tid; j < kTcMetaItems; j += kTcThreads) {
+        const long long item = (long long)blockIdx.x + (long long)j * gridDim.x;
+        if (item < T.items) {
+            const int b = (int)(item / per_b);
+            meta_sl[j] = P.seq_lens[b];
+            meta_qp[j] = P.q_pos[b];
+        }
+    }
+    // Q rows past an item's rows stay zero for the whole kernel (TMA writes
+    // only the first rows_per_tile rows of each slab).
+    for (int i = tid; i < QB * C::Q_BUF / 16; i += kTcThreads)
         reinterpret_cast<uint4 *>(qs)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 1) {
@@ -229,165 +280,241 @@ __global__ void __launch_bounds__(kTcThreads, (TcCfg<D, N, NSLOT>::MIN_BLOCKS))
         if (lane == 0) {
             prefetch_tmap(&map_k);
             prefetch_tmap(&map_v);
+            prefetch_tmap(&map_k32);
+            prefetch_tmap(&map_v32);
             prefetch_tmap(&map_q);
             const uint64_t policy = l2_policy_evict_first();
-            uint32_t f = 0, qi = 0;
+            uint32_t f = 0, k = 0;
             bool ok = true;
-            for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x) {
-                const TcItem it = tc_decode(T, item);
+            int j = 0;
+            for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
+                const TcItem it = tc_decode(T, item, j, meta_sl, meta_qp);
                 if (it.n_tiles == 0) continue;
-                ok = mbar_wait_bounded(&bars[C::B_QEMPTY], (qi & 1) ^ 1, P.fault, kFaultCopyTimeout);
-                if (!ok) break;
-                mbar_arrive_expect_tx(&bars[C::B_QFULL], SLABS * T.rows_per_tile * 128);
-                for (int s = 0; s < SLABS; ++s)
-                    tma_load_3d(qs + s * C::Q_SLAB, &map_q, 64 * s, it.h * P.G,
-                                it.b * P.q_len + it.i0, &bars[C::B_QFULL]);
-                ++qi;
+                const uint32_t qb = k % QB, quse = k / QB;
+                // Q of the item, issued after its first K tile so that a single
+                // Q buffer does not hold back the K stream
+                auto load_q = [&]() -> bool {
+                    if (!mbar_wait_bounded(&bars[C::B_QEMPTY + qb], (quse & 1) ^ 1, P.fault,
+                                           kFaultCopyTimeout))
+                        return false;
+                    mbar_arrive_expect_tx(&bars[C::B_QFULL + qb], SLABS * T.rows_per_tile * 128);
+                    for (int s = 0; s < SLABS; ++s)
+                        tma_load_3d(qs + qb * C::Q_BUF + s * C::Q_SLAB, &map_q, 64 * s,
+                                    it.h * P.G, it.b * P.q_len + it.i0, &bars[C::B_QFULL + qb]);
+                    return true;
+                };
+                ++k;
                 const int y0 = (it.b * P.Hkv + it.h) * P.L + it.cr.c_lo;
                 for (int t = 0; t < it.n_tiles && ok; ++t) {
+                    const int n_valid =
+                        min(kTcTileKeys, it.cr.c_hi - it.cr.c_lo - kTcTileKeys * t);
+                    const int nb =
+                        n_valid == kTcTileKeys ? 0 : (n_valid + kTcTailBox - 1) / kTcTailBox;
+                    const int y = y0 + kTcTileKeys * t;
                     for (int kv = 0; kv < 2 && ok; ++kv) {
+                        if (t == 0 && kv == 1) {
+                            ok = load_q();
+                            if (!ok) break;
+                        }
                         for (int s = 0; s < SLABS; ++s) {
                             const uint32_t slot = f % NSLOT;
                             ok = mbar_wait_bounded(&bars[C::B_EMPTY + slot], ((f / NSLOT) & 1) ^ 1,
                                                    P.fault, kFaultCopyTimeout);
                             if (!ok) break;
-                            mbar_arrive_expect_tx(&bars[C::B_FULL + slot], C::SLOT_BYTES);
-                            tma_load_2d_hint(ring + slot * C::SLOT_BYTES, kv ? &map_v : &map_k,
-                                             64 * s, y0 + kTcTileKeys * t,
-                                             &bars[C::B_FULL + slot], policy);
+                            uint8_t *dst = ring + slot * C::SLOT_BYTES;
+                            if (nb == 0) {
+                                mbar_arrive_expect_tx(&bars[C::B_FULL + slot], C::SLOT_BYTES);
+                                tma_load_2d_hint(dst, kv ? &map_v : &map_k, 64 * s, y,
+                                                 &bars[C::B_FULL + slot], policy);
+                            } else {
+                                mbar_arrive_expect_tx(&bars[C::B_FULL + slot],
+                                                      nb * kTcTailBox * 128);
+                                for (int bi = 0; bi < nb; ++bi)
+                                    tma_load_2d_hint(dst + bi * kTcTailBox * 128,
+                                                     kv ? &map_v32 : &map_k32, 64 * s,
+                                                     y + kTcTailBox * bi,
+                                                     &bars[C::B_FULL + slot], policy);
+                            }
                             ++f;
                         }
                     }
                 }
             }
-            if (!ok) *abort_flag = 1;
             // every copy this CTA issued has landed before it exits
             const uint32_t n_drain = f < (uint32_t)NSLOT ? f : (uint32_t)NSLOT;
-            for (uint32_t k = 0; k < n_drain; ++k) {
-                const uint32_t fi = f - 1 - k;
+            for (uint32_t q = 0; q < n_drain; ++q) {
+                const uint32_t fi = f - 1 - q;
                 mbar_wait_bounded(&bars[C::B_FULL + fi % NSLOT], (fi / NSLOT) & 1, P.fault,
                                   kFaultCopyTimeout);
             }
-            if (qi > 0)
-                mbar_wait_bounded(&bars[C::B_QFULL], (qi - 1) & 1, P.fault, kFaultCopyTimeout);
+            const uint32_t nq = k < (uint32_t)QB ? k : (uint32_t)QB;
+            for (uint32_t q = 0; q < nq; ++q) {
+                const uint32_t kq = k - 1 - q;
+                mbar_wait_bounded(&bars[C::B_QFULL + kq % QB], (kq / QB) & 1, P.fault,
+                                  kFaultCopyTimeout);
+            }
         }
     } else if (warp == 1) {
         // ============================================================ MMA
+        // An event loop over two cursors on the same tile sequence: S = K Q^T
+        // of the next tile and O += V^T P^T of the oldest tile whose P is
+        // ready are each issued as soon as their operands have landed, so
+        // neither waits behind the other.
         if (lane == 0) {
             constexpr uint32_t ID_QK = idesc_bf16_f32(128, N, 0, 0);
             constexpr uint32_t ID_PV = idesc_bf16_f32(128, N, 1, 0);
             const uint32_t ring_a = smem_u32(ring);
             const uint32_t qs_a = smem_u32(qs);
             const uint32_t ps_a = smem_u32(ps);
-            uint32_t f = 0, qi = 0, gt = 0, pc = 0, oc = 0;
-            bool ok = true;
-            for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x) {
-                const TcItem it = tc_decode(T, item);
-                if (it.n_tiles == 0) continue;
-                ok = mbar_wait_bounded(&bars[C::B_QFULL], qi & 1, P.fault, kFaultCopyTimeout);
-                if (!ok) break;
-                ++qi;
-                fence_after_sync();
-                const uint32_t fbase = f;
-                f += (uint32_t)it.n_tiles * 2 * SLABS;
-                auto qk = [&](int t) -> bool {
-                    const uint32_t g = gt + t;
-                    const uint32_t sb = g & 1, use = g >> 1;
-                    if (!mbar_wait_bounded(&bars[C::B_SFREE + sb], (use & 1) ^ 1, P.fault,
-                                           kFaultCopyTimeout))
-                        return false;
-                    fence_after_sync();
-                    for (int s = 0; s < SLABS; ++s) {
-                        const uint32_t fi = fbase + (uint32_t)t * 2 * SLABS + s;
-                        const uint32_t slot = fi % NSLOT;
-                        if (!mbar_wait_bounded(&bars[C::B_FULL + slot], (fi / NSLOT) & 1, P.fault,
-                                               kFaultCopyTimeout))
-                            return false;
-                        fence_after_sync();
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t a =
-                                smem_desc_sw128(ring_a + slot * C::SLOT_BYTES + kk * 32, 16, 1024);
-                            const uint64_t bdesc =
-                                smem_desc_sw128(qs_a + s * C::Q_SLAB + kk * 32, 16, 1024);
-                            mma_bf16_ss(tmem + sb * N, a, bdesc, ID_QK, (s | kk) != 0);
-                        }
-                        mma_commit(&bars[C::B_EMPTY + slot]);
+            struct Cursor {
+                int item, j, t, n_tiles;
+                uint32_t k, fbase, g;
+                bool valid;
+            };
+            // first tile of the next non-empty item at or after (item, j)
+            auto seek = [&](Cursor &c) {
+                for (; c.item < T.items; c.item += gridDim.x, ++c.j) {
+                    const TcItem it = tc_decode(T, c.item, c.j, meta_sl, meta_qp);
+                    if (it.n_tiles > 0) {
+                        c.n_tiles = it.n_tiles;
+                        c.t = 0;
+                        c.valid = true;
+                        return;
                     }
-                    mma_commit(&bars[C::B_SFULL + sb]);
-                    return true;
-                };
-                if (C::LOOKAHEAD) ok = qk(0);
-                for (int t = 0; t < it.n_tiles && ok; ++t) {
-                    if (C::LOOKAHEAD) {
-                        if (t + 1 < it.n_tiles) ok = qk(t + 1);
-                    } else {
-                        ok = qk(t);
-                    }
-                    if (!ok) break;
-                    if (t == it.n_tiles - 1) mma_commit(&bars[C::B_QEMPTY]);
-                    ok = mbar_wait_bounded(&bars[C::B_PFULL], pc & 1, P.fault, kFaultCopyTimeout);
-                    if (!ok) break;
-                    ++pc;
-                    fence_after_sync();
-                    if (t == 0) {
-                        ok = mbar_wait_bounded(&bars[C::B_OFREE], (oc & 1) ^ 1, P.fault,
-                                               kFaultCopyTimeout);
-                        if (!ok) break;
-                        ++oc;
-                        fence_after_sync();
-                    }
-                    for (int mh = 0; mh < D / 128 && ok; ++mh) {
-                        const uint32_t fi0 = fbase + (uint32_t)t * 2 * SLABS + SLABS + 2 * mh;
-                        const uint32_t s0 = fi0 % NSLOT, s1 = (fi0 + 1) % NSLOT;  // s1 = s0 + 1
-                        ok = mbar_wait_bounded(&bars[C::B_FULL + s0], (fi0 / NSLOT) & 1, P.fault,
-                                               kFaultCopyTimeout) &&
-                             mbar_wait_bounded(&bars[C::B_FULL + s1], ((fi0 + 1) / NSLOT) & 1,
-                                               P.fault, kFaultCopyTimeout);
-                        if (!ok) break;
-                        fence_after_sync();
-#pragma unroll
-                        for (int kk = 0; kk < 16; ++kk) {
-                            // A = V^T: MN-major, the two 64-dim slabs one slot apart;
-                            // B = P_hi for kk < 8, then P_lo
-                            const int k8 = kk & 7;
-                            const uint64_t a = smem_desc_sw128(
-                                ring_a + s0 * C::SLOT_BYTES + k8 * 2048, C::SLOT_BYTES, 1024);
-                            const uint64_t bdesc = smem_desc_sw128(
-                                ps_a + (kk >> 3) * C::P_LO + (k8 >> 2) * C::P_SLAB + (k8 & 3) * 32,
-                                16, 1024);
-                            mma_bf16_ss(tmem + 2 * N + mh * N, a, bdesc, ID_PV,
-                                        (t > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        mma_commit(&bars[C::B_EMPTY + s0]);
-                        mma_commit(&bars[C::B_EMPTY + s1]);
-                    }
-                    if (!ok) break;
-                    mma_commit(&bars[C::B_PVDONE]);
                 }
-                gt += it.n_tiles;
+                c.valid = false;
+            };
+            auto advance = [&](Cursor &c) {
+                ++c.g;
+                if (++c.t < c.n_tiles) return;
+                c.fbase += (uint32_t)c.n_tiles * 2 * SLABS;
+                ++c.k;
+                c.item += gridDim.x;
+                ++c.j;
+                seek(c);
+            };
+            Cursor qc{(int)blockIdx.x, 0, 0, 0, 0u, 0u, 0u, false};
+            seek(qc);
+            Cursor pc = qc;
+            bool ok = true;
+            long long idle_since = clock64();
+            while (pc.valid) {
+                bool progressed = false;
+                // ---- PV of tile pc.g (its S was issued before)
+                if (pc.g < qc.g || !qc.valid) {
+                    const uint32_t pb = pc.g % PB;
+                    const uint32_t fv = pc.fbase + (uint32_t)pc.t * 2 * SLABS + SLABS;
+                    bool ready = mbar_test(&bars[C::B_PFULL + pb], (pc.g / PB) & 1);
+                    if (ready && pc.t == 0)
+                        ready = mbar_test(&bars[C::B_OFREE + (pc.k & 1)], ((pc.k >> 1) & 1) ^ 1);
+#pragma unroll
+                    for (int s = 0; s < SLABS; ++s)
+                        ready = ready && mbar_test(&bars[C::B_FULL + (fv + s) % NSLOT],
+                                                   ((fv + s) / NSLOT) & 1);
+                    if (ready) {
+                        fence_after_sync();
+                        const uint32_t pbase = ps_a + pb * C::P_BUF;
+                        const uint32_t ob = pc.k & 1;
+#pragma unroll
+                        for (int mh = 0; mh < MH; ++mh) {
+                            const uint32_t s0 = (fv + 2 * mh) % NSLOT;  // s0 + 1 holds the next slab
+#pragma unroll
+                            for (int kk = 0; kk < 16; ++kk) {
+                                // A = V^T: MN-major, the two 64-dim slabs one slot apart;
+                                // B = P_hi for kk < 8, then P_lo
+                                const int k8 = kk & 7;
+                                const uint64_t a = smem_desc_sw128(
+                                    ring_a + s0 * C::SLOT_BYTES + k8 * 2048, C::SLOT_BYTES, 1024);
+                                const uint64_t bdesc = smem_desc_sw128(
+                                    pbase + (kk >> 3) * C::P_LO + (k8 >> 2) * C::P_SLAB +
+                                        (k8 & 3) * 32,
+                                    16, 1024);
+                                mma_bf16_ss(tmem + C::O_COL + (ob * MH + mh) * N, a, bdesc, ID_PV,
+                                            (pc.t > 0 || kk > 0) ? 1u : 0u);
+                            }
+                            mma_commit(&bars[C::B_EMPTY + s0]);
+                            mma_commit(&bars[C::B_EMPTY + s0 + 1]);
+                        }
+                        mma_commit(&bars[C::B_PVDONE + pb]);
+                        advance(pc);
+                        progressed = true;
+                    }
+                }
+                // ---- S of tile qc.g
+                if (qc.valid) {
+                    const uint32_t sb = qc.g & 1;
+                    const uint32_t fk = qc.fbase + (uint32_t)qc.t * 2 * SLABS;
+                    bool ready = mbar_test(&bars[C::B_SFREE + sb], ((qc.g >> 1) & 1) ^ 1) &&
+                                 mbar_test(&bars[C::B_QFULL + qc.k % QB], (qc.k / QB) & 1);
+#pragma unroll
+                    for (int s = 0; s < SLABS; ++s)
+                        ready = ready && mbar_test(&bars[C::B_FULL + (fk + s) % NSLOT],
+                                                   ((fk + s) / NSLOT) & 1);
+                    if (ready) {
+                        fence_after_sync();
+                        const uint32_t qaddr = qs_a + (qc.k % QB) * C::Q_BUF;
+#pragma unroll
+                        for (int s = 0; s < SLABS; ++s) {
+                            const uint32_t slot = (fk + s) % NSLOT;
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t a = smem_desc_sw128(
+                                    ring_a + slot * C::SLOT_BYTES + kk * 32, 16, 1024);
+                                const uint64_t bdesc =
+                                    smem_desc_sw128(qaddr + s * C::Q_SLAB + kk * 32, 16, 1024);
+                                mma_bf16_ss(tmem + sb * N, a, bdesc, ID_QK, (s | kk) != 0);
+                            }
+                            mma_commit(&bars[C::B_EMPTY + slot]);
+                        }
+                        mma_commit(&bars[C::B_SFULL + sb]);
+                        if (qc.t == qc.n_tiles - 1) mma_commit(&bars[C::B_QEMPTY + qc.k % QB]);
+                        advance(qc);
+                        progressed = true;
+                    }
+                }
+                if (progressed) {
+                    idle_since = clock64();
+                } else if (clock64() - idle_since < kWaitLimitCycles) {
+                    __nanosleep(20);  // leave issue slots to the softmax warps
+                } else {
+                    atomicOr(P.fault, kFaultCopyTimeout);
+                    ok = false;
+                    break;
+                }
             }
-            if (!ok) *abort_flag = 1;
+            (void)ok;
             // all issued MMAs complete before TMEM is released
             mma_commit(&bars[C::B_DRAIN]);
             mbar_wait_bounded(&bars[C::B_DRAIN], 0, P.fault, kFaultCopyTimeout);
         }
     } else {
         // ===================================================== softmax
-        const int sw = warp - 2;           // softmax warp 0..3
-        const int quad = warp & 3;         // TMEM lane quadrant of this warp
-        const int lk = quad * 32 + lane;   // TMEM lane: key of S^T, dim row of O^T
-        const int stid = tid - 64;         // 0..127
+        constexpr int HN = N / 2;                 // rows per softmax warpgroup
+        constexpr int CWH = HN >= 32 ? 32 : HN;  // TMEM columns per S load
+        constexpr int NCH = HN / CWH;
+        constexpr int OW = HN >= 16 ? 16 : 8;    // TMEM columns per O load / store
+        const int wg = (warp - 2) >> 2;          // softmax warpgroup
+        const int sw = (warp - 2) & 3;           // warp within the group
+        const int quad = warp & 3;               // TMEM lane quadrant of this warp
+        const int lk = quad * 32 + lane;         // TMEM lane: key of S^T, dim row of O^T
+        const int gtid = sw * 32 + lane;         // 0..127 within the group
+        const int r0 = wg * HN;                  // first packed row of this group
         const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
-        uint32_t gt = 0, pvw = 0, fbase = 0;
+        // P^T address pieces of this thread's key: the 16-byte chunk index
+        // of key lk inside a 128-byte row is XORed with (row & 7)
+        const uint32_t p_key = (uint32_t)(lk >> 6) * C::P_SLAB + (uint32_t)(lk & 7) * 2;
+        const uint32_t p_chunk = (uint32_t)(lk & 63) >> 3;
+        uint32_t g = 0, k = 0, fbase = 0;
         bool ok = true;
-        for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x) {
-            const TcItem it = tc_decode(T, item);
+        int j = 0;
+        for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
+            const TcItem it = tc_decode(T, item, j, meta_sl, meta_qp);
             const size_t bh = (size_t)it.b * P.Hkv + it.h;
+            const int my_rows = min(HN, it.rows - r0);  // rows of this group in the item
             if (it.n_tiles == 0) {
                 // no key in this chunk: empty result for every row
-                for (int idx = stid; idx < it.rows * D; idx += 128) {
-                    const int r = it.row0 + idx / D, d = idx % D;
+                for (int idx = gtid; idx < my_rows * D; idx += 128) {
+                    const int r = it.row0 + r0 + idx / D, d = idx % D;
                     const int i = r / P.G, gg = r - i * P.G;
                     const size_t orow =
                         ((size_t)it.b * P.q_len + i) * P.Hq + (size_t)it.h * P.G + gg;
@@ -405,135 +532,149 @@ __global__ void __launch_bounds__(kTcThreads, (TcCfg<D, N, NSLOT>::MIN_BLOCKS))
                 }
                 continue;
             }
-            for (int r = stid; r < N; r += 128) mref[r] = NEG_INF;
-            float lpart[C::NCH];
+            const uint32_t ob = k & 1;
+            float mref[HN], lrow[HN];
 #pragma unroll
-            for (int c = 0; c < C::NCH; ++c) lpart[c] = 0.f;
-            named_sync_softmax();
+            for (int r = 0; r < HN; ++r) {
+                mref[r] = NEG_INF;
+                lrow[r] = 0.f;
+            }
 
             const int qp_i0 = it.cr.qp + it.i0;  // position of the item's first draft row
-            for (int t = 0; t < it.n_tiles; ++t) {
-                const uint32_t sb = gt & 1, use = gt >> 1;
-                ok = !softmax_any(!mbar_wait_bounded(&bars[C::B_SFULL + sb], use & 1, P.fault,
-                                                     kFaultCopyTimeout));
+            for (int t = 0; t < it.n_tiles; ++t, ++g) {
+                const uint32_t sb = g & 1, suse = g >> 1;
+                ok = !group_any(wg, !mbar_wait_bounded(&bars[C::B_SFULL + sb], suse & 1,
+                                                       P.fault, kFaultCopyTimeout));
                 if (!ok) break;
                 fence_after_sync();
                 const int j0 = it.cr.c_lo + kTcTileKeys * t;
                 const int n_valid = min(kTcTileKeys, it.cr.c_hi - j0);
-                const int j = j0 + lk;
-                // packed rows [ra, rb) of this item whose window holds key j:
-                // draft row i sees j iff p_i - W < j <= p_i, p_i = qp_i0 + i
+                const int jk = j0 + lk;
+                // packed rows [ra, rb) of this item whose window holds key jk:
+                // draft row i sees jk iff p_i - W < jk <= p_i, p_i = qp_i0 + i;
+                // shifted to this group's rows
                 int ra = 0, rb = 0;
                 if (lk < n_valid) {
-                    const long long lo_i = (long long)j - qp_i0;
-                    const long long hi_i = (long long)j + P.window - qp_i0;
+                    const long long lo_i = (long long)jk - qp_i0;
+                    const long long hi_i = (long long)jk + P.window - qp_i0;
                     const long long a = lo_i < 0 ? 0 : lo_i * P.G;
                     long long bnd = hi_i < 0 ? 0 : hi_i * P.G;
                     if (bnd > it.rows) bnd = it.rows;
-                    ra = (int)(a < it.rows ? a : it.rows);
-                    rb = (int)bnd;
+                    ra = (int)(a < it.rows ? a : it.rows) - r0;
+                    rb = (int)bnd - r0;
                 }
-                const uint32_t scol = tl + sb * N;
-
-                // pass 1: does any score exceed its row's reference by more than 2^8?
-                bool flag = false;
+                // this group's scores into registers, then hand the S buffer back
+                float v[HN];
+                {
+                    uint32_t raw[HN];
 #pragma unroll
-                for (int c = 0; c < C::NCH; ++c) {
-                    uint32_t raw[CW];
-                    tmem_load_cols<CW>(scol + c * CW, raw);
+                    for (int c = 0; c < NCH; ++c)
+                        tmem_load<CWH>(tl + sb * N + r0 + c * CWH, raw + c * CWH);
+                    tmem_wait_ld();
+                    if (ra <= 0 && rb >= HN) {
 #pragma unroll
-                    for (int e = 0; e < CW; ++e) {
-                        const int r = c * CW + e;
-                        const float v = (r >= ra && r < rb) ? __uint_as_float(raw[e]) * P.qk_scale
-                                                            : NEG_INF;
-                        flag |= v > mref[r] + 8.f;
-                    }
-                }
-                const bool raise = softmax_any(flag);
-                if (raise) {
-                    // exact tile maximum per row, then raise the references
+                        for (int r = 0; r < HN; ++r) v[r] = __uint_as_float(raw[r]) * P.qk_scale;
+                    } else {
 #pragma unroll
-                    for (int c = 0; c < C::NCH; ++c) {
-                        uint32_t raw[CW];
-                        tmem_load_cols<CW>(scol + c * CW, raw);
-                        float v[CW];
-#pragma unroll
-                        for (int e = 0; e < CW; ++e) {
-                            const int r = c * CW + e;
-                            v[e] = (r >= ra && r < rb) ? __uint_as_float(raw[e]) * P.qk_scale
+                        for (int r = 0; r < HN; ++r)
+                            v[r] = (r >= ra && r < rb) ? __uint_as_float(raw[r]) * P.qk_scale
                                                        : NEG_INF;
-                        }
-                        const float m = lane_reduce<CW, true>(v);
-                        if (lane < CW) red[sw * N + c * CW + lane] = m;
                     }
-                    named_sync_softmax();
-                    for (int r = stid; r < N; r += 128) {
-                        const float tm = fmaxf(fmaxf(red[r], red[N + r]),
-                                               fmaxf(red[2 * N + r], red[3 * N + r]));
-                        const float mo = mref[r];
-                        const float mn = fmaxf(mo, tm);
-                        alpha[r] = (mn == mo) ? 1.f : fast_exp2(mo - mn);
-                        mref[r] = mn;
-                    }
-                    named_sync_softmax();
-                }
-                // PV of the previous tile done: P buffer free, O^T stable
-                if (t > 0) {
-                    ok = !softmax_any(!mbar_wait_bounded(&bars[C::B_PVDONE], pvw & 1, P.fault,
-                                                         kFaultCopyTimeout));
-                    if (!ok) break;
-                    ++pvw;
-                    fence_after_sync();
-                }
-                if (raise && t > 0) {
-#pragma unroll 1
-                    for (int mh = 0; mh < D / 128; ++mh) {
-#pragma unroll 1
-                        for (int c0 = 0; c0 < N; c0 += 16) {
-                            uint32_t o[16];
-                            const uint32_t ocol = tl + 2 * N + mh * N + c0;
-                            tmem_ld16(ocol, o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha[c0 + e]);
-                            tmem_st16(ocol, o);
-                        }
-                    }
-                    tmem_wait_st();
-#pragma unroll
-                    for (int c = 0; c < C::NCH; ++c) lpart[c] *= alpha[c * CW + (lane % CW)];
-                }
-                // pass 2: P = 2^(s - m_ref) into the swizzled P^T tile, row sums
-#pragma unroll
-                for (int c = 0; c < C::NCH; ++c) {
-                    uint32_t raw[CW];
-                    tmem_load_cols<CW>(scol + c * CW, raw);
-                    float pv[CW];
-#pragma unroll
-                    for (int e = 0; e < CW; ++e) {
-                        const int r = c * CW + e;
-                        const float m = mref[r];
-                        const float mu = m == NEG_INF ? 0.f : m;
-                        const float v = (r >= ra && r < rb) ? __uint_as_float(raw[e]) * P.qk_scale
-                                                            : NEG_INF;
-                        const float p = fast_exp2(v - mu);
-                        const __nv_bfloat16 hi = __float2bfloat16_rn(p);
-                        const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
-                        const uint32_t off = (lk >> 6) * C::P_SLAB + sw128_offset(r, lk & 63);
-                        *reinterpret_cast<__nv_bfloat16 *>(ps + off) = hi;
-                        *reinterpret_cast<__nv_bfloat16 *>(ps + C::P_LO + off) = lo;
-                        // the sum weights exactly what the two MMAs weight
-                        pv[e] = __bfloat162float(hi) + __bfloat162float(lo);
-                    }
-                    lpart[c] += lane_reduce<CW, false>(pv);
                 }
                 fence_before_sync();
                 mbar_arrive(&bars[C::B_SFREE + sb]);
-                // Keys past the chunk's end: their V rows are zeroed so that
-                // 0 * (whatever the cache holds there) cannot reach O; the
-                // TMA box always spans 128 keys.
-                if (n_valid < kTcTileKeys) {
+
+                bool flag = false;
+#pragma unroll
+                for (int r = 0; r < HN; ++r) flag |= v[r] > mref[r] + 8.f;
+                const bool raise = group_any(wg, flag);
+                if (raise) {
+                    // exact tile maximum per row; raise the references
+                    float *rd = red + (g & 1) * 4 * N + r0;
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        float tmp[CWH];
+#pragma unroll
+                        for (int e = 0; e < CWH; ++e) tmp[e] = v[c * CWH + e];
+                        const float m = lane_reduce<CWH, true>(tmp);
+                        if (lane < CWH) rd[sw * N + c * CWH + lane] = m;
+                    }
+                    group_sync(wg);
+                    const bool rescale = t > 0;
+#pragma unroll
+                    for (int r4 = 0; r4 < HN; r4 += 4) {
+                        const float4 a0 = *reinterpret_cast<const float4 *>(rd + r4);
+                        const float4 a1 = *reinterpret_cast<const float4 *>(rd + N + r4);
+                        const float4 a2 = *reinterpret_cast<const float4 *>(rd + 2 * N + r4);
+                        const float4 a3 = *reinterpret_cast<const float4 *>(rd + 3 * N + r4);
+                        const float tm[4] = {fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x)),
+                                             fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y)),
+                                             fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z)),
+                                             fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w))};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float mo = mref[r4 + e];
+                            const float mn = fmaxf(mo, tm[e]);
+                            const float al = (mn == mo) ? 1.f : fast_exp2(mo - mn);
+                            if (rescale && gtid == r4 + e) alpha_sm[r0 + r4 + e] = al;
+                            lrow[r4 + e] *= al;
+                            mref[r4 + e] = mn;
+                        }
+                    }
+                    if (rescale) {
+                        // every PV of this item so far has completed before O is scaled
+                        const uint32_t gp = g - 1;
+                        ok = !group_any(wg, !mbar_wait_bounded(&bars[C::B_PVDONE + gp % PB],
+                                                               (gp / PB) & 1, P.fault,
+                                                               kFaultCopyTimeout));
+                        if (!ok) break;
+                        fence_after_sync();  // (the vote also published alpha_sm)
+#pragma unroll 1
+                        for (int mh = 0; mh < MH; ++mh) {
+#pragma unroll 1
+                            for (int c0 = 0; c0 < HN; c0 += OW) {
+                                uint32_t o[OW];
+                                const uint32_t ocol =
+                                    tl + C::O_COL + (ob * MH + mh) * N + r0 + c0;
+                                tmem_load<OW>(ocol, o);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int e = 0; e < OW; ++e)
+                                    o[e] = __float_as_uint(__uint_as_float(o[e]) *
+                                                           alpha_sm[r0 + c0 + e]);
+                                tmem_store<OW>(ocol, o);
+                            }
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                // P buffer free: its previous PV has completed
+                const uint32_t pb = g % PB;
+                if (g >= (uint32_t)PB && !(raise && t > 0 && PB == 1)) {
+                    const uint32_t gp = g - PB;
+                    ok = !group_any(wg, !mbar_wait_bounded(&bars[C::B_PVDONE + pb],
+                                                           (gp / PB) & 1, P.fault,
+                                                           kFaultCopyTimeout));
+                    if (!ok) break;
+                }
+                // P = 2^(s - m_ref) as bf16 hi + lo into the swizzled P^T tiles
+                uint8_t *pt = ps + pb * C::P_BUF + p_key;
+#pragma unroll
+                for (int r = 0; r < HN; ++r) {
+                    const float mu = mref[r] == NEG_INF ? 0.f : mref[r];
+                    const float p = fast_exp2(v[r] - mu);
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(p);
+                    const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
+                    const int rr = r0 + r;
+                    const uint32_t off = (uint32_t)rr * 128 + ((p_chunk ^ (uint32_t)(rr & 7)) << 4);
+                    *reinterpret_cast<__nv_bfloat16 *>(pt + off) = hi;
+                    *reinterpret_cast<__nv_bfloat16 *>(pt + C::P_LO + off) = lo;
+                    lrow[r] += p;
+                }
+                // Keys past the chunk's end: their V rows are zeroed (by the
+                // first group) so that 0 * (whatever the slot holds there)
+                // cannot reach O.
+                if (n_valid < kTcTileKeys && wg == 0) {
                     const uint32_t fv = fbase + (uint32_t)t * 2 * SLABS + SLABS;
                     bool vok = true;
 #pragma unroll
@@ -541,7 +682,7 @@ __global__ void __launch_bounds__(kTcThreads, (TcCfg<D, N, NSLOT>::MIN_BLOCKS))
                         vok = vok && mbar_wait_bounded(&bars[C::B_FULL + (fv + s) % NSLOT],
                                                        ((fv + s) / NSLOT) & 1, P.fault,
                                                        kFaultCopyTimeout);
-                    ok = !softmax_any(!vok);
+                    ok = !group_any(wg, !vok);
                     if (!ok) break;
                     if (lk >= n_valid) {
 #pragma unroll
@@ -554,56 +695,36 @@ __global__ void __launch_bounds__(kTcThreads, (TcCfg<D, N, NSLOT>::MIN_BLOCKS))
                     }
                 }
                 fence_proxy_async_smem();
-                fence_before_sync();
-                mbar_arrive(&bars[C::B_PFULL]);
-                ++gt;
+                mbar_arrive(&bars[C::B_PFULL + pb]);
             }
             if (!ok) break;
 
             // -------------------------------------------------- epilogue
-            ok = !softmax_any(!mbar_wait_bounded(&bars[C::B_PVDONE], pvw & 1, P.fault,
-                                                 kFaultCopyTimeout));
+            const uint32_t gl = g - 1;  // the item's last tile
+            ok = !group_any(wg, !mbar_wait_bounded(&bars[C::B_PVDONE + gl % PB], (gl / PB) & 1,
+                                                   P.fault, kFaultCopyTimeout));
             if (!ok) break;
-            ++pvw;
             fence_after_sync();
+            // row sums: lanes, then the group's four warps
+            float *rl = red + (g & 1) * 4 * N + r0;
 #pragma unroll
-            for (int c = 0; c < C::NCH; ++c)
-                if (lane < CW) red[sw * N + c * CW + lane] = lpart[c];
-            named_sync_softmax();
-            for (int r = stid; r < N; r += 128)
-                lsum[r] = (red[r] + red[N + r]) + (red[2 * N + r] + red[3 * N + r]);
-            named_sync_softmax();
-#pragma unroll 1
-            for (int mh = 0; mh < D / 128; ++mh) {
-                const int d = mh * 128 + lk;
-#pragma unroll 1
-                for (int c0 = 0; c0 < N; c0 += 16) {
-                    if (c0 >= it.rows) break;
-                    uint32_t o[16];
-                    tmem_ld16(tl + 2 * N + mh * N + c0, o);
-                    tmem_wait_ld();
+            for (int c = 0; c < NCH; ++c) {
+                float tmp[CWH];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int r = c0 + e;
-                        if (r >= it.rows) break;
-                        const int rg = it.row0 + r;
-                        const float ov = __uint_as_float(o[e]);
-                        if (P.splits == 1) {
-                            const int i = rg / P.G, gg = rg - i * P.G;
-                            const size_t orow =
-                                ((size_t)it.b * P.q_len + i) * P.Hq + (size_t)it.h * P.G + gg;
-                            const float l = lsum[r];
-                            P.out[orow * D + d] = __float2bfloat16_rn(l > 0.f ? ov / l : 0.f);
-                        } else {
-                            const size_t prow = (bh * P.splits + it.split) * P.R + rg;
-                            P.part_acc[prow * D + d] = ov;
-                        }
-                    }
-                }
+                for (int e = 0; e < CWH; ++e) tmp[e] = lrow[c * CWH + e];
+                const float s = lane_reduce<CWH, false>(tmp);
+                if (lane < CWH) rl[sw * N + c * CWH + lane] = s;
             }
-            for (int r = stid; r < it.rows; r += 128) {
-                const int rg = it.row0 + r;
-                const float l = lsum[r], m = mref[r];
+            group_sync(wg);
+            if (gtid < my_rows) {
+                const int r = gtid;
+                const float l = (rl[r] + rl[N + r]) + (rl[2 * N + r] + rl[3 * N + r]);
+                float m = NEG_INF;
+#pragma unroll
+                for (int q = 0; q < HN; ++q)
+                    if (q == r) m = mref[q];
+                linv[r0 + r] = l > 0.f ? 1.f / l : 0.f;
+                const int rg = it.row0 + r0 + r;
                 if (P.splits == 1) {
                     if (P.lse != nullptr) {
                         const int i = rg / P.G, gg = rg - i * P.G;
@@ -617,12 +738,55 @@ __global__ void __launch_bounds__(kTcThreads, (TcCfg<D, N, NSLOT>::MIN_BLOCKS))
                     P.part_ml[prow * 2 + 1] = l;
                 }
             }
-            fence_before_sync();
-            mbar_arrive(&bars[C::B_OFREE]);
+            group_sync(wg);
+            // O^T through shared memory (the P buffers are idle now) into
+            // 16-byte row stores
+            uint8_t *stg = ps;
+            const bool part = P.splits > 1;
+#pragma unroll 1
+            for (int mh = 0; mh < MH; ++mh) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < HN; c0 += OW) {
+                    uint32_t o[OW];
+                    tmem_load<OW>(tl + C::O_COL + (ob * MH + mh) * N + r0 + c0, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < OW; ++e) {
+                        const int r = r0 + c0 + e;
+                        const float ov = __uint_as_float(o[e]);
+                        if (part)
+                            *reinterpret_cast<float *>(stg + r * 512 + lk * 4) = ov;
+                        else
+                            *reinterpret_cast<__nv_bfloat16 *>(stg + r * 256 + lk * 2) =
+                                __float2bfloat16_rn(ov * linv[r]);
+                    }
+                }
+                if (mh == MH - 1) {
+                    fence_before_sync();
+                    mbar_arrive(&bars[C::B_OFREE + ob]);  // O buffer may be reused
+                }
+                group_sync(wg);
+                const int cpr = part ? 32 : 16;  // 16-byte chunks per row of this half
+                for (int idx = gtid; idx < my_rows * cpr; idx += 128) {
+                    const int r = r0 + idx / cpr, c = idx % cpr;
+                    const int rg = it.row0 + r;
+                    const uint4 val =
+                        *reinterpret_cast<const uint4 *>(stg + r * (cpr * 16) + c * 16);
+                    if (part) {
+                        const size_t prow = (bh * P.splits + it.split) * P.R + rg;
+                        *reinterpret_cast<uint4 *>(P.part_acc + prow * D + mh * 128 + c * 4) = val;
+                    } else {
+                        const int i = rg / P.G, gg = rg - i * P.G;
+                        const size_t orow =
+                            ((size_t)it.b * P.q_len + i) * P.Hq + (size_t)it.h * P.G + gg;
+                        *reinterpret_cast<uint4 *>(P.out + orow * D + mh * 128 + c * 8) = val;
+                    }
+                }
+                group_sync(wg);
+            }
             fbase += (uint32_t)it.n_tiles * 2 * SLABS;
-            named_sync_softmax();
+            ++k;
         }
-        if (!ok) *abort_flag = 1;
     }
 
     // ---------------------------------------------------------- teardown

@@ -111,8 +111,8 @@ def test_plan_invariants(lib, B, q_len, Hq, Hkv, D, L, W, sms):
     if p["kernel"] == 1:
         assert p["grid_ctas"] == units
     else:                                   # persistent grid over the work items
-        assert p["kernel"] == 2 and 1 <= p["grid_ctas"] <= min(units, 2 * sms)
-        assert p["rows_per_tile"] <= (64 if D == 256 else 128)
+        assert p["kernel"] == 2 and 1 <= p["grid_ctas"] <= min(units, sms)
+        assert p["rows_per_tile"] <= 64
         assert p["rows_per_tile"] % (Hq // Hkv) == 0
     assert p["merge"] == (1 if p["num_splits"] > 1 else 0)
     assert p["workspace_bytes"] <= swa.swa_workspace_bytes(dims, W)
