@@ -359,8 +359,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // An event loop over two cursors on the same tile sequence: S = K Q^T
         // of the next tile and O += V^T P^T of the oldest tile whose P is
         // ready are each issued as soon as their operands have landed, so
-        // neither waits behind the other.
-        if (lane == 0) {
+        // neither waits behind the other.  The whole warp runs the loop (its
+        // lanes zero the ragged end of a partial V tile); lane 0 issues.
+        {
+            const bool leader = lane == 0;
             constexpr uint32_t ID_QK = idesc_bf16_f32(128, N, 0, 0);
             constexpr uint32_t ID_PV = idesc_bf16_f32(128, N, 1, 0);
             const uint32_t ring_a = smem_u32(ring);
@@ -393,11 +395,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ++c.j;
                 seek(c);
             };
+            // keys of tile t of the cursor's item (the chunk end is known from the
+            // item; tc_decode is repeated only when a tile is partial)
+            auto tile_keys = [&](const Cursor &c) -> int {
+                const TcItem it = tc_decode(T, c.item, c.j, meta_sl, meta_qp);
+                return min(kTcTileKeys, it.cr.c_hi - it.cr.c_lo - kTcTileKeys * c.t);
+            };
             Cursor qc{(int)blockIdx.x, 0, 0, 0, 0u, 0u, 0u, false};
             seek(qc);
             Cursor pc = qc;
             bool ok = true;
             long long idle_since = clock64();
+            int idle = 0;
             while (pc.valid) {
                 bool progressed = false;
                 // ---- PV of tile pc.g (its S was issued before)
@@ -413,29 +422,65 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                    ((fv + s) / NSLOT) & 1);
                     if (ready) {
                         fence_after_sync();
-                        const uint32_t pbase = ps_a + pb * C::P_BUF;
-                        const uint32_t ob = pc.k & 1;
-#pragma unroll
-                        for (int mh = 0; mh < MH; ++mh) {
-                            const uint32_t s0 = (fv + 2 * mh) % NSLOT;  // s0 + 1 holds the next slab
-#pragma unroll
-                            for (int kk = 0; kk < 16; ++kk) {
-                                // A = V^T: MN-major, the two 64-dim slabs one slot apart;
-                                // B = P_hi for kk < 8, then P_lo
-                                const int k8 = kk & 7;
-                                const uint64_t a = smem_desc_sw128(
-                                    ring_a + s0 * C::SLOT_BYTES + k8 * 2048, C::SLOT_BYTES, 1024);
-                                const uint64_t bdesc = smem_desc_sw128(
-                                    pbase + (kk >> 3) * C::P_LO + (k8 >> 2) * C::P_SLAB +
-                                        (k8 & 3) * 32,
-                                    16, 1024);
-                                mma_bf16_ss(tmem + C::O_COL + (ob * MH + mh) * N, a, bdesc, ID_PV,
-                                            (pc.t > 0 || kk > 0) ? 1u : 0u);
+                        // a partial tile: only the 16-key steps that hold valid keys
+                        // are multiplied; the rows of the last step past the chunk's
+                        // end are zeroed first, so that 0 * (whatever the slot holds
+                        // there) cannot reach O
+                        const int nv = pc.t == pc.n_tiles - 1 ? tile_keys(pc) : kTcTileKeys;
+                        const int steps = (nv + 15) >> 4;
+                        if (nv & 15) {
+                            const int zr = steps * 16 - nv;  // rows to clear, < 16
+#pragma unroll 1
+                            for (int idx = lane; idx < SLABS * zr * 8; idx += 32) {
+                                const int s = idx / (zr * 8), rem = idx - s * zr * 8;
+                                const int row = nv + rem / 8, q = rem & 7;
+                                reinterpret_cast<uint4 *>(ring + ((fv + s) % NSLOT) * C::SLOT_BYTES +
+                                                          row * 128)[q] = make_uint4(0, 0, 0, 0);
                             }
-                            mma_commit(&bars[C::B_EMPTY + s0]);
-                            mma_commit(&bars[C::B_EMPTY + s0 + 1]);
+                            fence_proxy_async_smem();
+                            __syncwarp();
                         }
-                        mma_commit(&bars[C::B_PVDONE + pb]);
+                        if (leader) {
+                            // descriptors differ only in the start address (16-byte
+                            // units in the low bits), so offsets are added to a base
+                            const uint64_t bbase =
+                                smem_desc_sw128(ps_a + pb * C::P_BUF, 16, 1024);
+                            const uint32_t ob = pc.k & 1;
+                            const uint32_t acc0 = pc.t > 0 ? 1u : 0u;
+#pragma unroll
+                            for (int mh = 0; mh < MH; ++mh) {
+                                const uint32_t s0 = (fv + 2 * mh) % NSLOT;  // s0 + 1: next slab
+                                // A = V^T: MN-major, the two 64-dim slabs one slot apart
+                                const uint64_t abase = smem_desc_sw128(
+                                    ring_a + s0 * C::SLOT_BYTES, C::SLOT_BYTES, 1024);
+                                const uint32_t d_t = tmem + C::O_COL + (ob * MH + mh) * N;
+                                // B = P_hi for the first pass, then P_lo
+                                if (steps == 8) {
+#pragma unroll
+                                    for (int kk = 0; kk < 16; ++kk) {
+                                        const int hl = kk >> 3, k8 = kk & 7;
+                                        mma_bf16_ss(d_t, abase + (uint64_t)(k8 * 128),
+                                                    bbase + (uint64_t)(hl * (C::P_LO >> 4) +
+                                                                       (k8 >> 2) * (C::P_SLAB >> 4) +
+                                                                       (k8 & 3) * 2),
+                                                    ID_PV, (acc0 | (uint32_t)kk) != 0);
+                                    }
+                                } else {
+                                    for (int kk = 0; kk < 2 * steps; ++kk) {
+                                        const int hl = kk >= steps, k8 = hl ? kk - steps : kk;
+                                        mma_bf16_ss(d_t, abase + (uint64_t)(k8 * 128),
+                                                    bbase + (uint64_t)(hl * (C::P_LO >> 4) +
+                                                                       (k8 >> 2) * (C::P_SLAB >> 4) +
+                                                                       (k8 & 3) * 2),
+                                                    ID_PV, (acc0 | (uint32_t)kk) != 0);
+                                    }
+                                }
+                                mma_commit(&bars[C::B_EMPTY + s0]);
+                                mma_commit(&bars[C::B_EMPTY + s0 + 1]);
+                            }
+                            mma_commit(&bars[C::B_PVDONE + pb]);
+                        }
+                        __syncwarp();
                         advance(pc);
                         progressed = true;
                     }
@@ -452,30 +497,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                    ((fk + s) / NSLOT) & 1);
                     if (ready) {
                         fence_after_sync();
-                        const uint32_t qaddr = qs_a + (qc.k % QB) * C::Q_BUF;
+                        if (leader) {
+                            const uint64_t qbase =
+                                smem_desc_sw128(qs_a + (qc.k % QB) * C::Q_BUF, 16, 1024);
 #pragma unroll
-                        for (int s = 0; s < SLABS; ++s) {
-                            const uint32_t slot = (fk + s) % NSLOT;
+                            for (int s = 0; s < SLABS; ++s) {
+                                const uint32_t slot = (fk + s) % NSLOT;
+                                const uint64_t abase =
+                                    smem_desc_sw128(ring_a + slot * C::SLOT_BYTES, 16, 1024);
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk) {
-                                const uint64_t a = smem_desc_sw128(
-                                    ring_a + slot * C::SLOT_BYTES + kk * 32, 16, 1024);
-                                const uint64_t bdesc =
-                                    smem_desc_sw128(qaddr + s * C::Q_SLAB + kk * 32, 16, 1024);
-                                mma_bf16_ss(tmem + sb * N, a, bdesc, ID_QK, (s | kk) != 0);
+                                for (int kk = 0; kk < 4; ++kk)
+                                    mma_bf16_ss(tmem + sb * N, abase + (uint64_t)(kk * 2),
+                                                qbase + (uint64_t)(s * (C::Q_SLAB >> 4) + kk * 2),
+                                                ID_QK, (s | kk) != 0);
+                                mma_commit(&bars[C::B_EMPTY + slot]);
                             }
-                            mma_commit(&bars[C::B_EMPTY + slot]);
+                            mma_commit(&bars[C::B_SFULL + sb]);
+                            if (qc.t == qc.n_tiles - 1)
+                                mma_commit(&bars[C::B_QEMPTY + qc.k % QB]);
                         }
-                        mma_commit(&bars[C::B_SFULL + sb]);
-                        if (qc.t == qc.n_tiles - 1) mma_commit(&bars[C::B_QEMPTY + qc.k % QB]);
+                        __syncwarp();
                         advance(qc);
                         progressed = true;
                     }
                 }
                 if (progressed) {
                     idle_since = clock64();
+                    idle = 0;
                 } else if (clock64() - idle_since < kWaitLimitCycles) {
-                    __nanosleep(20);  // leave issue slots to the softmax warps
+                    if (++idle > 8) __nanosleep(32);  // leave issue slots to the softmax warps
                 } else {
                     atomicOr(P.fault, kFaultCopyTimeout);
                     ok = false;
@@ -484,8 +534,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             (void)ok;
             // all issued MMAs complete before TMEM is released
-            mma_commit(&bars[C::B_DRAIN]);
-            mbar_wait_bounded(&bars[C::B_DRAIN], 0, P.fault, kFaultCopyTimeout);
+            if (leader) {
+                mma_commit(&bars[C::B_DRAIN]);
+                mbar_wait_bounded(&bars[C::B_DRAIN], 0, P.fault, kFaultCopyTimeout);
+            }
+            __syncwarp();
         }
     } else {
         // ===================================================== softmax
@@ -671,29 +724,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     *reinterpret_cast<__nv_bfloat16 *>(pt + C::P_LO + off) = lo;
                     lrow[r] += p;
                 }
-                // Keys past the chunk's end: their V rows are zeroed (by the
-                // first group) so that 0 * (whatever the slot holds there)
-                // cannot reach O.
-                if (n_valid < kTcTileKeys && wg == 0) {
-                    const uint32_t fv = fbase + (uint32_t)t * 2 * SLABS + SLABS;
-                    bool vok = true;
-#pragma unroll
-                    for (int s = 0; s < SLABS; ++s)
-                        vok = vok && mbar_wait_bounded(&bars[C::B_FULL + (fv + s) % NSLOT],
-                                                       ((fv + s) / NSLOT) & 1, P.fault,
-                                                       kFaultCopyTimeout);
-                    ok = !group_any(wg, !vok);
-                    if (!ok) break;
-                    if (lk >= n_valid) {
-#pragma unroll
-                        for (int s = 0; s < SLABS; ++s) {
-                            uint4 *row = reinterpret_cast<uint4 *>(
-                                ring + ((fv + s) % NSLOT) * C::SLOT_BYTES + lk * 128);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) row[q] = make_uint4(0, 0, 0, 0);
-                        }
-                    }
-                }
                 fence_proxy_async_smem();
                 mbar_arrive(&bars[C::B_PFULL + pb]);
             }
@@ -740,11 +770,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             group_sync(wg);
             // O^T through shared memory (the P buffers are idle now) into
-            // 16-byte row stores
+            // 16-byte row stores: a bf16 row of D dims at a time, an fp32
+            // partial row in halves of 128 dims
             uint8_t *stg = ps;
             const bool part = P.splits > 1;
+            if (!part) {
 #pragma unroll 1
-            for (int mh = 0; mh < MH; ++mh) {
+                for (int mh = 0; mh < MH; ++mh) {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < HN; c0 += OW) {
+                        uint32_t o[OW];
+                        tmem_load<OW>(tl + C::O_COL + (ob * MH + mh) * N + r0 + c0, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < OW; ++e) {
+                            const int r = r0 + c0 + e;
+                            *reinterpret_cast<__nv_bfloat16 *>(stg + r * (D * 2) +
+                                                               (mh * 128 + lk) * 2) =
+                                __float2bfloat16_rn(__uint_as_float(o[e]) * linv[r]);
+                        }
+                    }
+                }
+                fence_before_sync();
+                mbar_arrive(&bars[C::B_OFREE + ob]);  // O buffer may be reused
+                group_sync(wg);
+                constexpr int CPR = D / 8;  // 16-byte chunks per row
+                for (int idx = gtid; idx < my_rows * CPR; idx += 128) {
+                    const int r = r0 + idx / CPR, c = idx % CPR;
+                    const int rg = it.row0 + r;
+                    const int i = rg / P.G, gg = rg - i * P.G;
+                    const size_t orow =
+                        ((size_t)it.b * P.q_len + i) * P.Hq + (size_t)it.h * P.G + gg;
+                    *reinterpret_cast<uint4 *>(P.out + orow * D + c * 8) =
+                        *reinterpret_cast<const uint4 *>(stg + r * (D * 2) + c * 16);
+                }
+                group_sync(wg);
+            }
+#pragma unroll 1
+            for (int mh = 0; mh < MH && part; ++mh) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < HN; c0 += OW) {
                     uint32_t o[OW];
