@@ -19,11 +19,13 @@ template <int D, int N>
 struct Conf {
     // A ring of three K-or-V tiles lets V(t+1) load while V(t) waits for its
     // PV; at head_dim 256 that is 12 slots, which leaves room for one Q and
-    // one P buffer beside it (two at 16 rows).
+    // one P buffer beside it (two at 16 rows).  O^T (2N columns per head-dim
+    // half) is double-buffered unless TMEM runs out (head_dim 256, 64 rows).
     static constexpr int NSLOT = D == 256 ? (N <= 32 ? 12 : 8) : 10;
     static constexpr int QB = (D == 256 && N >= 32) ? 1 : (D == 128 && N == 64) ? 1 : 2;
     static constexpr int PB = (D == 256 && N >= 32) ? 1 : (N == 64) ? 1 : 2;
-    using C = TcCfg<D, N, NSLOT, QB, PB>;
+    static constexpr int OB = (D == 256 && N == 64) ? 1 : 2;
+    using C = TcCfg<D, N, NSLOT, QB, PB, OB>;
 };
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -45,7 +47,7 @@ template <int D, int N>
 cudaError_t launch(const TcLaunch &L, const CUtensorMap *maps, cudaStream_t stream) {
     using Cf = Conf<D, N>;
     using C = typename Cf::C;
-    auto kern = swa_tc_kernel<D, N, Cf::NSLOT, Cf::QB, Cf::PB>;
+    auto kern = swa_tc_kernel<D, N, Cf::NSLOT, Cf::QB, Cf::PB, Cf::OB>;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);

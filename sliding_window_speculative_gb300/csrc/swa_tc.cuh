@@ -13,7 +13,9 @@
 //
 // P is carried into the second MMA as two bf16 tiles, P = P_hi + P_lo with
 // P_hi = bf16(P) and P_lo = bf16(P - P_hi), so the weights keep about 16
-// significant bits instead of bf16's 8; the PV product is issued twice.
+// significant bits instead of bf16's 8.  The two tiles are stacked as one
+// B operand of 2N rows (an M=128 MMA costs the same up to N=64), and O^T
+// holds 2N columns whose halves the epilogue adds.
 //
 // K and V arrive by TMA in 16 KB slabs (128 keys x 64 dims, 128-byte
 // swizzle) through a ring of shared-memory slots; a tile with fewer than 128
@@ -55,15 +57,14 @@ constexpr int kTcTileKeys = 128;
 constexpr int kTcTailBox = 32;    // keys per box of a partial tile
 constexpr int kTcMetaItems = 16;  // items per CTA whose metadata is cached in smem
 
-template <int D, int N, int NSLOT, int QB, int PB>
+template <int D, int N, int NSLOT, int QB, int PB, int OB>
 struct TcCfg {
     static constexpr int SLABS = D / 64;
     static constexpr int SLOT_BYTES = 16384;
     static constexpr int Q_SLAB = N * 128;
     static constexpr int Q_BUF = SLABS * Q_SLAB;
-    static constexpr int P_SLAB = N * 128;
-    static constexpr int P_LO = 2 * P_SLAB;   // P_lo after P_hi (2 key slabs each)
-    static constexpr int P_BUF = 4 * P_SLAB;  // hi + lo
+    static constexpr int P_KSLAB = 2 * N * 128;  // 64 keys x (N hi + N lo rows)
+    static constexpr int P_BUF = 2 * P_KSLAB;     // 128 keys
     static constexpr int RING_OFF = 0;
     static constexpr int Q_OFF = RING_OFF + NSLOT * SLOT_BYTES;
     static constexpr int P_OFF = Q_OFF + QB * Q_BUF;
@@ -73,7 +74,7 @@ struct TcCfg {
     static constexpr int META_OFF = ALPHA_OFF + N * 4;        // int [2][kTcMetaItems]
     static constexpr int BAR_OFF = META_OFF + 2 * kTcMetaItems * 4;
     // ring full/empty, q full/empty [QB], s full/free [2], p full [PB],
-    // pv done [PB], o free [2], drain
+    // pv done [PB], o free [2] (OB used), drain
     static constexpr int B_FULL = 0, B_EMPTY = NSLOT, B_QFULL = 2 * NSLOT,
                          B_QEMPTY = B_QFULL + QB, B_SFULL = B_QEMPTY + QB, B_SFREE = B_SFULL + 2,
                          B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + PB, B_OFREE = B_PVDONE + PB,
@@ -81,13 +82,14 @@ struct TcCfg {
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base
     static constexpr int END = MISC_OFF + 16;
     static constexpr int SMEM_BYTES = END + 1024;  // slack for 1024-byte alignment
-    static constexpr int TMEM_USED = 2 * N + 2 * (D / 128) * N;
+    static constexpr int O_COLS = (D / 128) * 2 * N;  // one O^T buffer: hi and lo halves
+    static constexpr int TMEM_USED = 2 * N + OB * O_COLS;
     static constexpr int TMEM_COLS = TMEM_USED <= 32    ? 32
                                      : TMEM_USED <= 64  ? 64
                                      : TMEM_USED <= 128 ? 128
                                      : TMEM_USED <= 256 ? 256
                                                         : 512;
-    static constexpr int O_COL = 2 * N;           // O buffer ob at O_COL + ob * (D/128) * N
+    static constexpr int O_COL = 2 * N;           // O buffer ob at O_COL + ob * O_COLS
     static constexpr int CW = N >= 32 ? 32 : 16;  // TMEM columns per load
     static constexpr int NCH = N / CW;
     static_assert(NSLOT % 2 == 0 && NSLOT >= 2 * SLABS, "ring holds a K and a V tile, V in pairs");
@@ -198,14 +200,14 @@ __device__ __forceinline__ void tmem_store(uint32_t taddr, const uint32_t *r) {
     }
 }
 
-template <int D, int N, int NSLOT, int QB, int PB>
+template <int D, int N, int NSLOT, int QB, int PB, int OB>
 __global__ void __launch_bounds__(kTcThreads, 1)
     swa_tc_kernel(const __grid_constant__ TcParams T, const __grid_constant__ CUtensorMap map_k,
                   const __grid_constant__ CUtensorMap map_v,
                   const __grid_constant__ CUtensorMap map_k32,
                   const __grid_constant__ CUtensorMap map_v32,
                   const __grid_constant__ CUtensorMap map_q) {
-    using C = TcCfg<D, N, NSLOT, QB, PB>;
+    using C = TcCfg<D, N, NSLOT, QB, PB, OB>;
     using namespace tc;
     constexpr int SLABS = C::SLABS;
     constexpr int MH = D / 128;
@@ -364,7 +366,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         {
             const bool leader = lane == 0;
             constexpr uint32_t ID_QK = idesc_bf16_f32(128, N, 0, 0);
-            constexpr uint32_t ID_PV = idesc_bf16_f32(128, N, 1, 0);
+            constexpr uint32_t ID_PV = idesc_bf16_f32(128, 2 * N, 1, 0);
             const uint32_t ring_a = smem_u32(ring);
             const uint32_t qs_a = smem_u32(qs);
             const uint32_t ps_a = smem_u32(ps);
@@ -415,7 +417,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t fv = pc.fbase + (uint32_t)pc.t * 2 * SLABS + SLABS;
                     bool ready = mbar_test(&bars[C::B_PFULL + pb], (pc.g / PB) & 1);
                     if (ready && pc.t == 0)
-                        ready = mbar_test(&bars[C::B_OFREE + (pc.k & 1)], ((pc.k >> 1) & 1) ^ 1);
+                        ready = mbar_test(&bars[C::B_OFREE + pc.k % OB], ((pc.k / OB) & 1) ^ 1);
 #pragma unroll
                     for (int s = 0; s < SLABS; ++s)
                         ready = ready && mbar_test(&bars[C::B_FULL + (fv + s) % NSLOT],
@@ -445,7 +447,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             // units in the low bits), so offsets are added to a base
                             const uint64_t bbase =
                                 smem_desc_sw128(ps_a + pb * C::P_BUF, 16, 1024);
-                            const uint32_t ob = pc.k & 1;
+                            const uint32_t ob = pc.k % OB;
                             const uint32_t acc0 = pc.t > 0 ? 1u : 0u;
 #pragma unroll
                             for (int mh = 0; mh < MH; ++mh) {
@@ -453,27 +455,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                 // A = V^T: MN-major, the two 64-dim slabs one slot apart
                                 const uint64_t abase = smem_desc_sw128(
                                     ring_a + s0 * C::SLOT_BYTES, C::SLOT_BYTES, 1024);
-                                const uint32_t d_t = tmem + C::O_COL + (ob * MH + mh) * N;
-                                // B = P_hi for the first pass, then P_lo
+                                const uint32_t d_t = tmem + C::O_COL + ob * C::O_COLS + mh * 2 * N;
+                                // B = [P_hi; P_lo], 2N rows
                                 if (steps == 8) {
 #pragma unroll
-                                    for (int kk = 0; kk < 16; ++kk) {
-                                        const int hl = kk >> 3, k8 = kk & 7;
+                                    for (int k8 = 0; k8 < 8; ++k8)
                                         mma_bf16_ss(d_t, abase + (uint64_t)(k8 * 128),
-                                                    bbase + (uint64_t)(hl * (C::P_LO >> 4) +
-                                                                       (k8 >> 2) * (C::P_SLAB >> 4) +
+                                                    bbase + (uint64_t)((k8 >> 2) * (C::P_KSLAB >> 4) +
                                                                        (k8 & 3) * 2),
-                                                    ID_PV, (acc0 | (uint32_t)kk) != 0);
-                                    }
+                                                    ID_PV, (acc0 | (uint32_t)k8) != 0);
                                 } else {
-                                    for (int kk = 0; kk < 2 * steps; ++kk) {
-                                        const int hl = kk >= steps, k8 = hl ? kk - steps : kk;
+                                    for (int k8 = 0; k8 < steps; ++k8)
                                         mma_bf16_ss(d_t, abase + (uint64_t)(k8 * 128),
-                                                    bbase + (uint64_t)(hl * (C::P_LO >> 4) +
-                                                                       (k8 >> 2) * (C::P_SLAB >> 4) +
+                                                    bbase + (uint64_t)((k8 >> 2) * (C::P_KSLAB >> 4) +
                                                                        (k8 & 3) * 2),
-                                                    ID_PV, (acc0 | (uint32_t)kk) != 0);
-                                    }
+                                                    ID_PV, (acc0 | (uint32_t)k8) != 0);
                                 }
                                 mma_commit(&bars[C::B_EMPTY + s0]);
                                 mma_commit(&bars[C::B_EMPTY + s0 + 1]);
@@ -525,7 +521,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     idle_since = clock64();
                     idle = 0;
                 } else if (clock64() - idle_since < kWaitLimitCycles) {
-                    if (++idle > 8) __nanosleep(32);  // leave issue slots to the softmax warps
+                    ++idle;
                 } else {
                     atomicOr(P.fault, kFaultCopyTimeout);
                     ok = false;
@@ -555,7 +551,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
         // P^T address pieces of this thread's key: the 16-byte chunk index
         // of key lk inside a 128-byte row is XORed with (row & 7)
-        const uint32_t p_key = (uint32_t)(lk >> 6) * C::P_SLAB + (uint32_t)(lk & 7) * 2;
+        const uint32_t p_key = (uint32_t)(lk >> 6) * C::P_KSLAB + (uint32_t)(lk & 7) * 2;
         const uint32_t p_chunk = (uint32_t)(lk & 63) >> 3;
         uint32_t g = 0, k = 0, fbase = 0;
         bool ok = true;
@@ -585,7 +581,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 continue;
             }
-            const uint32_t ob = k & 1;
+            const uint32_t ob = k % OB;
+            const uint32_t ocol0 = tl + C::O_COL + ob * C::O_COLS;  // this lane's O^T row
             float mref[HN], lrow[HN];
 #pragma unroll
             for (int r = 0; r < HN; ++r) {
@@ -683,12 +680,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if (!ok) break;
                         fence_after_sync();  // (the vote also published alpha_sm)
 #pragma unroll 1
-                        for (int mh = 0; mh < MH; ++mh) {
+                        for (int mh = 0; mh < 2 * MH; ++mh) {  // hi and lo halves of each
 #pragma unroll 1
                             for (int c0 = 0; c0 < HN; c0 += OW) {
                                 uint32_t o[OW];
-                                const uint32_t ocol =
-                                    tl + C::O_COL + (ob * MH + mh) * N + r0 + c0;
+                                const uint32_t ocol = ocol0 + mh * N + r0 + c0;
                                 tmem_load<OW>(ocol, o);
                                 tmem_wait_ld();
 #pragma unroll
@@ -719,9 +715,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const __nv_bfloat16 hi = __float2bfloat16_rn(p);
                     const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
                     const int rr = r0 + r;
-                    const uint32_t off = (uint32_t)rr * 128 + ((p_chunk ^ (uint32_t)(rr & 7)) << 4);
-                    *reinterpret_cast<__nv_bfloat16 *>(pt + off) = hi;
-                    *reinterpret_cast<__nv_bfloat16 *>(pt + C::P_LO + off) = lo;
+                    const uint32_t rl = (uint32_t)(N + rr);  // P_lo row, same (rr & 7)
+                    const uint32_t sw = (p_chunk ^ (uint32_t)(rr & 7)) << 4;
+                    *reinterpret_cast<__nv_bfloat16 *>(pt + (uint32_t)rr * 128 + sw) = hi;
+                    *reinterpret_cast<__nv_bfloat16 *>(pt + rl * 128 + sw) = lo;
                     lrow[r] += p;
                 }
                 fence_proxy_async_smem();
@@ -779,15 +776,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int mh = 0; mh < MH; ++mh) {
 #pragma unroll 1
                     for (int c0 = 0; c0 < HN; c0 += OW) {
-                        uint32_t o[OW];
-                        tmem_load<OW>(tl + C::O_COL + (ob * MH + mh) * N + r0 + c0, o);
+                        uint32_t o[OW], ol[OW];
+                        tmem_load<OW>(ocol0 + mh * 2 * N + r0 + c0, o);
+                        tmem_load<OW>(ocol0 + mh * 2 * N + N + r0 + c0, ol);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < OW; ++e) {
                             const int r = r0 + c0 + e;
+                            const float ov = __uint_as_float(o[e]) + __uint_as_float(ol[e]);
                             *reinterpret_cast<__nv_bfloat16 *>(stg + r * (D * 2) +
                                                                (mh * 128 + lk) * 2) =
-                                __float2bfloat16_rn(__uint_as_float(o[e]) * linv[r]);
+                                __float2bfloat16_rn(ov * linv[r]);
                         }
                     }
                 }
@@ -810,18 +809,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int mh = 0; mh < MH && part; ++mh) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < HN; c0 += OW) {
-                    uint32_t o[OW];
-                    tmem_load<OW>(tl + C::O_COL + (ob * MH + mh) * N + r0 + c0, o);
+                    uint32_t o[OW], ol[OW];
+                    tmem_load<OW>(ocol0 + mh * 2 * N + r0 + c0, o);
+                    tmem_load<OW>(ocol0 + mh * 2 * N + N + r0 + c0, ol);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < OW; ++e) {
                         const int r = r0 + c0 + e;
-                        const float ov = __uint_as_float(o[e]);
-                        if (part)
-                            *reinterpret_cast<float *>(stg + r * 512 + lk * 4) = ov;
-                        else
-                            *reinterpret_cast<__nv_bfloat16 *>(stg + r * 256 + lk * 2) =
-                                __float2bfloat16_rn(ov * linv[r]);
+                        *reinterpret_cast<float *>(stg + r * 512 + lk * 4) =
+                            __uint_as_float(o[e]) + __uint_as_float(ol[e]);
                     }
                 }
                 if (mh == MH - 1) {
