@@ -372,6 +372,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t ps_a = smem_u32(ps);
             struct Cursor {
                 int item, j, t, n_tiles;
+                int last_keys;  // keys of the item's last tile
                 uint32_t k, fbase, g;
                 bool valid;
             };
@@ -381,6 +382,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const TcItem it = tc_decode(T, c.item, c.j, meta_sl, meta_qp);
                     if (it.n_tiles > 0) {
                         c.n_tiles = it.n_tiles;
+                        c.last_keys = it.cr.c_hi - it.cr.c_lo - kTcTileKeys * (it.n_tiles - 1);
                         c.t = 0;
                         c.valid = true;
                         return;
@@ -397,13 +399,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ++c.j;
                 seek(c);
             };
-            // keys of tile t of the cursor's item (the chunk end is known from the
-            // item; tc_decode is repeated only when a tile is partial)
-            auto tile_keys = [&](const Cursor &c) -> int {
-                const TcItem it = tc_decode(T, c.item, c.j, meta_sl, meta_qp);
-                return min(kTcTileKeys, it.cr.c_hi - it.cr.c_lo - kTcTileKeys * c.t);
-            };
-            Cursor qc{(int)blockIdx.x, 0, 0, 0, 0u, 0u, 0u, false};
+            Cursor qc{(int)blockIdx.x, 0, 0, 0, 0, 0u, 0u, 0u, false};
             seek(qc);
             Cursor pc = qc;
             bool ok = true;
@@ -428,16 +424,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         // are multiplied; the rows of the last step past the chunk's
                         // end are zeroed first, so that 0 * (whatever the slot holds
                         // there) cannot reach O
-                        const int nv = pc.t == pc.n_tiles - 1 ? tile_keys(pc) : kTcTileKeys;
+                        const int nv = pc.t == pc.n_tiles - 1 ? pc.last_keys : kTcTileKeys;
                         const int steps = (nv + 15) >> 4;
                         if (nv & 15) {
-                            const int zr = steps * 16 - nv;  // rows to clear, < 16
-#pragma unroll 1
-                            for (int idx = lane; idx < SLABS * zr * 8; idx += 32) {
-                                const int s = idx / (zr * 8), rem = idx - s * zr * 8;
-                                const int row = nv + rem / 8, q = rem & 7;
-                                reinterpret_cast<uint4 *>(ring + ((fv + s) % NSLOT) * C::SLOT_BYTES +
-                                                          row * 128)[q] = make_uint4(0, 0, 0, 0);
+                            // rows [nv, 16 * steps) of every V slab: a lane clears one
+                            // 16-byte chunk of four rows per pass
+                            const int row = nv + (lane >> 3), q = lane & 7;
+#pragma unroll
+                            for (int s = 0; s < SLABS; ++s) {
+                                uint8_t *slab = ring + ((fv + s) % NSLOT) * C::SLOT_BYTES;
+#pragma unroll
+                                for (int r4 = 0; r4 < 16; r4 += 4)
+                                    if (row + r4 < steps * 16)
+                                        reinterpret_cast<uint4 *>(slab + (row + r4) * 128)[q] =
+                                            make_uint4(0, 0, 0, 0);
                             }
                             fence_proxy_async_smem();
                             __syncwarp();
@@ -706,6 +706,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                            kFaultCopyTimeout));
                     if (!ok) break;
                 }
+                // the previous item's epilogue staged its output in the P buffers
+                if (t == 0 && k > 0) group_sync(wg);
                 // P = 2^(s - m_ref) as bf16 hi + lo into the swizzled P^T tiles
                 uint8_t *pt = ps + pb * C::P_BUF + p_key;
 #pragma unroll
@@ -727,12 +729,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (!ok) break;
 
             // -------------------------------------------------- epilogue
-            const uint32_t gl = g - 1;  // the item's last tile
-            ok = !group_any(wg, !mbar_wait_bounded(&bars[C::B_PVDONE + gl % PB], (gl / PB) & 1,
-                                                   P.fault, kFaultCopyTimeout));
-            if (!ok) break;
-            fence_after_sync();
-            // row sums: lanes, then the group's four warps
+            // row sums (they do not depend on the last PV): lanes, then the
+            // group's four warps
             float *rl = red + (g & 1) * 4 * N + r0;
 #pragma unroll
             for (int c = 0; c < NCH; ++c) {
@@ -765,12 +763,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     P.part_ml[prow * 2 + 1] = l;
                 }
             }
-            group_sync(wg);
+            const uint32_t gl = g - 1;  // the item's last tile
+            ok = !group_any(wg, !mbar_wait_bounded(&bars[C::B_PVDONE + gl % PB], (gl / PB) & 1,
+                                                   P.fault, kFaultCopyTimeout));
+            if (!ok) break;
+            fence_after_sync();  // (the vote also published linv)
             // O^T through shared memory (the P buffers are idle now) into
             // 16-byte row stores: a bf16 row of D dims at a time, an fp32
-            // partial row in halves of 128 dims
-            uint8_t *stg = ps;
+            // partial row in halves of 128 dims.  A group stages its rows only
+            // in the bytes of its own P rows (hi and lo, both key slabs), so
+            // the other group's P writes for the next item cannot collide.
             const bool part = P.splits > 1;
+            const int RB = part ? 512 : D * 2;   // staged bytes per row
+            const int RPC = HN * 128 / RB;       // rows per 128-byte-row chunk of the group
+            auto stg_row = [&](int rr) -> uint8_t * {
+                const int c = rr / RPC;
+                return ps + (c >> 1) * C::P_KSLAB + ((c & 1) * N + r0) * 128 + (rr % RPC) * RB;
+            };
             if (!part) {
 #pragma unroll 1
                 for (int mh = 0; mh < MH; ++mh) {
@@ -784,7 +793,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         for (int e = 0; e < OW; ++e) {
                             const int r = r0 + c0 + e;
                             const float ov = __uint_as_float(o[e]) + __uint_as_float(ol[e]);
-                            *reinterpret_cast<__nv_bfloat16 *>(stg + r * (D * 2) +
+                            *reinterpret_cast<__nv_bfloat16 *>(stg_row(c0 + e) +
                                                                (mh * 128 + lk) * 2) =
                                 __float2bfloat16_rn(ov * linv[r]);
                         }
@@ -801,9 +810,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const size_t orow =
                         ((size_t)it.b * P.q_len + i) * P.Hq + (size_t)it.h * P.G + gg;
                     *reinterpret_cast<uint4 *>(P.out + orow * D + c * 8) =
-                        *reinterpret_cast<const uint4 *>(stg + r * (D * 2) + c * 16);
+                        *reinterpret_cast<const uint4 *>(stg_row(r - r0) + c * 16);
                 }
-                group_sync(wg);
+                // (the group synchronises again before the staging area, a P
+                // buffer, is written by the next item)
             }
 #pragma unroll 1
             for (int mh = 0; mh < MH && part; ++mh) {
@@ -814,11 +824,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tmem_load<OW>(ocol0 + mh * 2 * N + N + r0 + c0, ol);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < OW; ++e) {
-                        const int r = r0 + c0 + e;
-                        *reinterpret_cast<float *>(stg + r * 512 + lk * 4) =
+                    for (int e = 0; e < OW; ++e)
+                        *reinterpret_cast<float *>(stg_row(c0 + e) + lk * 4) =
                             __uint_as_float(o[e]) + __uint_as_float(ol[e]);
-                    }
                 }
                 if (mh == MH - 1) {
                     fence_before_sync();
@@ -829,8 +837,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int idx = gtid; idx < my_rows * cpr; idx += 128) {
                     const int r = r0 + idx / cpr, c = idx % cpr;
                     const int rg = it.row0 + r;
-                    const uint4 val =
-                        *reinterpret_cast<const uint4 *>(stg + r * (cpr * 16) + c * 16);
+                    const uint4 val = *reinterpret_cast<const uint4 *>(stg_row(r - r0) + c * 16);
                     if (part) {
                         const size_t prow = (bh * P.splits + it.split) * P.R + rg;
                         *reinterpret_cast<uint4 *>(P.part_acc + prow * D + mh * 128 + c * 4) = val;
