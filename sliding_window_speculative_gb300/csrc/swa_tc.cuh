@@ -487,10 +487,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const uint32_t fk = qc.fbase + (uint32_t)qc.t * 2 * SLABS;
                     bool ready = mbar_test(&bars[C::B_SFREE + sb], ((qc.g >> 1) & 1) ^ 1) &&
                                  mbar_test(&bars[C::B_QFULL + qc.k % QB], (qc.k / QB) & 1);
+                    // A parity test is only meaningful when the slot's previous
+                    // fill has completed its phase, i.e. has been consumed.  The
+                    // previous fill of a K slab can be a V slab of an earlier tile
+                    // whose PV is still pending: then the slot is not ours yet.
 #pragma unroll
-                    for (int s = 0; s < SLABS; ++s)
-                        ready = ready && mbar_test(&bars[C::B_FULL + (fk + s) % NSLOT],
-                                                   ((fk + s) / NSLOT) & 1);
+                    for (int s = 0; s < SLABS; ++s) {
+                        const uint32_t fi = fk + s;
+                        if (fi >= (uint32_t)NSLOT) {
+                            const uint32_t fp = fi - NSLOT;
+                            if (fp % (2 * SLABS) >= (uint32_t)SLABS && pc.g <= fp / (2 * SLABS))
+                                ready = false;
+                        }
+                        ready = ready && mbar_test(&bars[C::B_FULL + fi % NSLOT], (fi / NSLOT) & 1);
+                    }
                     if (ready) {
                         fence_after_sync();
                         if (leader) {
