@@ -357,6 +357,18 @@ def oracle_sample(case, budget_s=10.0, max_calls=None, threads=None):
 
 # ------------------------------------------------------------------- main
 
+def aggregate(seconds, bytes_per_step, steps, dist=None, device="cpu"):
+    """Whole-job throughput: the slowest rank's time, every rank's bytes.
+    Returns (max seconds over ranks, aggregate GB/s)."""
+    world = 1
+    secs = torch.tensor([float(seconds)], dtype=torch.float64, device=device)
+    if dist is not None:
+        world = dist.get_world_size()
+        dist.all_reduce(secs, op=dist.ReduceOp.MAX)
+    slowest = float(secs.item())
+    return slowest, bytes_per_step * steps * world / slowest / 1e9
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -412,11 +424,7 @@ def main():
     sampler = ClockSampler(local)
     r = time_device(case, args.steps, args.warmup, args.splits, dist=dist)
     clocks = sampler.stop(*r["wall"])
-    secs = torch.tensor([r["seconds"]], device=dev)
-    if dist is not None:
-        dist.all_reduce(secs, op=dist.ReduceOp.MAX)
-    seconds = float(secs.item())
-    value = kv * args.steps * world / seconds / 1e9
+    seconds, value = aggregate(r["seconds"], kv, args.steps, dist, dev)
     us = seconds * 1e6 / args.steps
 
     peak, peak_src = peaks()
