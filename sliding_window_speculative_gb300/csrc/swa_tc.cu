@@ -13,19 +13,19 @@
 namespace swa {
 namespace {
 
-// Per (head_dim, padded rows): ring slots of 16 KB and Q / P buffer counts,
-// sized to one CTA per SM (at most 227 KB of shared memory).
+// Per (head_dim, padded rows): ring slots of one 128-key tile and Q / P
+// buffer counts, sized to one CTA per SM (at most 227 KB of shared memory).
 template <int D, int N>
 struct Conf {
     // A ring of three K-or-V tiles lets V(t+1) load while V(t) waits for its
-    // PV; at head_dim 256 that is 12 slots, which leaves room for one Q and
-    // one P buffer beside it (two at 16 rows).  O^T (2N columns per head-dim
-    // half) is double-buffered unless TMEM runs out (head_dim 256, 64 rows).
-    static constexpr int NSLOT = D == 256 ? (N <= 32 ? 12 : 8) : 10;
+    // PV; at head_dim 256 (64 KB tiles) that leaves room for one Q and one P
+    // buffer beside it (two at 16 rows).  O^T (2N columns per head-dim half)
+    // is double-buffered unless TMEM runs out (head_dim 256, 64 rows).
+    static constexpr int NT = D == 256 ? (N <= 32 ? 3 : 2) : 5;
     static constexpr int QB = (D == 256 && N >= 32) ? 1 : (D == 128 && N == 64) ? 1 : 2;
     static constexpr int PB = (D == 256 && N >= 32) ? 1 : (N == 64) ? 1 : 2;
     static constexpr int OB = (D == 256 && N == 64) ? 1 : 2;
-    using C = TcCfg<D, N, NSLOT, QB, PB, OB>;
+    using C = TcCfg<D, N, NT, QB, PB, OB>;
 };
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -44,10 +44,10 @@ bool load_encode() {
 }
 
 template <int D, int N>
-cudaError_t launch(const TcLaunch &L, const CUtensorMap *maps, cudaStream_t stream) {
+cudaError_t launch(const TcLaunch &L, const TcMaps &maps, cudaStream_t stream) {
     using Cf = Conf<D, N>;
     using C = typename Cf::C;
-    auto kern = swa_tc_kernel<D, N, Cf::NSLOT, Cf::QB, Cf::PB, Cf::OB>;
+    auto kern = swa_tc_kernel<D, N, Cf::NT, Cf::QB, Cf::PB, Cf::OB>;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -57,13 +57,12 @@ cudaError_t launch(const TcLaunch &L, const CUtensorMap *maps, cudaStream_t stre
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    kern<<<L.grid, kTcThreads, C::SMEM_BYTES, stream>>>(L.T, maps[0], maps[1], maps[2], maps[3],
-                                                         maps[4]);
+    kern<<<L.grid, kTcThreads, C::SMEM_BYTES, stream>>>(L.T, maps);
     return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_d(const TcLaunch &L, const CUtensorMap *maps, cudaStream_t s) {
+cudaError_t launch_d(const TcLaunch &L, const TcMaps &maps, cudaStream_t s) {
     switch (L.N) {
         case 16: return launch<D, 16>(L, maps, s);
         case 32: return launch<D, 32>(L, maps, s);
@@ -75,7 +74,7 @@ cudaError_t launch_d(const TcLaunch &L, const CUtensorMap *maps, cudaStream_t s)
 template <int D, int N>
 void conf_info(TcConfInfo *c) {
     using C = typename Conf<D, N>::C;
-    c->nslot = Conf<D, N>::NSLOT;
+    c->nslot = Conf<D, N>::NT;
     c->smem_bytes = C::SMEM_BYTES;
     c->tmem_cols = C::TMEM_COLS;
     c->ctas_per_sm = 1;  // persistent: one CTA per SM
@@ -107,25 +106,33 @@ cudaError_t tc_launch(const TcLaunch &L, cudaStream_t stream, char *err, size_t 
     }
     const AttnParams &P = L.T.a;
     const int D = L.D;
-    // maps: K and V cache viewed as [B * Hkv * L rows, D] in boxes of 128 and
-    // of 32 keys x 64 dims; queries viewed as [B * q_len, Hq, D] in boxes of
-    // (draft rows x G heads x 64 dims)
-    CUtensorMap maps[5];
-    {
-        cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)P.B * P.Hkv * (cuuint64_t)P.L};
-        cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-        cuuint32_t es[2] = {1, 1};
-        for (int m = 0; m < 4; ++m) {
-            cuuint32_t box[2] = {64, (cuuint32_t)(m < 2 ? kTcTileKeys : kTcTailBox)};
-            const void *base = (m & 1) ? L.v : L.k;
-            CUresult r = g_encode(&maps[m], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    // K and V cache viewed as rows of D bf16 (B * Hkv * L rows).  4D maps
+    // (x = 64 dims, y = row, z = 64-dim slab, w = 8-row atom; strides D*2,
+    // 128 and 8*D*2 bytes) with boxes of 16, 8, 4 and 2 atoms, and a 3D
+    // one-atom map (x, y, z) whose rows are bounds-checked one by one.
+    // Both land as [atom][slab][8 rows][128 bytes], 128-byte swizzled.
+    TcMaps maps;
+    const cuuint64_t rows = (cuuint64_t)P.B * P.Hkv * (cuuint64_t)P.L;
+    const cuuint32_t slabs = (cuuint32_t)(D / 64);
+    for (int kv = 0; kv < 2; ++kv) {
+        const void *base = kv ? L.v : L.k;
+        CUtensorMap *m4 = kv ? maps.v_atoms : maps.k_atoms;
+        for (int bi = 0; bi < 5; ++bi) {
+            const bool atom = bi == 4;
+            const cuuint32_t A = atom ? 1u : (16u >> bi);
+            cuuint64_t dims[4] = {64, rows, slabs, 16};
+            cuuint64_t strides[3] = {(cuuint64_t)D * 2, 128, (cuuint64_t)D * 2 * 8};
+            cuuint32_t box[4] = {64, 8, slabs, A};
+            cuuint32_t es[4] = {1, 1, 1, 1};
+            CUresult r = g_encode(atom ? (kv ? &maps.v_atom : &maps.k_atom) : &m4[bi],
+                                  CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, atom ? 3 : 4,
                                   const_cast<void *>(base), dims, strides, box, es,
                                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
             if (r != CUDA_SUCCESS) {
-                snprintf(err, errlen, "cuTensorMapEncodeTiled(%s cache) failed: %d",
-                         (m & 1) ? "V" : "K", (int)r);
+                snprintf(err, errlen, "cuTensorMapEncodeTiled(%s cache, %u-atom box) failed: %d",
+                         kv ? "V" : "K", (unsigned)A, (int)r);
                 return cudaErrorInvalidValue;
             }
         }
@@ -135,7 +142,7 @@ cudaError_t tc_launch(const TcLaunch &L, cudaStream_t stream, char *err, size_t 
         cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)P.Hq * D * 2};
         cuuint32_t box[3] = {64, (cuuint32_t)P.G, (cuuint32_t)L.T.q_rows_per_tile};
         cuuint32_t es[3] = {1, 1, 1};
-        CUresult r = g_encode(&maps[4], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+        CUresult r = g_encode(&maps.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                               const_cast<void *>(L.q), dims, strides, box, es,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

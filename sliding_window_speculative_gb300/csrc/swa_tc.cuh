@@ -17,9 +17,15 @@
 // B operand of 2N rows (an M=128 MMA costs the same up to N=64), and O^T
 // holds 2N columns whose halves the epilogue adds.
 //
-// K and V arrive by TMA in 16 KB slabs (128 keys x 64 dims, 128-byte
-// swizzle) through a ring of shared-memory slots; a tile with fewer than 128
-// keys is fetched in 32-key boxes.  Q, P and O are double-buffered (where
+// K and V arrive by TMA a whole tile at a time into a ring of tile slots.
+// A tile is laid out as 8-key atoms, each atom holding the D/64 head-dim
+// slabs of its 8 keys as 1024-byte 128-byte-swizzled blocks:
+//   [atom a][slab s][key row r][128 bytes]
+// A 4D tensor map (x = 64 dims, y = cache row, z = slab, w = atom) loads
+// 8*A consecutive rows from any start row in one copy, so a full tile is one
+// TMA and a partial tile of n keys at most five (binary decomposition of
+// n / 8 atoms, then a one-atom 3D box for the last n % 8 keys, whose rows
+// past the cache the TMA zero-fills).  Q, P and O are double-buffered (where
 // shared memory allows) so consecutive tiles and items overlap: the MMA lane
 // issues the next tile's S (across item boundaries) before the current
 // tile's PV, and the epilogue of one item runs while the next item's loads
@@ -57,28 +63,29 @@ constexpr int kTcTileKeys = 128;
 constexpr int kTcTailBox = 32;    // keys per box of a partial tile
 constexpr int kTcMetaItems = 16;  // items per CTA whose metadata is cached in smem
 
-template <int D, int N, int NSLOT, int QB, int PB, int OB>
+template <int D, int N, int NT, int QB, int PB, int OB>
 struct TcCfg {
     static constexpr int SLABS = D / 64;
-    static constexpr int SLOT_BYTES = 16384;
+    static constexpr int ATOM_BYTES = SLABS * 1024;            // 8 keys x D
+    static constexpr int TILE_BYTES = (kTcTileKeys / 8) * ATOM_BYTES;
     static constexpr int Q_SLAB = N * 128;
     static constexpr int Q_BUF = SLABS * Q_SLAB;
     static constexpr int P_KSLAB = 2 * N * 128;  // 64 keys x (N hi + N lo rows)
     static constexpr int P_BUF = 2 * P_KSLAB;     // 128 keys
     static constexpr int RING_OFF = 0;
-    static constexpr int Q_OFF = RING_OFF + NSLOT * SLOT_BYTES;
+    static constexpr int Q_OFF = RING_OFF + NT * TILE_BYTES;
     static constexpr int P_OFF = Q_OFF + QB * Q_BUF;
     static constexpr int RED_OFF = P_OFF + PB * P_BUF;        // float [2][4][N]
     static constexpr int LINV_OFF = RED_OFF + 2 * 4 * N * 4;  // float [N]
     static constexpr int ALPHA_OFF = LINV_OFF + N * 4;        // float [N]
     static constexpr int META_OFF = ALPHA_OFF + N * 4;        // int [2][kTcMetaItems]
     static constexpr int BAR_OFF = META_OFF + 2 * kTcMetaItems * 4;
-    // ring full/empty, q full/empty [QB], s full/free [2], p full [PB],
+    // ring full/empty [NT], q full/empty [QB], s full/free [2], p full [PB],
     // pv done [PB], o free [2] (OB used), drain
-    static constexpr int B_FULL = 0, B_EMPTY = NSLOT, B_QFULL = 2 * NSLOT,
-                         B_QEMPTY = B_QFULL + QB, B_SFULL = B_QEMPTY + QB, B_SFREE = B_SFULL + 2,
-                         B_PFULL = B_SFREE + 2, B_PVDONE = B_PFULL + PB, B_OFREE = B_PVDONE + PB,
-                         B_DRAIN = B_OFREE + 2, NBARS = B_DRAIN + 1;
+    static constexpr int B_FULL = 0, B_EMPTY = NT, B_QFULL = 2 * NT, B_QEMPTY = B_QFULL + QB,
+                         B_SFULL = B_QEMPTY + QB, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2,
+                         B_PVDONE = B_PFULL + PB, B_OFREE = B_PVDONE + PB, B_DRAIN = B_OFREE + 2,
+                         NBARS = B_DRAIN + 1;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base
     static constexpr int END = MISC_OFF + 16;
     static constexpr int SMEM_BYTES = END + 1024;  // slack for 1024-byte alignment
@@ -92,7 +99,7 @@ struct TcCfg {
     static constexpr int O_COL = 2 * N;           // O buffer ob at O_COL + ob * O_COLS
     static constexpr int CW = N >= 32 ? 32 : 16;  // TMEM columns per load
     static constexpr int NCH = N / CW;
-    static_assert(NSLOT % 2 == 0 && NSLOT >= 2 * SLABS, "ring holds a K and a V tile, V in pairs");
+    static_assert(NT >= 2, "ring holds at least a K and a V tile");
     static_assert(N % 16 == 0 && N >= 16 && N <= 64, "rows per tile");
     static_assert(TMEM_USED <= 512, "TMEM");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
@@ -200,14 +207,10 @@ __device__ __forceinline__ void tmem_store(uint32_t taddr, const uint32_t *r) {
     }
 }
 
-template <int D, int N, int NSLOT, int QB, int PB, int OB>
+template <int D, int N, int NT, int QB, int PB, int OB>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    swa_tc_kernel(const __grid_constant__ TcParams T, const __grid_constant__ CUtensorMap map_k,
-                  const __grid_constant__ CUtensorMap map_v,
-                  const __grid_constant__ CUtensorMap map_k32,
-                  const __grid_constant__ CUtensorMap map_v32,
-                  const __grid_constant__ CUtensorMap map_q) {
-    using C = TcCfg<D, N, NSLOT, QB, PB, OB>;
+    swa_tc_kernel(const __grid_constant__ TcParams T, const __grid_constant__ TcMaps M) {
+    using C = TcCfg<D, N, NT, QB, PB, OB>;
     using namespace tc;
     constexpr int SLABS = C::SLABS;
     constexpr int MH = D / 128;
@@ -234,7 +237,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     // ---------------------------------------------------------------- setup
     if (tid == 0) {
-        for (int i = 0; i < NSLOT; ++i) {
+        for (int i = 0; i < NT; ++i) {
             mbar_init(&bars[C::B_FULL + i], 1);
             mbar_init(&bars[C::B_EMPTY + i], 1);
         }
@@ -280,13 +283,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0) {
         // ======================================================= producer
         if (lane == 0) {
-            prefetch_tmap(&map_k);
-            prefetch_tmap(&map_v);
-            prefetch_tmap(&map_k32);
-            prefetch_tmap(&map_v32);
-            prefetch_tmap(&map_q);
+            prefetch_tmap(&M.k_atoms[0]);
+            prefetch_tmap(&M.v_atoms[0]);
+            prefetch_tmap(&M.k_atom);
+            prefetch_tmap(&M.v_atom);
+            prefetch_tmap(&M.q);
             const uint64_t policy = l2_policy_evict_first();
-            uint32_t f = 0, k = 0;
+            uint32_t f = 0, k = 0;  // fills (two per tile: K then V), items with keys
             bool ok = true;
             int j = 0;
             for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
@@ -301,7 +304,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         return false;
                     mbar_arrive_expect_tx(&bars[C::B_QFULL + qb], SLABS * T.rows_per_tile * 128);
                     for (int s = 0; s < SLABS; ++s)
-                        tma_load_3d(qs + qb * C::Q_BUF + s * C::Q_SLAB, &map_q, 64 * s,
+                        tma_load_3d(qs + qb * C::Q_BUF + s * C::Q_SLAB, &M.q, 64 * s,
                                     it.h * P.G, it.b * P.q_len + it.i0, &bars[C::B_QFULL + qb]);
                     return true;
                 };
@@ -310,43 +313,57 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int t = 0; t < it.n_tiles && ok; ++t) {
                     const int n_valid =
                         min(kTcTileKeys, it.cr.c_hi - it.cr.c_lo - kTcTileKeys * t);
-                    const int nb =
-                        n_valid == kTcTileKeys ? 0 : (n_valid + kTcTailBox - 1) / kTcTailBox;
+                    const int atoms = n_valid >> 3, rem = n_valid & 7;
                     const int y = y0 + kTcTileKeys * t;
                     for (int kv = 0; kv < 2 && ok; ++kv) {
                         if (t == 0 && kv == 1) {
                             ok = load_q();
                             if (!ok) break;
                         }
-                        for (int s = 0; s < SLABS; ++s) {
-                            const uint32_t slot = f % NSLOT;
-                            ok = mbar_wait_bounded(&bars[C::B_EMPTY + slot], ((f / NSLOT) & 1) ^ 1,
-                                                   P.fault, kFaultCopyTimeout);
-                            if (!ok) break;
-                            uint8_t *dst = ring + slot * C::SLOT_BYTES;
-                            if (nb == 0) {
-                                mbar_arrive_expect_tx(&bars[C::B_FULL + slot], C::SLOT_BYTES);
-                                tma_load_2d_hint(dst, kv ? &map_v : &map_k, 64 * s, y,
-                                                 &bars[C::B_FULL + slot], policy);
-                            } else {
-                                mbar_arrive_expect_tx(&bars[C::B_FULL + slot],
-                                                      nb * kTcTailBox * 128);
-                                for (int bi = 0; bi < nb; ++bi)
-                                    tma_load_2d_hint(dst + bi * kTcTailBox * 128,
-                                                     kv ? &map_v32 : &map_k32, 64 * s,
-                                                     y + kTcTailBox * bi,
-                                                     &bars[C::B_FULL + slot], policy);
+                        const uint32_t slot = f % NT;
+                        ok = mbar_wait_bounded(&bars[C::B_EMPTY + slot], ((f / NT) & 1) ^ 1,
+                                               P.fault, kFaultCopyTimeout);
+                        if (!ok) break;
+                        uint8_t *dst = ring + slot * C::TILE_BYTES;
+                        uint64_t *bar = &bars[C::B_FULL + slot];
+                        const CUtensorMap *m4 = kv ? M.v_atoms : M.k_atoms;
+                        const CUtensorMap *m1 = kv ? &M.v_atom : &M.k_atom;
+                        mbar_arrive_expect_tx(bar, (uint32_t)(atoms + (rem != 0)) * C::ATOM_BYTES);
+                        if (atoms == 16) {
+                            tma_load_4d_hint(dst, &m4[0], 0, y, 0, 0, bar, policy);
+                        } else {
+                            // whole atoms lie inside the chunk, so the 4D boxes
+                            // (whose rows span two coordinates) stay inside the
+                            // cache; the last, partial atom goes through the
+                            // bounds-checked one-atom box
+                            int a = 0;
+#pragma unroll
+                            for (int bi = 1; bi < 4; ++bi) {
+                                const int na = 16 >> bi;
+                                if (atoms & na) {
+                                    tma_load_4d_hint(dst + a * C::ATOM_BYTES, &m4[bi], 0, y + 8 * a,
+                                                     0, 0, bar, policy);
+                                    a += na;
+                                }
                             }
-                            ++f;
+                            if (atoms & 1) {
+                                tma_load_3d_hint(dst + a * C::ATOM_BYTES, m1, 0, y + 8 * a, 0, bar,
+                                                 policy);
+                                ++a;
+                            }
+                            if (rem != 0)
+                                tma_load_3d_hint(dst + a * C::ATOM_BYTES, m1, 0, y + 8 * a, 0, bar,
+                                                 policy);
                         }
+                        ++f;
                     }
                 }
             }
             // every copy this CTA issued has landed before it exits
-            const uint32_t n_drain = f < (uint32_t)NSLOT ? f : (uint32_t)NSLOT;
+            const uint32_t n_drain = f < (uint32_t)NT ? f : (uint32_t)NT;
             for (uint32_t q = 0; q < n_drain; ++q) {
                 const uint32_t fi = f - 1 - q;
-                mbar_wait_bounded(&bars[C::B_FULL + fi % NSLOT], (fi / NSLOT) & 1, P.fault,
+                mbar_wait_bounded(&bars[C::B_FULL + fi % NT], (fi / NT) & 1, P.fault,
                                   kFaultCopyTimeout);
             }
             const uint32_t nq = k < (uint32_t)QB ? k : (uint32_t)QB;
@@ -370,10 +387,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t ring_a = smem_u32(ring);
             const uint32_t qs_a = smem_u32(qs);
             const uint32_t ps_a = smem_u32(ps);
+            // tile g of this CTA fills ring slots 2g (K) and 2g + 1 (V), modulo NT
             struct Cursor {
                 int item, j, t, n_tiles;
                 int last_keys;  // keys of the item's last tile
-                uint32_t k, fbase, g;
+                uint32_t k, g;
                 bool valid;
             };
             // first tile of the next non-empty item at or after (item, j)
@@ -393,13 +411,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             auto advance = [&](Cursor &c) {
                 ++c.g;
                 if (++c.t < c.n_tiles) return;
-                c.fbase += (uint32_t)c.n_tiles * 2 * SLABS;
                 ++c.k;
                 c.item += gridDim.x;
                 ++c.j;
                 seek(c);
             };
-            Cursor qc{(int)blockIdx.x, 0, 0, 0, 0, 0u, 0u, 0u, false};
+            Cursor qc{(int)blockIdx.x, 0, 0, 0, 0, 0u, 0u, false};
             seek(qc);
             Cursor pc = qc;
             bool ok = true;
@@ -410,14 +427,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // ---- PV of tile pc.g (its S was issued before)
                 if (pc.g < qc.g || !qc.valid) {
                     const uint32_t pb = pc.g % PB;
-                    const uint32_t fv = pc.fbase + (uint32_t)pc.t * 2 * SLABS + SLABS;
+                    const uint32_t fv = 2 * pc.g + 1;
+                    const uint32_t vslot = fv % NT;
                     bool ready = mbar_test(&bars[C::B_PFULL + pb], (pc.g / PB) & 1);
                     if (ready && pc.t == 0)
                         ready = mbar_test(&bars[C::B_OFREE + pc.k % OB], ((pc.k / OB) & 1) ^ 1);
-#pragma unroll
-                    for (int s = 0; s < SLABS; ++s)
-                        ready = ready && mbar_test(&bars[C::B_FULL + (fv + s) % NSLOT],
-                                                   ((fv + s) / NSLOT) & 1);
+                    ready = ready && mbar_test(&bars[C::B_FULL + vslot], (fv / NT) & 1);
                     if (ready) {
                         fence_after_sync();
                         // a partial tile: only the 16-key steps that hold valid keys
@@ -426,18 +441,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         // there) cannot reach O
                         const int nv = pc.t == pc.n_tiles - 1 ? pc.last_keys : kTcTileKeys;
                         const int steps = (nv + 15) >> 4;
+                        uint8_t *vt = ring + vslot * C::TILE_BYTES;
                         if (nv & 15) {
-                            // rows [nv, 16 * steps) of every V slab: a lane clears one
+                            // key rows [nv, 16 * steps) of every slab: a lane clears one
                             // 16-byte chunk of four rows per pass
                             const int row = nv + (lane >> 3), q = lane & 7;
 #pragma unroll
                             for (int s = 0; s < SLABS; ++s) {
-                                uint8_t *slab = ring + ((fv + s) % NSLOT) * C::SLOT_BYTES;
 #pragma unroll
-                                for (int r4 = 0; r4 < 16; r4 += 4)
-                                    if (row + r4 < steps * 16)
-                                        reinterpret_cast<uint4 *>(slab + (row + r4) * 128)[q] =
+                                for (int r4 = 0; r4 < 16; r4 += 4) {
+                                    const int r = row + r4;
+                                    if (r < steps * 16)
+                                        reinterpret_cast<uint4 *>(vt + (r >> 3) * C::ATOM_BYTES +
+                                                                  s * 1024 + (r & 7) * 128)[q] =
                                             make_uint4(0, 0, 0, 0);
+                                }
                             }
                             fence_proxy_async_smem();
                             __syncwarp();
@@ -447,33 +465,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             // units in the low bits), so offsets are added to a base
                             const uint64_t bbase =
                                 smem_desc_sw128(ps_a + pb * C::P_BUF, 16, 1024);
+                            // A = V^T, MN-major: 64-dim blocks one slab (1024 B) apart,
+                            // 8-key groups one atom apart
+                            const uint64_t abase = smem_desc_sw128(
+                                ring_a + vslot * C::TILE_BYTES, 1024, C::ATOM_BYTES);
                             const uint32_t ob = pc.k % OB;
                             const uint32_t acc0 = pc.t > 0 ? 1u : 0u;
 #pragma unroll
                             for (int mh = 0; mh < MH; ++mh) {
-                                const uint32_t s0 = (fv + 2 * mh) % NSLOT;  // s0 + 1: next slab
-                                // A = V^T: MN-major, the two 64-dim slabs one slot apart
-                                const uint64_t abase = smem_desc_sw128(
-                                    ring_a + s0 * C::SLOT_BYTES, C::SLOT_BYTES, 1024);
+                                const uint64_t ah = abase + (uint64_t)(mh * (2048 >> 4));
                                 const uint32_t d_t = tmem + C::O_COL + ob * C::O_COLS + mh * 2 * N;
                                 // B = [P_hi; P_lo], 2N rows
                                 if (steps == 8) {
 #pragma unroll
                                     for (int k8 = 0; k8 < 8; ++k8)
-                                        mma_bf16_ss(d_t, abase + (uint64_t)(k8 * 128),
+                                        mma_bf16_ss(d_t, ah + (uint64_t)(k8 * (2 * C::ATOM_BYTES >> 4)),
                                                     bbase + (uint64_t)((k8 >> 2) * (C::P_KSLAB >> 4) +
                                                                        (k8 & 3) * 2),
                                                     ID_PV, (acc0 | (uint32_t)k8) != 0);
                                 } else {
                                     for (int k8 = 0; k8 < steps; ++k8)
-                                        mma_bf16_ss(d_t, abase + (uint64_t)(k8 * 128),
+                                        mma_bf16_ss(d_t, ah + (uint64_t)(k8 * (2 * C::ATOM_BYTES >> 4)),
                                                     bbase + (uint64_t)((k8 >> 2) * (C::P_KSLAB >> 4) +
                                                                        (k8 & 3) * 2),
                                                     ID_PV, (acc0 | (uint32_t)k8) != 0);
                                 }
-                                mma_commit(&bars[C::B_EMPTY + s0]);
-                                mma_commit(&bars[C::B_EMPTY + s0 + 1]);
                             }
+                            mma_commit(&bars[C::B_EMPTY + vslot]);
                             mma_commit(&bars[C::B_PVDONE + pb]);
                         }
                         __syncwarp();
@@ -484,40 +502,37 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // ---- S of tile qc.g
                 if (qc.valid) {
                     const uint32_t sb = qc.g & 1;
-                    const uint32_t fk = qc.fbase + (uint32_t)qc.t * 2 * SLABS;
+                    const uint32_t fk = 2 * qc.g;
+                    const uint32_t kslot = fk % NT;
                     bool ready = mbar_test(&bars[C::B_SFREE + sb], ((qc.g >> 1) & 1) ^ 1) &&
                                  mbar_test(&bars[C::B_QFULL + qc.k % QB], (qc.k / QB) & 1);
                     // A parity test is only meaningful when the slot's previous
                     // fill has completed its phase, i.e. has been consumed.  The
-                    // previous fill of a K slab can be a V slab of an earlier tile
-                    // whose PV is still pending: then the slot is not ours yet.
-#pragma unroll
-                    for (int s = 0; s < SLABS; ++s) {
-                        const uint32_t fi = fk + s;
-                        if (fi >= (uint32_t)NSLOT) {
-                            const uint32_t fp = fi - NSLOT;
-                            if (fp % (2 * SLABS) >= (uint32_t)SLABS && pc.g <= fp / (2 * SLABS))
-                                ready = false;
-                        }
-                        ready = ready && mbar_test(&bars[C::B_FULL + fi % NSLOT], (fi / NSLOT) & 1);
+                    // previous fill of a K slot can be the V tile of an earlier
+                    // tile whose PV is still pending: then the slot is not ours yet.
+                    if (fk >= (uint32_t)NT) {
+                        const uint32_t fp = fk - NT;
+                        if ((fp & 1) && pc.g <= fp / 2) ready = false;
                     }
+                    ready = ready && mbar_test(&bars[C::B_FULL + kslot], (fk / NT) & 1);
                     if (ready) {
                         fence_after_sync();
                         if (leader) {
                             const uint64_t qbase =
                                 smem_desc_sw128(qs_a + (qc.k % QB) * C::Q_BUF, 16, 1024);
+                            // A = K, K-major: 8-key groups one atom apart, the 64-dim
+                            // slab s at s * 1024 B
+                            const uint64_t abase =
+                                smem_desc_sw128(ring_a + kslot * C::TILE_BYTES, 16, C::ATOM_BYTES);
 #pragma unroll
                             for (int s = 0; s < SLABS; ++s) {
-                                const uint32_t slot = (fk + s) % NSLOT;
-                                const uint64_t abase =
-                                    smem_desc_sw128(ring_a + slot * C::SLOT_BYTES, 16, 1024);
 #pragma unroll
                                 for (int kk = 0; kk < 4; ++kk)
-                                    mma_bf16_ss(tmem + sb * N, abase + (uint64_t)(kk * 2),
+                                    mma_bf16_ss(tmem + sb * N, abase + (uint64_t)(s * 64 + kk * 2),
                                                 qbase + (uint64_t)(s * (C::Q_SLAB >> 4) + kk * 2),
                                                 ID_QK, (s | kk) != 0);
-                                mma_commit(&bars[C::B_EMPTY + slot]);
                             }
+                            mma_commit(&bars[C::B_EMPTY + kslot]);
                             mma_commit(&bars[C::B_SFULL + sb]);
                             if (qc.t == qc.n_tiles - 1)
                                 mma_commit(&bars[C::B_QEMPTY + qc.k % QB]);
@@ -563,7 +578,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // of key lk inside a 128-byte row is XORed with (row & 7)
         const uint32_t p_key = (uint32_t)(lk >> 6) * C::P_KSLAB + (uint32_t)(lk & 7) * 2;
         const uint32_t p_chunk = (uint32_t)(lk & 63) >> 3;
-        uint32_t g = 0, k = 0, fbase = 0;
+        uint32_t g = 0, k = 0;
         bool ok = true;
         int j = 0;
         for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
@@ -860,8 +875,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 group_sync(wg);
             }
-            fbase += (uint32_t)it.n_tiles * 2 * SLABS;
-            ++k;
+                        ++k;
         }
     }
 

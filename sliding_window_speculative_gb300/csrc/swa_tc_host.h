@@ -1,6 +1,7 @@
 // Internal interface between the C-ABI layer and the tensor-core path.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 
@@ -16,8 +17,20 @@ struct TcParams {
     int items;            // splits * Hkv * row_tiles * B
 };
 
+// TMA tensor maps of one call.  The cache is viewed as rows of D bf16
+// (B * Hkv * L rows); a map with box "A atoms" loads 8*A consecutive rows
+// from any start row as A blocks of [head-dim slab][8 rows][128 bytes], so
+// a 128-key tile arrives in one copy and a partial tile in a few.
+struct TcMaps {
+    CUtensorMap k_atoms[4];  // 4D boxes of 16, 8, 4, 2 atoms
+    CUtensorMap k_atom;      // 3D box of one atom (rows past the cache are zero-filled)
+    CUtensorMap v_atoms[4];
+    CUtensorMap v_atom;
+    CUtensorMap q;           // 3D box (64 dims x G heads x draft rows)
+};
+
 struct TcConfInfo {
-    int nslot;        // ring slots of 16 KB
+    int nslot;        // ring slots of one 128-key tile each
     int smem_bytes;   // dynamic shared memory per CTA
     int tmem_cols;    // TMEM columns per CTA
     int ctas_per_sm;  // resident CTAs per SM the plan assumes

@@ -5,8 +5,8 @@
 //
 // Shared-memory operand layout used throughout: 128-byte swizzled tiles as
 // written by TMA with CU_TENSOR_MAP_SWIZZLE_128B, i.e. rows of 128 bytes
-// (64 bf16) in 1024-byte atoms of 8 rows, the 16-byte chunk c of row r
-// stored at chunk c ^ (r % 8).  Atoms must be 1024-byte aligned.
+// (64 bf16) in 1024-byte blocks of 8 rows, the 16-byte chunk c of row r
+// stored at chunk c ^ (r % 8).  Blocks must be 1024-byte aligned.
 #pragma once
 
 #include <cuda.h>
@@ -176,6 +176,27 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const CUtensorMap *m
         "[%0], [%1, {%2, %3, %4}], [%5];"
         ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
           "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d_hint(void *smem_dst, const CUtensorMap *map, int x,
+                                                 int y, int z, uint64_t *bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+          "r"(z), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_hint(void *smem_dst, const CUtensorMap *map, int x,
+                                                 int y, int z, int w, uint64_t *bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+          "r"(z), "r"(w), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 
