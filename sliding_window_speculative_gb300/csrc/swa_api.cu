@@ -246,8 +246,7 @@ cudaError_t launch_simt(const swa::AttnParams &P, cudaStream_t stream) {
         attr_done[dev] = true;
     }
     dim3 grid(P.splits, P.Hkv * P.row_tiles, P.B);
-    kern<<<grid, swa::kSimtThreads, C::SMEM_BYTES, stream>>>(P);
-    return cudaGetLastError();
+    return swa::launch_kernel(kern, grid, dim3(swa::kSimtThreads), C::SMEM_BYTES, stream, P);
 }
 
 template <int D>
@@ -263,8 +262,7 @@ cudaError_t launch_merge(const swa::AttnParams &P, cudaStream_t s) {
     const long long threads = (long long)P.B * P.Hkv * P.R * (D / 8);
     const long long blocks = (threads + 255) / 256;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    swa::swa_merge_kernel<D><<<(unsigned)blocks, 256, 0, s>>>(P);
-    return cudaGetLastError();
+    return swa::launch_kernel(swa::swa_merge_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, s, P);
 }
 
 // Launches the attention kernel of `pl` (and the merge kernel when the

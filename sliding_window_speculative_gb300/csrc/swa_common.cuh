@@ -125,6 +125,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream is still
+// running; grid_dep_wait() blocks until that kernel has completed and its
+// memory is visible, so every read of caller data comes after it.
+// grid_dep_trigger() lets the next kernel in the stream start its own
+// prologue early.  Both are no-ops for a kernel launched without the
+// attribute.
+__device__ __forceinline__ void grid_dep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // exp2 through the SFU.
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;

@@ -151,6 +151,8 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
     const int rg = warp % NRG, kg = warp / NRG;
     float *pbuf = pbuf_all + warp * (C::KB * RPW);
 
+    grid_dep_wait();
+    grid_dep_trigger();
     const ChunkRange cr = chunk_range(P, b, split);
     const int n_keys = cr.c_hi - cr.c_lo;
     const int n_tiles = n_keys > 0 ? (n_keys + kSimtTileKeys - 1) / kSimtTileKeys : 0;
@@ -377,6 +379,8 @@ template <int D>
 __global__ void __launch_bounds__(256) swa_merge_kernel(const AttnParams P) {
     const float NEG_INF = -__int_as_float(0x7f800000);
     constexpr int CPR = D / 8;
+    grid_dep_wait();
+    grid_dep_trigger();
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long rows = (long long)P.B * P.Hkv * P.R;
     if (idx >= rows * CPR) return;

@@ -57,8 +57,7 @@ cudaError_t launch(const TcLaunch &L, const TcMaps &maps, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    kern<<<L.grid, kTcThreads, C::SMEM_BYTES, stream>>>(L.T, maps);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(L.grid), dim3(kTcThreads), C::SMEM_BYTES, stream, L.T, maps);
 }
 
 template <int D>

@@ -236,6 +236,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int per_b = P.row_tiles * P.splits * P.Hkv;  // items per sequence
 
     // ---------------------------------------------------------------- setup
+    // Nothing before grid_dep_wait() reads memory the previous kernel in the
+    // stream may write: the tensor maps are kernel parameters, so their
+    // descriptors are fetched while that kernel finishes.
+    if (warp == 0 && lane < 11) {
+        const CUtensorMap *mp = lane < 4    ? &M.k_atoms[lane]
+                                : lane < 8  ? &M.v_atoms[lane - 4]
+                                : lane == 8 ? &M.k_atom
+                                : lane == 9 ? &M.v_atom
+                                            : &M.q;
+        prefetch_tmap(mp);
+    }
     if (tid == 0) {
         for (int i = 0; i < NT; ++i) {
             mbar_init(&bars[C::B_FULL + i], 1);
@@ -257,15 +268,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mbar_init(&bars[C::B_DRAIN], 1);
         fence_barrier_init();
     }
-    // metadata of this CTA's first items
-    for (int j = tid; j < kTcMetaItems; j += kTcThreads) {
-        const long long item = (long long)blockIdx.x + (long long)j * gridDim.x;
-        if (item < T.items) {
-            const int b = (int)(item / per_b);
-            meta_sl[j] = P.seq_lens[b];
-            meta_qp[j] = P.q_pos[b];
-        }
-    }
     // Q rows past an item's rows stay zero for the whole kernel (TMA writes
     // only the first rows_per_tile rows of each slab).
     for (int i = tid; i < QB * C::Q_BUF / 16; i += kTcThreads)
@@ -275,6 +277,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
+    grid_dep_wait();
+    grid_dep_trigger();
+    // metadata of this CTA's first items
+    for (int j = tid; j < kTcMetaItems; j += kTcThreads) {
+        const long long item = (long long)blockIdx.x + (long long)j * gridDim.x;
+        if (item < T.items) {
+            const int b = (int)(item / per_b);
+            meta_sl[j] = P.seq_lens[b];
+            meta_qp[j] = P.q_pos[b];
+        }
+    }
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -283,12 +296,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 0) {
         // ======================================================= producer
         if (lane == 0) {
-            prefetch_tmap(&M.k_atoms[0]);
-            prefetch_tmap(&M.v_atoms[0]);
-            prefetch_tmap(&M.k_atom);
-            prefetch_tmap(&M.v_atom);
-            prefetch_tmap(&M.q);
             const uint64_t policy = l2_policy_evict_first();
+            // The copies of one tile (K or V) of n_valid keys starting at cache
+            // row y into `dst`, completing on `bar`.
+            auto tile_copies = [&](int kv, int y, int n_valid, uint8_t *dst, uint64_t *bar) {
+                const int atoms = n_valid >> 3, rem = n_valid & 7;
+                const CUtensorMap *m4 = kv ? M.v_atoms : M.k_atoms;
+                const CUtensorMap *m1 = kv ? &M.v_atom : &M.k_atom;
+                if (atoms == 16) {
+                    tma_load_4d_hint(dst, &m4[0], 0, y, 0, 0, bar, policy);
+                    return;
+                }
+                // whole atoms lie inside the chunk, so the 4D boxes (whose rows
+                // span two coordinates) stay inside the cache; the last, partial
+                // atom goes through the bounds-checked one-atom box
+                int a = 0;
+#pragma unroll
+                for (int bi = 1; bi < 4; ++bi) {
+                    const int na = 16 >> bi;
+                    if (atoms & na) {
+                        tma_load_4d_hint(dst + a * C::ATOM_BYTES, &m4[bi], 0, y + 8 * a, 0, 0, bar,
+                                         policy);
+                        a += na;
+                    }
+                }
+                for (int e = 0; e < (atoms & 1) + (rem != 0); ++e, ++a)
+                    tma_load_3d_hint(dst + a * C::ATOM_BYTES, m1, 0, y + 8 * a, 0, bar, policy);
+            };
             uint32_t f = 0, k = 0;  // fills (two per tile: K then V), items with keys
             bool ok = true;
             int j = 0;
@@ -324,37 +358,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         ok = mbar_wait_bounded(&bars[C::B_EMPTY + slot], ((f / NT) & 1) ^ 1,
                                                P.fault, kFaultCopyTimeout);
                         if (!ok) break;
-                        uint8_t *dst = ring + slot * C::TILE_BYTES;
                         uint64_t *bar = &bars[C::B_FULL + slot];
-                        const CUtensorMap *m4 = kv ? M.v_atoms : M.k_atoms;
-                        const CUtensorMap *m1 = kv ? &M.v_atom : &M.k_atom;
                         mbar_arrive_expect_tx(bar, (uint32_t)(atoms + (rem != 0)) * C::ATOM_BYTES);
-                        if (atoms == 16) {
-                            tma_load_4d_hint(dst, &m4[0], 0, y, 0, 0, bar, policy);
-                        } else {
-                            // whole atoms lie inside the chunk, so the 4D boxes
-                            // (whose rows span two coordinates) stay inside the
-                            // cache; the last, partial atom goes through the
-                            // bounds-checked one-atom box
-                            int a = 0;
-#pragma unroll
-                            for (int bi = 1; bi < 4; ++bi) {
-                                const int na = 16 >> bi;
-                                if (atoms & na) {
-                                    tma_load_4d_hint(dst + a * C::ATOM_BYTES, &m4[bi], 0, y + 8 * a,
-                                                     0, 0, bar, policy);
-                                    a += na;
-                                }
-                            }
-                            if (atoms & 1) {
-                                tma_load_3d_hint(dst + a * C::ATOM_BYTES, m1, 0, y + 8 * a, 0, bar,
-                                                 policy);
-                                ++a;
-                            }
-                            if (rem != 0)
-                                tma_load_3d_hint(dst + a * C::ATOM_BYTES, m1, 0, y + 8 * a, 0, bar,
-                                                 policy);
-                        }
+                        tile_copies(kv, y, n_valid, ring + slot * C::TILE_BYTES, bar);
                         ++f;
                     }
                 }
@@ -875,7 +881,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 group_sync(wg);
             }
-                        ++k;
+            ++k;
         }
     }
 

@@ -4,6 +4,9 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
+#include <stdlib.h>
+
+#include <utility>
 
 #include "swa_simt.cuh"
 
@@ -42,6 +45,34 @@ struct TcLaunch {
     int grid;   // persistent CTAs
     const void *k, *v, *q;
 };
+
+// Kernels are launched with programmatic stream serialization (programmatic
+// dependent launch): each may begin its prologue while the previous kernel
+// in the stream finishes, and waits (griddepcontrol.wait) before it reads
+// any caller memory.  SWA_PDL=0 in the environment turns it off.
+inline bool pdl_enabled() {
+    static const bool on = [] {
+        const char *v = getenv("SWA_PDL");
+        return !(v != nullptr && v[0] == '0');
+    }();
+    return on;
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Constants of the (head_dim, padded rows) configuration; false if none.
 bool tc_conf(int D, int N, TcConfInfo *c);
