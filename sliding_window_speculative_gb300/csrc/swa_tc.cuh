@@ -61,7 +61,20 @@ namespace swa {
 constexpr int kTcThreads = 320;
 constexpr int kTcTileKeys = 128;
 constexpr int kTcTailBox = 32;    // keys per box of a partial tile
-constexpr int kTcMetaItems = 16;  // items per CTA whose metadata is cached in smem
+constexpr int kTcMetaItems = 8;   // items per CTA decoded once into shared memory
+// Initial per-row reference maximum (log2 units): finite, so P = 2^(s - m)
+// needs no special case, yet below any score of a row with keys, so the
+// first tile always raises it.
+constexpr float kNoRef = -1.0e30f;
+
+struct TcItem {
+    int b, h, split, rt;
+    ChunkRange cr;
+    int n_tiles;
+    int row0;  // first packed row of the item
+    int rows;  // packed rows of the item
+    int i0;    // first draft row
+};
 
 template <int D, int N, int NT, int QB, int PB, int OB>
 struct TcCfg {
@@ -78,8 +91,9 @@ struct TcCfg {
     static constexpr int RED_OFF = P_OFF + PB * P_BUF;        // float [2][4][N]
     static constexpr int LINV_OFF = RED_OFF + 2 * 4 * N * 4;  // float [N]
     static constexpr int ALPHA_OFF = LINV_OFF + N * 4;        // float [N]
-    static constexpr int META_OFF = ALPHA_OFF + N * 4;        // int [2][kTcMetaItems]
-    static constexpr int BAR_OFF = META_OFF + 2 * kTcMetaItems * 4;
+    static constexpr int ROW_OFF = ALPHA_OFF + N * 4;          // uint32 [N] output rows
+    static constexpr int META_OFF = ROW_OFF + N * 4;           // TcItem [kTcMetaItems]
+    static constexpr int BAR_OFF = META_OFF + kTcMetaItems * (int)sizeof(TcItem);
     // ring full/empty [NT], q full/empty [QB], s full/free [2], p full [PB],
     // pv done [PB], o free [2] (OB used), drain
     static constexpr int B_FULL = 0, B_EMPTY = NT, B_QFULL = 2 * NT, B_QEMPTY = B_QFULL + QB,
@@ -106,19 +120,9 @@ struct TcCfg {
     static_assert(PB * P_BUF >= N * 512, "epilogue staging fits in the P buffers");
 };
 
-struct TcItem {
-    int b, h, split, rt;
-    ChunkRange cr;
-    int n_tiles;
-    int row0;  // first packed row of the item
-    int rows;  // packed rows of the item
-    int i0;    // first draft row
-};
 
-// Work item `item`; `j` is its position in this CTA's item sequence (its
-// metadata may sit in shared memory).
-__device__ __forceinline__ TcItem tc_decode(const TcParams &T, int item, int j,
-                                            const int *meta_sl, const int *meta_qp) {
+// Work item `item` (its sequence's seq_len / q_pos read from global memory).
+__device__ __forceinline__ TcItem tc_decode_global(const TcParams &T, int item) {
     const AttnParams &P = T.a;
     TcItem it;
     int rest = item;
@@ -128,16 +132,21 @@ __device__ __forceinline__ TcItem tc_decode(const TcParams &T, int item, int j,
     rest /= P.splits;
     it.h = rest % P.Hkv;
     it.b = rest / P.Hkv;
-    if (j < kTcMetaItems)
-        it.cr = chunk_range_of(P, meta_qp[j], meta_sl[j], it.split);
-    else
-        it.cr = chunk_range(P, it.b, it.split);
+    it.cr = chunk_range(P, it.b, it.split);
     const int nk = it.cr.c_hi - it.cr.c_lo;
     it.n_tiles = nk > 0 ? (nk + kTcTileKeys - 1) / kTcTileKeys : 0;
     it.row0 = it.rt * T.rows_per_tile;
     it.rows = min(P.R - it.row0, T.rows_per_tile);
     it.i0 = it.rt * T.q_rows_per_tile;
     return it;
+}
+
+// Work item `item`, the j-th of this CTA: the first kTcMetaItems were
+// decoded once at set-up into shared memory.
+__device__ __forceinline__ TcItem tc_decode(const TcParams &T, int item, int j,
+                                            const TcItem *meta) {
+    if (j < kTcMetaItems) return meta[j];
+    return tc_decode_global(T, item);
 }
 
 // Barrier of one softmax warpgroup (128 threads), ids 1 / 3.
@@ -226,14 +235,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float *red = reinterpret_cast<float *>(sm + C::RED_OFF);
     float *linv = reinterpret_cast<float *>(sm + C::LINV_OFF);
     float *alpha_sm = reinterpret_cast<float *>(sm + C::ALPHA_OFF);
-    int *meta_sl = reinterpret_cast<int *>(sm + C::META_OFF);
-    int *meta_qp = meta_sl + kTcMetaItems;
+    uint32_t *rowidx = reinterpret_cast<uint32_t *>(sm + C::ROW_OFF);
+    TcItem *meta = reinterpret_cast<TcItem *>(sm + C::META_OFF);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::BAR_OFF);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::MISC_OFF);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int per_b = P.row_tiles * P.splits * P.Hkv;  // items per sequence
 
     // ---------------------------------------------------------------- setup
     // Nothing before grid_dep_wait() reads memory the previous kernel in the
@@ -282,11 +290,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // metadata of this CTA's first items
     for (int j = tid; j < kTcMetaItems; j += kTcThreads) {
         const long long item = (long long)blockIdx.x + (long long)j * gridDim.x;
-        if (item < T.items) {
-            const int b = (int)(item / per_b);
-            meta_sl[j] = P.seq_lens[b];
-            meta_qp[j] = P.q_pos[b];
-        }
+        if (item < T.items) meta[j] = tc_decode_global(T, (int)item);
     }
     fence_before_sync();
     __syncthreads();
@@ -327,7 +331,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = true;
             int j = 0;
             for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
-                const TcItem it = tc_decode(T, item, j, meta_sl, meta_qp);
+                const TcItem it = tc_decode(T, item, j, meta);
                 if (it.n_tiles == 0) continue;
                 const uint32_t qb = k % QB, quse = k / QB;
                 // Q of the item, issued after its first K tile so that a single
@@ -403,7 +407,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // first tile of the next non-empty item at or after (item, j)
             auto seek = [&](Cursor &c) {
                 for (; c.item < T.items; c.item += gridDim.x, ++c.j) {
-                    const TcItem it = tc_decode(T, c.item, c.j, meta_sl, meta_qp);
+                    const TcItem it = tc_decode(T, c.item, c.j, meta);
                     if (it.n_tiles > 0) {
                         c.n_tiles = it.n_tiles;
                         c.last_keys = it.cr.c_hi - it.cr.c_lo - kTcTileKeys * (it.n_tiles - 1);
@@ -588,7 +592,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = true;
         int j = 0;
         for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
-            const TcItem it = tc_decode(T, item, j, meta_sl, meta_qp);
+            const TcItem it = tc_decode(T, item, j, meta);
             const size_t bh = (size_t)it.b * P.Hkv + it.h;
             const int my_rows = min(HN, it.rows - r0);  // rows of this group in the item
             if (it.n_tiles == 0) {
@@ -617,7 +621,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float mref[HN], lrow[HN];
 #pragma unroll
             for (int r = 0; r < HN; ++r) {
-                mref[r] = NEG_INF;
+                mref[r] = kNoRef;
                 lrow[r] = 0.f;
             }
 
@@ -739,19 +743,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
                 // the previous item's epilogue staged its output in the P buffers
                 if (t == 0 && k > 0) group_sync(wg);
-                // P = 2^(s - m_ref) as bf16 hi + lo into the swizzled P^T tiles
-                uint8_t *pt = ps + pb * C::P_BUF + p_key;
+                // P = 2^(s - m_ref) as bf16 hi + lo into the swizzled P^T tiles:
+                // P_hi = P truncated to bf16, P_lo = the rest rounded to bf16
+                // (P_hi + P_lo within 2^-16 of P).  Row r0 + r of the tile; r0
+                // is a multiple of 8, so the row's swizzle phase is r & 7.
+                uint8_t *pt = ps + pb * C::P_BUF + p_key + r0 * 128;
 #pragma unroll
                 for (int r = 0; r < HN; ++r) {
-                    const float mu = mref[r] == NEG_INF ? 0.f : mref[r];
-                    const float p = fast_exp2(v[r] - mu);
-                    const __nv_bfloat16 hi = __float2bfloat16_rn(p);
-                    const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
-                    const int rr = r0 + r;
-                    const uint32_t rl = (uint32_t)(N + rr);  // P_lo row, same (rr & 7)
-                    const uint32_t sw = (p_chunk ^ (uint32_t)(rr & 7)) << 4;
-                    *reinterpret_cast<__nv_bfloat16 *>(pt + (uint32_t)rr * 128 + sw) = hi;
-                    *reinterpret_cast<__nv_bfloat16 *>(pt + rl * 128 + sw) = lo;
+                    const float p = fast_exp2(v[r] - mref[r]);
+                    const uint32_t bits = __float_as_uint(p);
+                    const float lo = p - __uint_as_float(bits & 0xffff0000u);
+                    const uint32_t sw = (p_chunk ^ (uint32_t)(r & 7)) << 4;
+                    *reinterpret_cast<uint16_t *>(pt + r * 128 + sw) = (uint16_t)(bits >> 16);
+                    *reinterpret_cast<uint16_t *>(pt + (N + r) * 128 + sw) =
+                        __bfloat16_as_ushort(__float2bfloat16_rn(lo));
                     lrow[r] += p;
                 }
                 fence_proxy_async_smem();
@@ -779,15 +784,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
                 for (int q = 0; q < HN; ++q)
                     if (q == r) m = mref[q];
-                linv[r0 + r] = l > 0.f ? 1.f / l : 0.f;
+                linv[r0 + r] = l > 0.f ? __frcp_rn(l) : 0.f;
                 const int rg = it.row0 + r0 + r;
                 if (P.splits == 1) {
-                    if (P.lse != nullptr) {
-                        const int i = rg / P.G, gg = rg - i * P.G;
-                        const size_t orow =
-                            ((size_t)it.b * P.q_len + i) * P.Hq + (size_t)it.h * P.G + gg;
+                    // output row of packed row rg: draft row rg / G of query head
+                    // h * G + rg % G (below 2^31 by the plan's size checks)
+                    const int i = rg / P.G, gg = rg - i * P.G;
+                    const uint32_t orow =
+                        (uint32_t)(((size_t)it.b * P.q_len + i) * P.Hq + (size_t)it.h * P.G + gg);
+                    rowidx[r0 + r] = orow;
+                    if (P.lse != nullptr)
                         P.lse[orow] = l > 0.f ? (m + __log2f(l)) * kLn2 : NEG_INF;
-                    }
                 } else {
                     const size_t prow = (bh * P.splits + it.split) * P.R + rg;
                     P.part_ml[prow * 2] = l > 0.f ? m : NEG_INF;
@@ -804,17 +811,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // partial row in halves of 128 dims.  A group stages its rows only
             // in the bytes of its own P rows (hi and lo, both key slabs), so
             // the other group's P writes for the next item cannot collide.
-            const bool part = P.splits > 1;
-            const int RB = part ? 512 : D * 2;   // staged bytes per row
-            const int RPC = HN * 128 / RB;       // rows per 128-byte-row chunk of the group
-            auto stg_row = [&](int rr) -> uint8_t * {
+            // Staged row rr (RB bytes) of the group sits in the group's
+            // 128-byte P rows, RPC staged rows per P row.
+            auto stg_row = [&](int rr, int RB, int RPC) -> uint8_t * {
                 const int c = rr / RPC;
                 return ps + (c >> 1) * C::P_KSLAB + ((c & 1) * N + r0) * 128 + (rr % RPC) * RB;
             };
-            if (!part) {
-#pragma unroll 1
+            if (P.splits == 1) {
+                constexpr int RB = D * 2, RPC = HN * 128 / RB;
+#pragma unroll
                 for (int mh = 0; mh < MH; ++mh) {
-#pragma unroll 1
+#pragma unroll
                     for (int c0 = 0; c0 < HN; c0 += OW) {
                         uint32_t o[OW], ol[OW];
                         tmem_load<OW>(ocol0 + mh * 2 * N + r0 + c0, o);
@@ -822,11 +829,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < OW; ++e) {
-                            const int r = r0 + c0 + e;
                             const float ov = __uint_as_float(o[e]) + __uint_as_float(ol[e]);
-                            *reinterpret_cast<__nv_bfloat16 *>(stg_row(c0 + e) +
+                            *reinterpret_cast<__nv_bfloat16 *>(stg_row(c0 + e, RB, RPC) +
                                                                (mh * 128 + lk) * 2) =
-                                __float2bfloat16_rn(ov * linv[r]);
+                                __float2bfloat16_rn(ov * linv[r0 + c0 + e]);
                         }
                     }
                 }
@@ -835,51 +841,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 group_sync(wg);
                 constexpr int CPR = D / 8;  // 16-byte chunks per row
                 for (int idx = gtid; idx < my_rows * CPR; idx += 128) {
-                    const int r = r0 + idx / CPR, c = idx % CPR;
-                    const int rg = it.row0 + r;
-                    const int i = rg / P.G, gg = rg - i * P.G;
-                    const size_t orow =
-                        ((size_t)it.b * P.q_len + i) * P.Hq + (size_t)it.h * P.G + gg;
-                    *reinterpret_cast<uint4 *>(P.out + orow * D + c * 8) =
-                        *reinterpret_cast<const uint4 *>(stg_row(r - r0) + c * 16);
+                    const int r = idx / CPR, c = idx % CPR;
+                    *reinterpret_cast<uint4 *>(P.out + (size_t)rowidx[r0 + r] * D + c * 8) =
+                        *reinterpret_cast<const uint4 *>(stg_row(r, RB, RPC) + c * 16);
                 }
                 // (the group synchronises again before the staging area, a P
                 // buffer, is written by the next item)
-            }
+            } else {
+                constexpr int RB = 512, RPC = HN * 128 / RB;
+                const size_t prow0 = (bh * P.splits + it.split) * P.R + it.row0 + r0;
 #pragma unroll 1
-            for (int mh = 0; mh < MH && part; ++mh) {
-#pragma unroll 1
-                for (int c0 = 0; c0 < HN; c0 += OW) {
-                    uint32_t o[OW], ol[OW];
-                    tmem_load<OW>(ocol0 + mh * 2 * N + r0 + c0, o);
-                    tmem_load<OW>(ocol0 + mh * 2 * N + N + r0 + c0, ol);
-                    tmem_wait_ld();
+                for (int mh = 0; mh < MH; ++mh) {
 #pragma unroll
-                    for (int e = 0; e < OW; ++e)
-                        *reinterpret_cast<float *>(stg_row(c0 + e) + lk * 4) =
-                            __uint_as_float(o[e]) + __uint_as_float(ol[e]);
-                }
-                if (mh == MH - 1) {
-                    fence_before_sync();
-                    mbar_arrive(&bars[C::B_OFREE + ob]);  // O buffer may be reused
-                }
-                group_sync(wg);
-                const int cpr = part ? 32 : 16;  // 16-byte chunks per row of this half
-                for (int idx = gtid; idx < my_rows * cpr; idx += 128) {
-                    const int r = r0 + idx / cpr, c = idx % cpr;
-                    const int rg = it.row0 + r;
-                    const uint4 val = *reinterpret_cast<const uint4 *>(stg_row(r - r0) + c * 16);
-                    if (part) {
-                        const size_t prow = (bh * P.splits + it.split) * P.R + rg;
-                        *reinterpret_cast<uint4 *>(P.part_acc + prow * D + mh * 128 + c * 4) = val;
-                    } else {
-                        const int i = rg / P.G, gg = rg - i * P.G;
-                        const size_t orow =
-                            ((size_t)it.b * P.q_len + i) * P.Hq + (size_t)it.h * P.G + gg;
-                        *reinterpret_cast<uint4 *>(P.out + orow * D + mh * 128 + c * 8) = val;
+                    for (int c0 = 0; c0 < HN; c0 += OW) {
+                        uint32_t o[OW], ol[OW];
+                        tmem_load<OW>(ocol0 + mh * 2 * N + r0 + c0, o);
+                        tmem_load<OW>(ocol0 + mh * 2 * N + N + r0 + c0, ol);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < OW; ++e)
+                            *reinterpret_cast<float *>(stg_row(c0 + e, RB, RPC) + lk * 4) =
+                                __uint_as_float(o[e]) + __uint_as_float(ol[e]);
                     }
+                    if (mh == MH - 1) {
+                        fence_before_sync();
+                        mbar_arrive(&bars[C::B_OFREE + ob]);  // O buffer may be reused
+                    }
+                    group_sync(wg);
+                    for (int idx = gtid; idx < my_rows * 32; idx += 128) {
+                        const int r = idx / 32, c = idx % 32;
+                        *reinterpret_cast<uint4 *>(P.part_acc + (prow0 + r) * D + mh * 128 + c * 4) =
+                            *reinterpret_cast<const uint4 *>(stg_row(r, RB, RPC) + c * 16);
+                    }
+                    group_sync(wg);
                 }
-                group_sync(wg);
             }
             ++k;
         }
