@@ -21,6 +21,7 @@ __device__ uint32_t g_fault_word = 0;
 namespace {
 
 constexpr int kMaxSplits = 64;
+static_assert(kMaxSplits <= swa::kMergeMaxSplits, "the merge kernel weighs at most 64 splits");
 constexpr int kMaxQLen = 64;      // SPLITKV_VERIFY_MAX_Q
 constexpr int kMaxDevices = 64;
 
@@ -94,7 +95,8 @@ int forced_kernel() {
 
 // Split heuristic.  Host-only: seq_lens live on the device, so the
 // worst-case span W + q_len - 1 (bounded by the cache length) is used.
-//  - Tensor-core path (head_dim 128/256, >= 16 packed rows): one chunk per
+//  - Tensor-core path (head_dim 128/256; >= 16 packed rows, or a batch whose
+//    (sequence, KV head) units cover half the SMs): one chunk per
 //    (sequence, KV head, row tile) once those units cover half the SMs;
 //    otherwise enough chunks of >= 64 keys to reach every SM.  Persistent
 //    grid of at most SMs x resident CTAs.
@@ -117,7 +119,12 @@ Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
                           (long long)d->batch * d->q_len < (1LL << 31) &&
                           (long long)d->batch * d->num_kv_heads * d->q_len * kMaxSplits <
                               (1LL << 31);
-    const bool use_tc = tc_shape && (force == 2 || (force == 0 && R >= 16));
+    // The tensor-core kernel needs >= 16 packed rows to fill an MMA without
+    // waste, but below that it still wins once the (sequence, KV head) units
+    // alone cover half the SMs: its MMAs cost the same for 4 rows as for 16,
+    // and its K/V stream is the faster one.
+    const bool big_batch = (long long)d->batch * d->num_kv_heads * 2 >= num_sms;
+    const bool use_tc = tc_shape && (force == 2 || (force == 0 && (R >= 16 || big_batch)));
     int splits;
     if (use_tc) {
         p.kernel = 2;
@@ -259,10 +266,10 @@ cudaError_t launch_simt_d(const Plan &pl, const swa::AttnParams &P, cudaStream_t
 
 template <int D>
 cudaError_t launch_merge(const swa::AttnParams &P, cudaStream_t s) {
-    const long long threads = (long long)P.B * P.Hkv * P.R * (D / 8);
-    const long long blocks = (threads + 255) / 256;
+    const long long blocks = (long long)P.B * P.Hkv * P.R;  // one per packed row
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    return swa::launch_kernel(swa::swa_merge_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, s, P);
+    return swa::launch_kernel(swa::swa_merge_kernel<D>, dim3((unsigned)blocks),
+                              dim3(swa::kMergeThreads), 0, s, P);
 }
 
 // Launches the attention kernel of `pl` (and the merge kernel when the

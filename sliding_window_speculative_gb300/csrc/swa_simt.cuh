@@ -374,51 +374,93 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
 // Log-sum-exp merge of the split partials of every packed row:
 //   M = max_s m_s, Lambda = sum_s l_s 2^(m_s - M),
 //   out = sum_s acc_s 2^(m_s - M) / Lambda, lse = (M + log2 Lambda) ln 2.
-// One thread per (row, 8 dims).
+// One block per packed row (sequence, KV head, row).  The block first turns
+// the splits' (m, l) into weights in shared memory; then each thread sums a
+// residue class of splits for one 8-dim chunk, so all of a row's partial
+// loads are in flight at once, and the classes are added up in shared
+// memory.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeMaxSplits = 64;
+
 template <int D>
-__global__ void __launch_bounds__(256) swa_merge_kernel(const AttnParams P) {
+__global__ void __launch_bounds__(kMergeThreads) swa_merge_kernel(const AttnParams P) {
     const float NEG_INF = -__int_as_float(0x7f800000);
-    constexpr int CPR = D / 8;
+    constexpr int CPR = D / 8;                    // 8-dim chunks per row
+    constexpr int NG = kMergeThreads / CPR;       // split classes
+    __shared__ float w_s[kMergeMaxSplits];        // 2^(m_s - M), 0 for empty splits
+    __shared__ float red[2];                      // M, Lambda
+    __shared__ __align__(16) float part[NG][D];   // per-class sums
     grid_dep_wait();
     grid_dep_trigger();
-    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long rows = (long long)P.B * P.Hkv * P.R;
-    if (idx >= rows * CPR) return;
-    const long long grow = idx / CPR;  // (b*Hkv + h) * R + r
-    const int dc = (int)(idx % CPR);
+    const long long grow = blockIdx.x;            // (b*Hkv + h) * R + r
     const long long bh = grow / P.R;
     const int r = (int)(grow % P.R);
     const int b = (int)(bh / P.Hkv), h = (int)(bh % P.Hkv);
     const size_t base = (size_t)bh * P.splits * P.R + r;  // split s at base + s*R
-    float M = NEG_INF;
-    for (int s = 0; s < P.splits; ++s) M = fmaxf(M, P.part_ml[(base + (size_t)s * P.R) * 2]);
-    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    float Lam = 0.f;
-    if (M != NEG_INF) {
-        for (int s = 0; s < P.splits; ++s) {
-            const size_t prow = base + (size_t)s * P.R;
-            const float ms = P.part_ml[prow * 2];
-            if (ms == NEG_INF) continue;
-            const float w = fast_exp2(ms - M);
-            Lam += w * P.part_ml[prow * 2 + 1];
-            const float4 *a = reinterpret_cast<const float4 *>(P.part_acc + prow * D + dc * 8);
-            const float4 a0 = a[0], a1 = a[1];
-            o[0] = fmaf(w, a0.x, o[0]); o[1] = fmaf(w, a0.y, o[1]);
-            o[2] = fmaf(w, a0.z, o[2]); o[3] = fmaf(w, a0.w, o[3]);
-            o[4] = fmaf(w, a1.x, o[4]); o[5] = fmaf(w, a1.y, o[5]);
-            o[6] = fmaf(w, a1.z, o[6]); o[7] = fmaf(w, a1.w, o[7]);
+    const int tid = threadIdx.x;
+    if (tid < 32) {
+        // warp 0: M and the weights (splits <= 64, two per lane)
+        float m0 = NEG_INF, m1 = NEG_INF, l0 = 0.f, l1 = 0.f;
+        if (tid < P.splits) {
+            m0 = P.part_ml[(base + (size_t)tid * P.R) * 2];
+            l0 = P.part_ml[(base + (size_t)tid * P.R) * 2 + 1];
+        }
+        if (tid + 32 < P.splits) {
+            m1 = P.part_ml[(base + (size_t)(tid + 32) * P.R) * 2];
+            l1 = P.part_ml[(base + (size_t)(tid + 32) * P.R) * 2 + 1];
+        }
+        float M = fmaxf(m0, m1);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        const float w0 = (M == NEG_INF || m0 == NEG_INF) ? 0.f : fast_exp2(m0 - M);
+        const float w1 = (M == NEG_INF || m1 == NEG_INF) ? 0.f : fast_exp2(m1 - M);
+        float lam = w0 * l0 + w1 * l1;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) lam += __shfl_xor_sync(0xffffffffu, lam, off);
+        w_s[tid] = w0;
+        w_s[tid + 32] = w1;
+        if (tid == 0) {
+            red[0] = M;
+            red[1] = lam;
         }
     }
-    const float inv = Lam > 0.f ? 1.f / Lam : 0.f;
-    const int i = r / P.G, gg = r % P.G;
-    const size_t orow = ((size_t)b * P.q_len + i) * P.Hq + (size_t)h * P.G + gg;
-    uint4 w;
-    w.x = pack_bf16x2(o[0] * inv, o[1] * inv);
-    w.y = pack_bf16x2(o[2] * inv, o[3] * inv);
-    w.z = pack_bf16x2(o[4] * inv, o[5] * inv);
-    w.w = pack_bf16x2(o[6] * inv, o[7] * inv);
-    *reinterpret_cast<uint4 *>(P.out + orow * D + dc * 8) = w;
-    if (dc == 0 && P.lse != nullptr) P.lse[orow] = Lam > 0.f ? (M + __log2f(Lam)) * kLn2 : NEG_INF;
+    __syncthreads();
+    const int c = tid % CPR, sg = tid / CPR;
+    float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int sp = sg; sp < P.splits; sp += NG) {
+        const float w = w_s[sp];
+        const float4 *a = reinterpret_cast<const float4 *>(P.part_acc + (base + (size_t)sp * P.R) * D + c * 8);
+        const float4 a0 = a[0], a1 = a[1];
+        o[0] = fmaf(w, a0.x, o[0]); o[1] = fmaf(w, a0.y, o[1]);
+        o[2] = fmaf(w, a0.z, o[2]); o[3] = fmaf(w, a0.w, o[3]);
+        o[4] = fmaf(w, a1.x, o[4]); o[5] = fmaf(w, a1.y, o[5]);
+        o[6] = fmaf(w, a1.z, o[6]); o[7] = fmaf(w, a1.w, o[7]);
+    }
+    *reinterpret_cast<float4 *>(&part[sg][c * 8]) = make_float4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<float4 *>(&part[sg][c * 8 + 4]) = make_float4(o[4], o[5], o[6], o[7]);
+    __syncthreads();
+    if (tid < CPR) {
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int g2 = 0; g2 < NG; ++g2) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] += part[g2][tid * 8 + e];
+        }
+        const float Lam = red[1];
+        const float inv = Lam > 0.f ? 1.f / Lam : 0.f;
+        const int i = r / P.G, gg = r % P.G;
+        const size_t orow = ((size_t)b * P.q_len + i) * P.Hq + (size_t)h * P.G + gg;
+        uint4 wv;
+        wv.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        wv.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        wv.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+        wv.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+        *reinterpret_cast<uint4 *>(P.out + orow * D + tid * 8) = wv;
+        if (tid == 0 && P.lse != nullptr)
+            P.lse[orow] = Lam > 0.f ? (red[0] + __log2f(Lam)) * kLn2 : NEG_INF;
+    }
 }
 
 }  // namespace swa

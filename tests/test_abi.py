@@ -124,7 +124,11 @@ def test_plan_kernel_choice(lib, monkeypatch):
     q8 = swa.make_dims(1, 8, 8, 2, 256, 4096)
     assert swa.swa_plan(q8, 188, 152)["kernel"] == 2            # 32 packed rows: tensor cores
     q1 = swa.make_dims(1, 1, 8, 2, 256, 4096)
-    assert swa.swa_plan(q1, 188, 152)["kernel"] == 1            # 4 rows: CUDA cores
+    assert swa.swa_plan(q1, 188, 152)["kernel"] == 1            # 4 rows, 2 units: CUDA cores
+    q1_big = swa.make_dims(76, 1, 8, 2, 256, 4096)              # 152 units: tensor cores
+    assert swa.swa_plan(q1_big, 188, 152)["kernel"] == 2
+    assert swa.swa_plan(swa.make_dims(75, 1, 8, 2, 256, 4096), 188, 152)["kernel"] == 2
+    assert swa.swa_plan(swa.make_dims(37, 1, 8, 2, 256, 4096), 188, 152)["kernel"] == 1
     d64 = swa.make_dims(1, 8, 2, 1, 64, 40)
     assert swa.swa_plan(d64, 16, 152)["kernel"] == 1            # head_dim 64: CUDA cores
     q64 = swa.swa_plan(swa.make_dims(512, 64, 8, 2, 256, 32768), 1024, 152)
