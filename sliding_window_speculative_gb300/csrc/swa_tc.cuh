@@ -62,6 +62,11 @@ constexpr int kTcThreads = 320;
 constexpr int kTcTileKeys = 128;
 constexpr int kTcTailBox = 32;    // keys per box of a partial tile
 constexpr int kTcMetaItems = 8;   // items per CTA decoded once into shared memory
+// Ring slots are handed out in any order (the first free one), so a K tile,
+// consumed as soon as its scores are computed, frees its slot long before
+// the V tiles around it; a table of the recent fills tells the MMA lane
+// where each landed: entry f % kFillTab = (f << 8) | (use parity << 4) | slot.
+constexpr int kFillTab = 16;
 // Initial per-row reference maximum (log2 units): finite, so P = 2^(s - m)
 // needs no special case, yet below any score of a row with keys, so the
 // first tile always raises it.
@@ -93,7 +98,8 @@ struct TcCfg {
     static constexpr int ALPHA_OFF = LINV_OFF + N * 4;        // float [N]
     static constexpr int ROW_OFF = ALPHA_OFF + N * 4;          // uint32 [N] output rows
     static constexpr int META_OFF = ROW_OFF + N * 4;           // TcItem [kTcMetaItems]
-    static constexpr int BAR_OFF = META_OFF + kTcMetaItems * (int)sizeof(TcItem);
+    static constexpr int FTAB_OFF = META_OFF + kTcMetaItems * (int)sizeof(TcItem);  // uint32 [kFillTab]
+    static constexpr int BAR_OFF = FTAB_OFF + kFillTab * 4;
     // ring full/empty [NT], q full/empty [QB], s full/free [2], p full [PB],
     // pv done [PB], o free [2] (OB used), drain
     static constexpr int B_FULL = 0, B_EMPTY = NT, B_QFULL = 2 * NT, B_QEMPTY = B_QFULL + QB,
@@ -237,6 +243,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     float *alpha_sm = reinterpret_cast<float *>(sm + C::ALPHA_OFF);
     uint32_t *rowidx = reinterpret_cast<uint32_t *>(sm + C::ROW_OFF);
     TcItem *meta = reinterpret_cast<TcItem *>(sm + C::META_OFF);
+    volatile uint32_t *ftab = reinterpret_cast<volatile uint32_t *>(sm + C::FTAB_OFF);
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::BAR_OFF);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::MISC_OFF);
 
@@ -288,6 +295,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     grid_dep_wait();
     grid_dep_trigger();
     // metadata of this CTA's first items
+    for (int i = tid; i < kFillTab; i += kTcThreads) ftab[i] = 0xffffffffu;
     for (int j = tid; j < kTcMetaItems; j += kTcThreads) {
         const long long item = (long long)blockIdx.x + (long long)j * gridDim.x;
         if (item < T.items) meta[j] = tc_decode_global(T, (int)item);
@@ -328,6 +336,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     tma_load_3d_hint(dst + a * C::ATOM_BYTES, m1, 0, y + 8 * a, 0, bar, policy);
             };
             uint32_t f = 0, k = 0;  // fills (two per tile: K then V), items with keys
+            uint32_t uses[NT];      // fills handed to each slot so far
+#pragma unroll
+            for (int s2 = 0; s2 < NT; ++s2) uses[s2] = 0;
             bool ok = true;
             int j = 0;
             for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
@@ -358,10 +369,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             ok = load_q();
                             if (!ok) break;
                         }
-                        const uint32_t slot = f % NT;
-                        ok = mbar_wait_bounded(&bars[C::B_EMPTY + slot], ((f / NT) & 1) ^ 1,
-                                               P.fault, kFaultCopyTimeout);
+                        // the first free slot: never used, or its last fill consumed
+                        int slot = -1;
+                        uint32_t par = 0;
+                        const long long w0 = clock64();
+                        for (int spin = 0;; ++spin) {
+#pragma unroll
+                            for (int s2 = 0; s2 < NT; ++s2) {
+                                if (slot < 0 && (uses[s2] == 0 ||
+                                                 mbar_test(&bars[C::B_EMPTY + s2], (uses[s2] - 1) & 1))) {
+                                    slot = s2;
+                                    par = uses[s2] & 1;
+                                    ++uses[s2];
+                                }
+                            }
+                            if (slot >= 0) break;
+                            if (clock64() - w0 > kWaitLimitCycles) {
+                                atomicOr(P.fault, kFaultCopyTimeout);
+                                ok = false;
+                                break;
+                            }
+                            if (spin > 8) __nanosleep(32);
+                        }
                         if (!ok) break;
+                        ftab[f % kFillTab] = (f << 8) | (par << 4) | (uint32_t)slot;
                         uint64_t *bar = &bars[C::B_FULL + slot];
                         mbar_arrive_expect_tx(bar, (uint32_t)(atoms + (rem != 0)) * C::ATOM_BYTES);
                         tile_copies(kv, y, n_valid, ring + slot * C::TILE_BYTES, bar);
@@ -370,12 +401,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             // every copy this CTA issued has landed before it exits
-            const uint32_t n_drain = f < (uint32_t)NT ? f : (uint32_t)NT;
-            for (uint32_t q = 0; q < n_drain; ++q) {
-                const uint32_t fi = f - 1 - q;
-                mbar_wait_bounded(&bars[C::B_FULL + fi % NT], (fi / NT) & 1, P.fault,
-                                  kFaultCopyTimeout);
-            }
+#pragma unroll
+            for (int s2 = 0; s2 < NT; ++s2)
+                if (uses[s2] > 0)
+                    mbar_wait_bounded(&bars[C::B_FULL + s2], (uses[s2] - 1) & 1, P.fault,
+                                      kFaultCopyTimeout);
             const uint32_t nq = k < (uint32_t)QB ? k : (uint32_t)QB;
             for (uint32_t q = 0; q < nq; ++q) {
                 const uint32_t kq = k - 1 - q;
@@ -397,12 +427,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t ring_a = smem_u32(ring);
             const uint32_t qs_a = smem_u32(qs);
             const uint32_t ps_a = smem_u32(ps);
-            // tile g of this CTA fills ring slots 2g (K) and 2g + 1 (V), modulo NT
+            // tile g of this CTA is fills 2g (K) and 2g + 1 (V); the fill table
+            // says which slot (and use parity) each landed in
             struct Cursor {
                 int item, j, t, n_tiles;
                 int last_keys;  // keys of the item's last tile
                 uint32_t k, g;
                 bool valid;
+                int slot;       // this cursor's fill: slot, parity (-1: not yet looked up)
+                uint32_t par;
+            };
+            auto lookup = [&](Cursor &c, uint32_t fill) -> bool {
+                if (c.slot >= 0) return true;
+                const uint32_t e = ftab[fill % kFillTab];
+                if ((e >> 8) != (fill & 0xffffffu)) return false;
+                c.slot = (int)(e & 15u);
+                c.par = (e >> 4) & 1u;
+                return true;
             };
             // first tile of the next non-empty item at or after (item, j)
             auto seek = [&](Cursor &c) {
@@ -420,13 +461,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             };
             auto advance = [&](Cursor &c) {
                 ++c.g;
+                c.slot = -1;
                 if (++c.t < c.n_tiles) return;
                 ++c.k;
                 c.item += gridDim.x;
                 ++c.j;
                 seek(c);
             };
-            Cursor qc{(int)blockIdx.x, 0, 0, 0, 0, 0u, 0u, false};
+            Cursor qc{(int)blockIdx.x, 0, 0, 0, 0, 0u, 0u, false, -1, 0u};
             seek(qc);
             Cursor pc = qc;
             bool ok = true;
@@ -437,12 +479,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // ---- PV of tile pc.g (its S was issued before)
                 if (pc.g < qc.g || !qc.valid) {
                     const uint32_t pb = pc.g % PB;
-                    const uint32_t fv = 2 * pc.g + 1;
-                    const uint32_t vslot = fv % NT;
                     bool ready = mbar_test(&bars[C::B_PFULL + pb], (pc.g / PB) & 1);
                     if (ready && pc.t == 0)
                         ready = mbar_test(&bars[C::B_OFREE + pc.k % OB], ((pc.k / OB) & 1) ^ 1);
-                    ready = ready && mbar_test(&bars[C::B_FULL + vslot], (fv / NT) & 1);
+                    ready = ready && lookup(pc, 2 * pc.g + 1) &&
+                            mbar_test(&bars[C::B_FULL + pc.slot], pc.par);
+                    const uint32_t vslot = (uint32_t)pc.slot;
                     if (ready) {
                         fence_after_sync();
                         // a partial tile: only the 16-key steps that hold valid keys
@@ -509,22 +551,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         progressed = true;
                     }
                 }
-                // ---- S of tile qc.g
-                if (qc.valid) {
+                // ---- S of tile qc.g, at most one tile ahead of the PV cursor: the
+                // tensor pipe runs in issue order, so an S batch issued early
+                // would hold back the PV that the softmax warps wait for
+                if (qc.valid && qc.g <= pc.g + 1) {
                     const uint32_t sb = qc.g & 1;
-                    const uint32_t fk = 2 * qc.g;
-                    const uint32_t kslot = fk % NT;
                     bool ready = mbar_test(&bars[C::B_SFREE + sb], ((qc.g >> 1) & 1) ^ 1) &&
-                                 mbar_test(&bars[C::B_QFULL + qc.k % QB], (qc.k / QB) & 1);
-                    // A parity test is only meaningful when the slot's previous
-                    // fill has completed its phase, i.e. has been consumed.  The
-                    // previous fill of a K slot can be the V tile of an earlier
-                    // tile whose PV is still pending: then the slot is not ours yet.
-                    if (fk >= (uint32_t)NT) {
-                        const uint32_t fp = fk - NT;
-                        if ((fp & 1) && pc.g <= fp / 2) ready = false;
-                    }
-                    ready = ready && mbar_test(&bars[C::B_FULL + kslot], (fk / NT) & 1);
+                                 mbar_test(&bars[C::B_QFULL + qc.k % QB], (qc.k / QB) & 1) &&
+                                 lookup(qc, 2 * qc.g) &&
+                                 mbar_test(&bars[C::B_FULL + qc.slot], qc.par);
+                    const uint32_t kslot = (uint32_t)qc.slot;
                     if (ready) {
                         fence_after_sync();
                         if (leader) {
@@ -686,26 +722,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     }
                     group_sync(wg);
                     const bool rescale = t > 0;
+                    // all four warps' maxima first (no shared-memory store in
+                    // between, so the loads issue back to back), then the
+                    // references and the rescale factor
+                    float tm[HN];
 #pragma unroll
                     for (int r4 = 0; r4 < HN; r4 += 4) {
                         const float4 a0 = *reinterpret_cast<const float4 *>(rd + r4);
                         const float4 a1 = *reinterpret_cast<const float4 *>(rd + N + r4);
                         const float4 a2 = *reinterpret_cast<const float4 *>(rd + 2 * N + r4);
                         const float4 a3 = *reinterpret_cast<const float4 *>(rd + 3 * N + r4);
-                        const float tm[4] = {fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x)),
-                                             fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y)),
-                                             fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z)),
-                                             fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w))};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float mo = mref[r4 + e];
-                            const float mn = fmaxf(mo, tm[e]);
-                            const float al = (mn == mo) ? 1.f : fast_exp2(mo - mn);
-                            if (rescale && gtid == r4 + e) alpha_sm[r0 + r4 + e] = al;
-                            lrow[r4 + e] *= al;
-                            mref[r4 + e] = mn;
-                        }
+                        tm[r4] = fmaxf(fmaxf(a0.x, a1.x), fmaxf(a2.x, a3.x));
+                        tm[r4 + 1] = fmaxf(fmaxf(a0.y, a1.y), fmaxf(a2.y, a3.y));
+                        tm[r4 + 2] = fmaxf(fmaxf(a0.z, a1.z), fmaxf(a2.z, a3.z));
+                        tm[r4 + 3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
                     }
+                    float my_alpha = 1.f;
+#pragma unroll
+                    for (int r = 0; r < HN; ++r) {
+                        const float mo = mref[r];
+                        const float mn = fmaxf(mo, tm[r]);
+                        const float al = (mn == mo) ? 1.f : fast_exp2(mo - mn);
+                        if (gtid == r) my_alpha = al;
+                        lrow[r] *= al;
+                        mref[r] = mn;
+                    }
+                    if (rescale && gtid < HN) alpha_sm[r0 + gtid] = my_alpha;
                     if (rescale) {
                         // every PV of this item so far has completed before O is scaled
                         const uint32_t gp = g - 1;
@@ -819,6 +861,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             };
             if (P.splits == 1) {
                 constexpr int RB = D * 2, RPC = HN * 128 / RB;
+                // 1/l of the group's rows into registers first: no shared-memory
+                // load then sits between the staging stores
+                float li[HN];
+#pragma unroll
+                for (int r = 0; r < HN; ++r) li[r] = linv[r0 + r];
 #pragma unroll
                 for (int mh = 0; mh < MH; ++mh) {
 #pragma unroll
@@ -832,7 +879,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                             const float ov = __uint_as_float(o[e]) + __uint_as_float(ol[e]);
                             *reinterpret_cast<__nv_bfloat16 *>(stg_row(c0 + e, RB, RPC) +
                                                                (mh * 128 + lk) * 2) =
-                                __float2bfloat16_rn(ov * linv[r0 + c0 + e]);
+                                __float2bfloat16_rn(ov * li[c0 + e]);
                         }
                     }
                 }
