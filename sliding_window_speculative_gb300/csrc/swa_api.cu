@@ -21,6 +21,7 @@ __device__ uint32_t g_fault_word = 0;
 namespace {
 
 constexpr int kMaxSplits = 64;
+constexpr int kTcKeysPerTile = 128;  // keys per tensor-core tile (MMA M)
 static_assert(kMaxSplits <= swa::kMergeMaxSplits, "the merge kernel weighs at most 64 splits");
 constexpr int kMaxQLen = 64;      // SPLITKV_VERIFY_MAX_Q
 constexpr int kMaxDevices = 64;
@@ -96,10 +97,10 @@ int forced_kernel() {
 // Split heuristic.  Host-only: seq_lens live on the device, so the
 // worst-case span W + q_len - 1 (bounded by the cache length) is used.
 //  - Tensor-core path (head_dim 128/256; >= 16 packed rows, or a batch whose
-//    (sequence, KV head) units cover half the SMs): one chunk per
-//    (sequence, KV head, row tile) once those units cover half the SMs;
-//    otherwise enough chunks of >= 64 keys to reach every SM.  Persistent
-//    grid of at most SMs x resident CTAs.
+//    (sequence, KV head) units cover half the SMs): one chunk per (sequence,
+//    KV head, row tile) once those units cover half the SMs or the span is at
+//    most three 128-key tiles; otherwise enough chunks of >= 128 keys to reach
+//    every SM.  Persistent grid of at most SMs x resident CTAs.
 //  - CUDA-core path: enough CTAs to cover every SM about twice, chunks of at
 //    least one 32-key tile.
 // Chunks are multiples of 16 keys; at most kMaxSplits chunks.
@@ -140,11 +141,14 @@ Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
         const long long units = (long long)d->batch * d->num_kv_heads * p.row_tiles;
         if (d->num_splits > 0) {
             splits = d->num_splits;
-        } else if (units * 2 >= num_sms) {
+        } else if (units * 2 >= num_sms || span <= 3 * kTcKeysPerTile) {
+            // a split costs a partial round trip, a dependent merge launch
+            // and the merge (~2.5 us measured on GB300), which a span of up to
+            // three 128-key tiles (~1.2 us each) does not win back
             splits = 1;
         } else {
             long long s = (num_sms + units - 1) / units;
-            const long long by_len = (span + 63) / 64;
+            const long long by_len = (span + kTcKeysPerTile - 1) / kTcKeysPerTile;
             splits = (int)(s < by_len ? s : by_len);
         }
         if (splits < 1) splits = 1;

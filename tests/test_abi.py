@@ -149,9 +149,17 @@ def test_plan_forced_splits(lib, monkeypatch):
     assert swa.swa_plan(dims, 188, 152)["num_splits"] <= 64
 
 
-def test_plan_fills_the_gpu_for_one_sequence(lib):
+def test_plan_splits_long_spans_of_one_sequence(lib):
+    # a W=188 span (two 128-key tiles) stays one chunk on the tensor-core
+    # path: a split's merge costs more than the tile it saves
     p = swa.swa_plan(swa.make_dims(1, 8, 8, 2, 256, 4096), 188, 152)
-    assert p["num_splits"] > 1
+    assert p["kernel"] == 2 and p["num_splits"] == 1
+    # a full-context decode spreads over the SMs in chunks of >= 128 keys
+    p = swa.swa_plan(swa.make_dims(1, 8, 8, 2, 256, 4096), 4096, 152)
+    assert p["kernel"] == 2 and p["num_splits"] == 32 and p["chunk_keys"] == 128
+    # the CUDA-core path (q_len 1, one sequence) still splits W=188
+    p = swa.swa_plan(swa.make_dims(1, 1, 8, 2, 256, 4096), 188, 152)
+    assert p["kernel"] == 1 and p["num_splits"] > 1
 
 
 def test_binding_rejects_cpu_tensors(lib):

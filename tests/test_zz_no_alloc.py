@@ -41,11 +41,12 @@ def _close(out, lse, ref_out, ref_lse, what):
         assert np.abs(la[fin] - lb[fin]).max() <= LSE_ATOL, what
 
 
-@pytest.mark.parametrize("name,splits", [("single_stream", 0), ("single_stream", 4),
+@pytest.mark.parametrize("name,splits", [("full_decode", 0), ("single_stream", 4),
                                          ("tiny_q8", 3), ("batched", 2)])
 def test_noalloc_matches_allocating_entry_point(name, splits):
     import sliding_window_speculative_gb300 as swa
-    case = {"single_stream": lambda: inputs.single_stream(device="cuda"),
+    case = {"full_decode": lambda: inputs.window_vs_full(4096, device="cuda"),
+            "single_stream": lambda: inputs.single_stream(device="cuda"),
             "tiny_q8": lambda: inputs.tiny(8, device="cuda"),
             "batched": lambda: inputs.batched(device="cuda")}[name]()
     plan = swa.swa_plan(swa.dims_of(case.q, case.k_cache, splits), case.window,
