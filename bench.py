@@ -369,6 +369,66 @@ def aggregate(seconds, bytes_per_step, steps, dist=None, device="cpu"):
     return slowest, bytes_per_step * steps * world / slowest / 1e9
 
 
+def source_digest():
+    """sha256 (first 16 hex digits) of the CUDA library's sources: a traffic
+    figure taken by ncu applies only while it matches."""
+    import hashlib
+    csrc = os.path.join(ROOT, "sliding_window_speculative_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload):
+    """DRAM bytes (read + write) per launch of the dominant kernel, from the
+    committed ncu summary profiles/traffic.json, or None when that capture
+    predates the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None, None
+    if d.get("source_sha") != source_digest():
+        return None, "stale"
+    w = d.get("workloads", {}).get(workload)
+    if not w:
+        return None, None
+    return int(w["dram_bytes_per_launch"]), w.get("kernel")
+
+
+def launch_floor(steps, graph_len=1000):
+    """Per-launch time of a one-element kernel replayed from a CUDA graph the
+    way the calls are: the floor any single-kernel call sits on."""
+    x = torch.zeros(1, device="cuda")
+    stream = torch.cuda.Stream()
+    n = max(1, min(graph_len, steps))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            x.add_(1.0)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(n):
+            x.add_(1.0)
+    with torch.cuda.stream(stream):
+        g.replay()
+    stream.synchronize()
+    reps = max(1, steps // n)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            g.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) * 1e3 / (reps * n)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -430,6 +490,8 @@ def main():
     peak, peak_src = peaks()
     launches_per_call = 1 + plan["merge"]
     achieved = total / (us * 1e-6) / 1e9
+    traffic, traffic_kernel = ncu_traffic(args.workload)
+    floor_us = launch_floor(args.steps) if rank == 0 else None
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
@@ -446,8 +508,16 @@ def main():
                      (" + swa_merge_kernel" if plan["merge"] else ""),
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
-                     "traffic": None,
-                     "note": "achieved = algorithmic bytes per call / device time per call"},
+                     "traffic": traffic,
+                     "traffic_source": ("profiles/traffic.json (ncu dram__bytes_read.sum + "
+                                        "dram__bytes_write.sum per launch)" if traffic else
+                                        ("stale: kernel sources changed since the capture"
+                                         if traffic_kernel == "stale" else None)),
+                     "launch_floor_us": round(floor_us, 3) if floor_us else None,
+                     "floor_frac": round(floor_us * launches_per_call / us, 4) if floor_us else None,
+                     "note": "achieved = algorithmic bytes per call / device time per call "
+                             "(one attention kernel per call when the plan does not split); "
+                             "floor_frac = launch floor x kernels per call / time per call"},
         "clocks": clocks,
         "gpu_launches": launches_per_call * args.steps,
     }
@@ -471,7 +541,7 @@ def main():
                           "kv_gbs": round(k2 / (r2["us_per_call"] * 1e-6) / 1e9, 2),
                           "achieved_gbs": round(ach, 2), "frac": round(ach / peak, 4),
                           "steps": steps2, "replicas": r2["replicas"],
-                          "splits": p2["num_splits"]}
+                          "splits": p2["num_splits"], "traffic": ncu_traffic(name)[0]}
             del c2
             torch.cuda.empty_cache()
         line["also"] = also
