@@ -42,6 +42,7 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
+KERNEL_NAMES = {1: "swa_simt_kernel", 2: "swa_tc_kernel", 3: "swa_rows_kernel"}
 METRIC = "verify-attn µs/call and KV GB/s (% of GB300 HBM peak) at W=188, q_len=8"
 UNIT = "GB/s"
 
@@ -503,8 +504,7 @@ def main():
                          if r["replicas"] > 1 else "inputs larger than L2",
                    "timing": "CUDA graph of calls, CUDA events on the launching stream",
                    "plan": plan, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
-        "roofline": {"bound": "hbm", "kernel": ("swa_tc_kernel" if plan["kernel"] == 2
-                                                 else "swa_simt_kernel") +
+        "roofline": {"bound": "hbm", "kernel": KERNEL_NAMES.get(plan["kernel"], "?") +
                      (" + swa_merge_kernel" if plan["merge"] else ""),
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
@@ -536,7 +536,7 @@ def main():
             p2 = swa.swa_plan(swa.dims_of(c2.q, c2.k_cache), c2.window,
                               torch.cuda.get_device_properties(dev).multi_processor_count)
             ach = t2 / (r2["us_per_call"] * 1e-6) / 1e9
-            also[name] = {"kernel": "tc" if p2["kernel"] == 2 else "simt",
+            also[name] = {"kernel": KERNEL_NAMES.get(p2["kernel"], "?"),
                           "us_per_call": round(r2["us_per_call"], 3),
                           "kv_gbs": round(k2 / (r2["us_per_call"] * 1e-6) / 1e9, 2),
                           "achieved_gbs": round(ach, 2), "frac": round(ach / peak, 4),

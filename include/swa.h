@@ -119,7 +119,8 @@ swa_status swa_release_workspace(void);
 /* What the library would launch for these dims on a GPU with `num_sms`
  * SMs (pure host arithmetic, no CUDA call). */
 typedef struct {
-    int32_t kernel;        /* 1 = CUDA-core (SIMT) chunk kernel, 2 = tensor-core (tcgen05) kernel */
+    int32_t kernel;        /* 1 = CUDA-core (SIMT) chunk kernel, 2 = key-major tensor-core
+                              (tcgen05) kernel, 3 = rows-major tensor-core kernel */
     int32_t num_splits;    /* chunks per (sequence, KV head)                    */
     int32_t chunk_keys;    /* keys per chunk                                    */
     int32_t row_tiles;     /* CTAs along the packed rows R = q_len * G          */

@@ -91,6 +91,7 @@ int forced_kernel() {
     if (v == nullptr) return 0;
     if (strcmp(v, "simt") == 0) return 1;
     if (strcmp(v, "tc") == 0) return 2;
+    if (strcmp(v, "rows") == 0) return 3;
     return 0;
 }
 
@@ -127,7 +128,16 @@ Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
     const bool big_batch = (long long)d->batch * d->num_kv_heads * 2 >= num_sms;
     const bool use_tc = tc_shape && (force == 2 || (force == 0 && (R >= 16 || big_batch)));
     int splits;
-    if (use_tc) {
+    const bool use_rows = tc_shape && force == 3;
+    if (use_rows) {
+        // rows-major kernel: up to 128 packed rows per item (the MMA's M)
+        p.kernel = 3;
+        const int max_rows = 128;
+        p.rows_per_tile = R <= max_rows ? R : (max_rows / G) * G;
+        p.q_rows_per_tile = p.rows_per_tile / G;
+        p.row_tiles = ceil_div(d->q_len, p.q_rows_per_tile);
+        p.tc_n = p.rows_per_tile <= 32 ? 32 : p.rows_per_tile <= 64 ? 64 : 128;
+    } else if (use_tc) {
         p.kernel = 2;
         // rows per item: at most 64 (shared memory holds Q and P tiles beside
         // the ring; the softmax keeps a row's reference maximum in registers)
@@ -136,8 +146,9 @@ Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
         p.q_rows_per_tile = p.rows_per_tile / G;
         p.row_tiles = ceil_div(d->q_len, p.q_rows_per_tile);
         p.tc_n = p.rows_per_tile <= 16 ? 16 : p.rows_per_tile <= 32 ? 32 : 64;
-        swa::TcConfInfo ci{};
-        swa::tc_conf(D, p.tc_n, &ci);
+    }
+    if (use_rows || use_tc) {
+        const int ctas_per_sm = 1;  // both tensor-core kernels: one persistent CTA per SM
         const long long units = (long long)d->batch * d->num_kv_heads * p.row_tiles;
         if (d->num_splits > 0) {
             splits = d->num_splits;
@@ -160,7 +171,7 @@ Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
         p.splits = splits;
         p.chunk = (int)chunk;
         p.items = (long long)splits * units;
-        const long long slots = (long long)num_sms * ci.ctas_per_sm;
+        const long long slots = (long long)num_sms * ctas_per_sm;
         p.grid = p.items < slots ? p.items : slots;
     } else {
         p.kernel = 1;
@@ -281,7 +292,7 @@ cudaError_t launch_merge(const swa::AttnParams &P, cudaStream_t s) {
 swa_status launch_plan(const Plan &pl, const swa_dims *dims, const swa::AttnParams &P,
                        const void *q, const void *k_cache, const void *v_cache, cudaStream_t s) {
     cudaError_t e;
-    if (pl.kernel == 2) {
+    if (pl.kernel >= 2) {
         swa::TcLaunch L{};
         L.T.a = P;
         L.T.rows_per_tile = pl.rows_per_tile;
@@ -289,6 +300,7 @@ swa_status launch_plan(const Plan &pl, const swa_dims *dims, const swa::AttnPara
         L.T.items = (int)pl.items;
         L.D = dims->head_dim;
         L.N = pl.tc_n;
+        L.rows_major = pl.kernel == 3;
         L.grid = (int)pl.grid;
         L.q = q;
         L.k = k_cache;

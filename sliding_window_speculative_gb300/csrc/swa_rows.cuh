@@ -1,0 +1,616 @@
+// Tensor-core (tcgen05) split-KV kernel with query rows as the MMA's M
+// dimension, for sliding-window verify attention.
+//
+// For every tile of 128 keys of a work item (sequence, KV head, key chunk,
+// row tile of up to 128 packed rows):
+//
+//   S[128 rows x 128 keys] = Q[128 x D] . K_tile^T          (TMEM, fp32)
+//   O[128 rows x D]       += P_hi . V_tile + P_lo . V_tile  (TMEM, fp32)
+//
+// The packed rows (G query heads of the KV head times the draft rows) are
+// the TMEM lanes, so a softmax thread owns one row: the row maximum, the
+// weights and the row sum stay inside the thread, and P goes back into the
+// TMEM columns of its S buffer (P_hi = bf16 truncation in columns 0..63,
+// P_lo = the rest rounded to bf16 in 64..127) as the A operand of the two
+// PV MMAs.  P never touches shared memory, and nothing is reduced across
+// threads.
+//
+// Q sits in shared memory as [slab][QR rows][128 bytes] (QR = 32, 64 or
+// 128); an MMA reads 128 rows per slab, so with fewer rows it reads past the
+// buffer into the ring: those S rows are never used.  K and V tiles arrive
+// exactly as for the key-major kernel (one 4D TMA per tile into first-free
+// ring slots, atoms of [slab][8 rows][128 B]); K is the B operand of the
+// score MMA (K-major), V the B operand of the PV MMAs (MN-major, N = D).
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer (one lane)
+//   warp 1      TMEM owner and MMA issuer (one lane)
+//   warps 2..5  softmax / epilogue; warp w owns TMEM lanes 32 (w % 4)..,
+//               i.e. packed rows 32 (w % 4)..; warps without rows idle.
+//
+// TMEM: S/P buffers at columns 0 and 128, O at 256 (two O buffers at head
+// dim 128).  Every wait is bounded; a wait that gives up sets the fault
+// word and the roles leave their loops.
+#pragma once
+
+#include "swa_tc.cuh"
+
+namespace swa {
+
+constexpr int kRowsThreads = 192;
+
+template <int D, int QR, int NT, int QB>
+struct RowsCfg {
+    static constexpr int SLABS = D / 64;
+    static constexpr int ATOM_BYTES = SLABS * 1024;  // 8 keys x D
+    static constexpr int TILE_BYTES = (kTcTileKeys / 8) * ATOM_BYTES;
+    static constexpr int Q_SLAB = QR * 128;          // QR rows x 64 dims
+    static constexpr int Q_BUF = SLABS * Q_SLAB;
+    static constexpr int Q_OFF = 0;                  // Q first: short-Q reads run into the ring
+    static constexpr int RING_OFF = QB * Q_BUF;
+    static constexpr int META_OFF = RING_OFF + NT * TILE_BYTES;  // TcItem [kTcMetaItems]
+    static constexpr int FTAB_OFF = META_OFF + kTcMetaItems * (int)sizeof(TcItem);
+    static constexpr int BAR_OFF = FTAB_OFF + kFillTab * 4;
+    static constexpr int OB = D == 128 ? 2 : 1;      // O buffers in TMEM
+    // ring full/empty [NT], q full/empty [QB], s full [2], s free [2],
+    // p full [2], pv done [2], o free [OB], drain
+    static constexpr int B_FULL = 0, B_EMPTY = NT, B_QFULL = 2 * NT, B_QEMPTY = B_QFULL + QB,
+                         B_SFULL = B_QEMPTY + QB, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2,
+                         B_PVDONE = B_PFULL + 2, B_OFREE = B_PVDONE + 2, B_DRAIN = B_OFREE + OB,
+                         NBARS = B_DRAIN + 1;
+    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base
+    static constexpr int END = MISC_OFF + 16;
+    static constexpr int SMEM_BYTES = END + 1024;  // slack for 1024-byte alignment
+    static constexpr int O_COL = 256;
+    static constexpr int TMEM_COLS = 512;
+    static_assert(QR == 32 || QR == 64 || QR == 128, "Q rows");
+    static_assert(NT >= 2, "ring holds at least a K and a V tile");
+    static_assert(O_COL + OB * D <= TMEM_COLS, "TMEM");
+    static_assert(QB * Q_BUF - Q_SLAB + 128 * 128 <= RING_OFF + NT * TILE_BYTES,
+                  "an MMA's 128-row read of the last Q slab stays in shared memory");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+template <int D, int QR, int NT, int QB>
+__global__ void __launch_bounds__(kRowsThreads, 1)
+    swa_rows_kernel(const __grid_constant__ TcParams T, const __grid_constant__ TcMaps M) {
+    using C = RowsCfg<D, QR, NT, QB>;
+    using namespace tc;
+    constexpr int SLABS = C::SLABS;
+    constexpr int OB = C::OB;
+    const float NEG_INF = -__int_as_float(0x7f800000);
+    const AttnParams &P = T.a;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~static_cast<uintptr_t>(1023));
+    uint8_t *qs = sm + C::Q_OFF;
+    uint8_t *ring = sm + C::RING_OFF;
+    TcItem *meta = reinterpret_cast<TcItem *>(sm + C::META_OFF);
+    volatile uint32_t *ftab = reinterpret_cast<volatile uint32_t *>(sm + C::FTAB_OFF);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + C::BAR_OFF);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::MISC_OFF);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    // quadrants (warps of 32 rows) that hold packed rows of an item
+    const int act_q = (T.rows_per_tile + 31) >> 5;
+    const uint32_t n_act = 32u * (uint32_t)act_q;
+
+    // ---------------------------------------------------------------- setup
+    if (warp == 0 && lane < 11) {
+        const CUtensorMap *mp = lane < 4    ? &M.k_atoms[lane]
+                                : lane < 8  ? &M.v_atoms[lane - 4]
+                                : lane == 8 ? &M.k_atom
+                                : lane == 9 ? &M.v_atom
+                                            : &M.q;
+        prefetch_tmap(mp);
+    }
+    if (tid == 0) {
+        for (int i = 0; i < NT; ++i) {
+            mbar_init(&bars[C::B_FULL + i], 1);
+            mbar_init(&bars[C::B_EMPTY + i], 1);
+        }
+        for (int i = 0; i < QB; ++i) {
+            mbar_init(&bars[C::B_QFULL + i], 1);
+            mbar_init(&bars[C::B_QEMPTY + i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars[C::B_SFULL + i], 1);
+            mbar_init(&bars[C::B_SFREE + i], 1);
+            mbar_init(&bars[C::B_PFULL + i], n_act);
+            mbar_init(&bars[C::B_PVDONE + i], 1);
+        }
+        for (int i = 0; i < OB; ++i) mbar_init(&bars[C::B_OFREE + i], n_act);
+        mbar_init(&bars[C::B_DRAIN], 1);
+        fence_barrier_init();
+    }
+    for (int i = tid; i < kFillTab; i += kRowsThreads) ftab[i] = 0xffffffffu;
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    grid_dep_wait();
+    grid_dep_trigger();
+    for (int j = tid; j < kTcMetaItems; j += kRowsThreads) {
+        const long long item = (long long)blockIdx.x + (long long)j * gridDim.x;
+        if (item < T.items) meta[j] = tc_decode_global(T, (int)item);
+    }
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ======================================================= producer
+        if (lane == 0) {
+            const uint64_t policy = l2_policy_evict_first();
+            // the copies of one K or V tile of n_valid keys starting at cache row y
+            auto tile_copies = [&](int kv, int y, int n_valid, uint8_t *dst, uint64_t *bar) {
+                const int atoms = n_valid >> 3, rem = n_valid & 7;
+                const CUtensorMap *m4 = kv ? M.v_atoms : M.k_atoms;
+                const CUtensorMap *m1 = kv ? &M.v_atom : &M.k_atom;
+                if (atoms == 16) {
+                    tma_load_4d_hint(dst, &m4[0], 0, y, 0, 0, bar, policy);
+                    return;
+                }
+                // whole atoms lie inside the chunk (4D boxes); the last, partial
+                // atom goes through the bounds-checked one-atom box
+                int a = 0;
+#pragma unroll
+                for (int bi = 1; bi < 4; ++bi) {
+                    const int na = 16 >> bi;
+                    if (atoms & na) {
+                        tma_load_4d_hint(dst + a * C::ATOM_BYTES, &m4[bi], 0, y + 8 * a, 0, 0, bar,
+                                         policy);
+                        a += na;
+                    }
+                }
+                for (int e = 0; e < (atoms & 1) + (rem != 0); ++e, ++a)
+                    tma_load_3d_hint(dst + a * C::ATOM_BYTES, m1, 0, y + 8 * a, 0, bar, policy);
+            };
+            uint32_t f = 0, k = 0;  // fills (two per tile: K then V), items with keys
+            uint32_t uses[NT];      // fills handed to each slot so far
+#pragma unroll
+            for (int s2 = 0; s2 < NT; ++s2) uses[s2] = 0;
+            bool ok = true;
+            int j = 0;
+            for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
+                const TcItem it = tc_decode(T, item, j, meta);
+                if (it.n_tiles == 0) continue;
+                const uint32_t qb = k % QB, quse = k / QB;
+                // Q of the item (its rows x 64 dims per slab), issued after the
+                // item's first K tile
+                auto load_q = [&]() -> bool {
+                    if (!mbar_wait_bounded(&bars[C::B_QEMPTY + qb], (quse & 1) ^ 1, P.fault,
+                                           kFaultCopyTimeout))
+                        return false;
+                    mbar_arrive_expect_tx(&bars[C::B_QFULL + qb], SLABS * T.rows_per_tile * 128);
+                    for (int s = 0; s < SLABS; ++s)
+                        tma_load_3d(qs + qb * C::Q_BUF + s * C::Q_SLAB, &M.q, 64 * s,
+                                    it.h * P.G, it.b * P.q_len + it.i0, &bars[C::B_QFULL + qb]);
+                    return true;
+                };
+                ++k;
+                const int y0 = (it.b * P.Hkv + it.h) * P.L + it.cr.c_lo;
+                for (int t = 0; t < it.n_tiles && ok; ++t) {
+                    const int n_valid =
+                        min(kTcTileKeys, it.cr.c_hi - it.cr.c_lo - kTcTileKeys * t);
+                    const int atoms = n_valid >> 3, rem = n_valid & 7;
+                    const int y = y0 + kTcTileKeys * t;
+                    for (int kv = 0; kv < 2 && ok; ++kv) {
+                        if (t == 0 && kv == 1) {
+                            ok = load_q();
+                            if (!ok) break;
+                        }
+                        // the first free slot: never used, or its last fill consumed
+                        int slot = -1;
+                        uint32_t par = 0;
+                        const long long w0 = clock64();
+                        for (int spin = 0;; ++spin) {
+#pragma unroll
+                            for (int s2 = 0; s2 < NT; ++s2) {
+                                if (slot < 0 && (uses[s2] == 0 ||
+                                                 mbar_test(&bars[C::B_EMPTY + s2], (uses[s2] - 1) & 1))) {
+                                    slot = s2;
+                                    par = uses[s2] & 1;
+                                    ++uses[s2];
+                                }
+                            }
+                            if (slot >= 0) break;
+                            if (clock64() - w0 > kWaitLimitCycles) {
+                                atomicOr(P.fault, kFaultCopyTimeout);
+                                ok = false;
+                                break;
+                            }
+                            if (spin > 8) __nanosleep(32);
+                        }
+                        if (!ok) break;
+                        ftab[f % kFillTab] = (f << 8) | (par << 4) | (uint32_t)slot;
+                        uint64_t *bar = &bars[C::B_FULL + slot];
+                        mbar_arrive_expect_tx(bar, (uint32_t)(atoms + (rem != 0)) * C::ATOM_BYTES);
+                        tile_copies(kv, y, n_valid, ring + slot * C::TILE_BYTES, bar);
+                        ++f;
+                    }
+                }
+            }
+            // every copy this CTA issued has landed before it exits
+#pragma unroll
+            for (int s2 = 0; s2 < NT; ++s2)
+                if (uses[s2] > 0)
+                    mbar_wait_bounded(&bars[C::B_FULL + s2], (uses[s2] - 1) & 1, P.fault,
+                                      kFaultCopyTimeout);
+            const uint32_t nq = k < (uint32_t)QB ? k : (uint32_t)QB;
+            for (uint32_t q = 0; q < nq; ++q) {
+                const uint32_t kq = k - 1 - q;
+                mbar_wait_bounded(&bars[C::B_QFULL + kq % QB], (kq / QB) & 1, P.fault,
+                                  kFaultCopyTimeout);
+            }
+        }
+    } else if (warp == 1) {
+        // ============================================================ MMA
+        // Two cursors over the tile sequence: S = Q K^T of the next tile and
+        // O += P_hi V + P_lo V of the oldest tile whose P is in TMEM, each
+        // issued as soon as its operands are there (S at most one tile ahead
+        // of PV).  The whole warp runs the loop; lane 0 issues.
+        {
+            const bool leader = lane == 0;
+            constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, 0, 0);
+            constexpr uint32_t ID_O = idesc_bf16_f32(128, D, 0, 1);
+            const uint32_t ring_a = smem_u32(ring);
+            const uint32_t qs_a = smem_u32(qs);
+            struct Cursor {
+                int item, j, t, n_tiles;
+                int last_keys;  // keys of the item's last tile
+                uint32_t k, g;
+                bool valid;
+                int slot;       // this cursor's fill: slot, parity (-1: not yet looked up)
+                uint32_t par;
+            };
+            auto lookup = [&](Cursor &c, uint32_t fill) -> bool {
+                if (c.slot >= 0) return true;
+                const uint32_t e = ftab[fill % kFillTab];
+                if ((e >> 8) != (fill & 0xffffffu)) return false;
+                c.slot = (int)(e & 15u);
+                c.par = (e >> 4) & 1u;
+                return true;
+            };
+            auto seek = [&](Cursor &c) {
+                for (; c.item < T.items; c.item += gridDim.x, ++c.j) {
+                    const TcItem it = tc_decode(T, c.item, c.j, meta);
+                    if (it.n_tiles > 0) {
+                        c.n_tiles = it.n_tiles;
+                        c.last_keys = it.cr.c_hi - it.cr.c_lo - kTcTileKeys * (it.n_tiles - 1);
+                        c.t = 0;
+                        c.valid = true;
+                        return;
+                    }
+                }
+                c.valid = false;
+            };
+            auto advance = [&](Cursor &c) {
+                ++c.g;
+                c.slot = -1;
+                if (++c.t < c.n_tiles) return;
+                ++c.k;
+                c.item += gridDim.x;
+                ++c.j;
+                seek(c);
+            };
+            Cursor qc{(int)blockIdx.x, 0, 0, 0, 0, 0u, 0u, false, -1, 0u};
+            seek(qc);
+            Cursor pc = qc;
+            bool ok = true;
+            long long idle_since = clock64();
+            while (pc.valid) {
+                bool progressed = false;
+                // ---- PV of tile pc.g (its S was issued before)
+                if (pc.g < qc.g || !qc.valid) {
+                    const uint32_t sb = pc.g & 1;
+                    bool ready = mbar_test(&bars[C::B_PFULL + sb], (pc.g >> 1) & 1);
+                    if (ready && pc.t == 0)
+                        ready = mbar_test(&bars[C::B_OFREE + pc.k % OB], ((pc.k / OB) & 1) ^ 1);
+                    ready = ready && lookup(pc, 2 * pc.g + 1) &&
+                            mbar_test(&bars[C::B_FULL + pc.slot], pc.par);
+                    if (ready) {
+                        const uint32_t vslot = (uint32_t)pc.slot;
+                        fence_after_sync();
+                        // a partial tile: only the 16-key steps that hold valid keys
+                        // are multiplied; the V rows of the last step past the
+                        // chunk's end are zeroed first (P is 0 there, but the slot
+                        // may hold anything)
+                        const int nv = pc.t == pc.n_tiles - 1 ? pc.last_keys : kTcTileKeys;
+                        const int steps = (nv + 15) >> 4;
+                        uint8_t *vt = ring + vslot * C::TILE_BYTES;
+                        if (nv & 15) {
+                            const int row = nv + (lane >> 3), q = lane & 7;
+#pragma unroll
+                            for (int s = 0; s < SLABS; ++s) {
+#pragma unroll
+                                for (int r4 = 0; r4 < 16; r4 += 4) {
+                                    const int r = row + r4;
+                                    if (r < steps * 16)
+                                        reinterpret_cast<uint4 *>(vt + (r >> 3) * C::ATOM_BYTES +
+                                                                  s * 1024 + (r & 7) * 128)[q] =
+                                            make_uint4(0, 0, 0, 0);
+                                }
+                            }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                        }
+                        if (leader) {
+                            // B = V, MN-major: 64-dim blocks one slab (1024 B) apart,
+                            // 8-key groups one atom apart; a 16-key step is two atoms
+                            const uint64_t vbase = smem_desc_sw128(ring_a + vslot * C::TILE_BYTES,
+                                                                   1024, C::ATOM_BYTES);
+                            const uint32_t d_t = tmem + C::O_COL + (pc.k % OB) * D;
+                            const uint32_t p_t = tmem + sb * 128;  // P_hi; P_lo at +64
+                            const uint32_t acc0 = pc.t > 0 ? 1u : 0u;
+                            for (int k8 = 0; k8 < steps; ++k8)
+                                mma_bf16_ts(d_t, p_t + k8 * 8,
+                                            vbase + (uint64_t)(k8 * (2 * C::ATOM_BYTES >> 4)), ID_O,
+                                            (acc0 | (uint32_t)k8) != 0);
+                            for (int k8 = 0; k8 < steps; ++k8)
+                                mma_bf16_ts(d_t, p_t + 64 + k8 * 8,
+                                            vbase + (uint64_t)(k8 * (2 * C::ATOM_BYTES >> 4)), ID_O, 1u);
+                            mma_commit(&bars[C::B_EMPTY + vslot]);
+                            mma_commit(&bars[C::B_SFREE + sb]);
+                            mma_commit(&bars[C::B_PVDONE + sb]);
+                        }
+                        __syncwarp();
+                        advance(pc);
+                        progressed = true;
+                    }
+                }
+                // ---- S of tile qc.g, at most one tile ahead of the PV cursor
+                if (qc.valid && qc.g <= pc.g + 1) {
+                    const uint32_t sb = qc.g & 1;
+                    bool ready = mbar_test(&bars[C::B_SFREE + sb], ((qc.g >> 1) & 1) ^ 1) &&
+                                 mbar_test(&bars[C::B_QFULL + qc.k % QB], (qc.k / QB) & 1) &&
+                                 lookup(qc, 2 * qc.g) &&
+                                 mbar_test(&bars[C::B_FULL + qc.slot], qc.par);
+                    if (ready) {
+                        const uint32_t kslot = (uint32_t)qc.slot;
+                        fence_after_sync();
+                        if (leader) {
+                            // A = Q, K-major: 8-row groups 1024 B apart, slab s at
+                            // s * Q_SLAB; B = K, K-major: 8-key groups one atom apart,
+                            // slab s at s * 1024
+                            const uint64_t qbase =
+                                smem_desc_sw128(qs_a + (qc.k % QB) * C::Q_BUF, 16, 1024);
+                            const uint64_t kbase =
+                                smem_desc_sw128(ring_a + kslot * C::TILE_BYTES, 16, C::ATOM_BYTES);
+#pragma unroll
+                            for (int s = 0; s < SLABS; ++s) {
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    mma_bf16_ss(tmem + sb * 128,
+                                                qbase + (uint64_t)(s * (C::Q_SLAB >> 4) + kk * 2),
+                                                kbase + (uint64_t)(s * 64 + kk * 2), ID_S,
+                                                (s | kk) != 0);
+                            }
+                            mma_commit(&bars[C::B_EMPTY + kslot]);
+                            mma_commit(&bars[C::B_SFULL + sb]);
+                            if (qc.t == qc.n_tiles - 1)
+                                mma_commit(&bars[C::B_QEMPTY + qc.k % QB]);
+                        }
+                        __syncwarp();
+                        advance(qc);
+                        progressed = true;
+                    }
+                }
+                if (progressed) {
+                    idle_since = clock64();
+                } else if (clock64() - idle_since > kWaitLimitCycles) {
+                    atomicOr(P.fault, kFaultCopyTimeout);
+                    ok = false;
+                    break;
+                }
+            }
+            (void)ok;
+            // all issued MMAs complete before TMEM is released
+            if (leader) {
+                mma_commit(&bars[C::B_DRAIN]);
+                mbar_wait_bounded(&bars[C::B_DRAIN], 0, P.fault, kFaultCopyTimeout);
+            }
+            __syncwarp();
+        }
+    } else {
+        // ===================================================== softmax
+        const int quad = warp & 3;  // TMEM lane quadrant = packed rows 32 quad ..
+        if (quad < act_q) {
+            const int r = quad * 32 + lane;  // packed row within the row tile
+            const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
+            const float sc = P.qk_scale;
+            uint32_t g = 0, k = 0;
+            bool ok = true;
+            int j = 0;
+            for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
+                const TcItem it = tc_decode(T, item, j, meta);
+                const bool live = r < it.rows;
+                const int rg = it.row0 + r;  // packed row of the (sequence, KV head)
+                const int i = rg / P.G, gg = rg - i * P.G;
+                const size_t orow =
+                    ((size_t)it.b * P.q_len + i) * P.Hq + (size_t)it.h * P.G + gg;
+                const size_t prow =
+                    (((size_t)it.b * P.Hkv + it.h) * P.splits + it.split) * P.R + rg;
+                if (it.n_tiles == 0) {
+                    // no key in this chunk: empty result
+                    if (live) {
+                        if (P.splits == 1) {
+                            for (int d = 0; d < D; d += 8)
+                                *reinterpret_cast<uint4 *>(P.out + orow * D + d) =
+                                    make_uint4(0, 0, 0, 0);
+                            if (P.lse != nullptr) P.lse[orow] = NEG_INF;
+                        } else {
+                            for (int d = 0; d < D; d += 4)
+                                *reinterpret_cast<float4 *>(P.part_acc + prow * D + d) =
+                                    make_float4(0.f, 0.f, 0.f, 0.f);
+                            P.part_ml[prow * 2] = NEG_INF;
+                            P.part_ml[prow * 2 + 1] = 0.f;
+                        }
+                    }
+                    continue;
+                }
+                // keys of the chunk this row sees: [jlo, jhi]; draft row i sits at
+                // position q_pos + i and sees (p - W, p]
+                const long long pp = (long long)it.cr.qp + i;
+                long long jlo = pp - P.window + 1, jhi = pp;
+                if (jlo < it.cr.c_lo) jlo = it.cr.c_lo;
+                if (jhi > it.cr.c_hi - 1) jhi = it.cr.c_hi - 1;
+                if (!live) {
+                    jlo = 1;
+                    jhi = 0;
+                }
+                const uint32_t ob = k % OB;
+                float mref = kNoRef, lsum = 0.f;
+                for (int t = 0; t < it.n_tiles; ++t, ++g) {
+                    const uint32_t sb = g & 1;
+                    ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[C::B_SFULL + sb], (g >> 1) & 1,
+                                                                   P.fault, kFaultCopyTimeout));
+                    if (!ok) break;
+                    fence_after_sync();
+                    const long long j0 = (long long)it.cr.c_lo + (long long)kTcTileKeys * t;
+                    const long long ca_l = jlo - j0, cb_l = jhi - j0;
+                    const int ca = ca_l < 0 ? 0 : (ca_l > 128 ? 128 : (int)ca_l);
+                    const int cb = cb_l < -1 ? -1 : (cb_l > 127 ? 127 : (int)cb_l);
+                    // this row's 128 scores, masked to [ca, cb], scaled into log2 units
+                    uint32_t sraw[128];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        tmem_ld32(tl + sb * 128 + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sraw + 32 * c));
+                    tmem_wait_ld();
+                    float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+#pragma unroll
+                    for (int c = 0; c < 128; ++c) {
+                        const float x =
+                            (c >= ca && c <= cb) ? __uint_as_float(sraw[c]) * sc : NEG_INF;
+                        sraw[c] = __float_as_uint(x);
+                        m4[c & 3] = fmaxf(m4[c & 3], x);
+                    }
+                    const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    // raise the reference when a score exceeds it by 2^8 (always on
+                    // the row's first scores); O of the item's earlier tiles is then
+                    // rescaled in TMEM once their PVs have completed
+                    const bool raise = mt > mref + 8.f;
+                    if (__any_sync(0xffffffffu, raise && t > 0)) {
+                        const uint32_t gp = g - 1;
+                        ok = __all_sync(0xffffffffu,
+                                        mbar_wait_bounded(&bars[C::B_PVDONE + (gp & 1)], (gp >> 1) & 1,
+                                                          P.fault, kFaultCopyTimeout));
+                        if (!ok) break;
+                        fence_after_sync();
+                        const float al = raise ? fast_exp2(mref - mt) : 1.f;
+                        const uint32_t oc = tl + C::O_COL + ob * D;
+#pragma unroll 1
+                        for (int c0 = 0; c0 < D; c0 += 32) {
+                            uint32_t o[32];
+                            tmem_ld32(oc + c0, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                o[e] = __float_as_uint(__uint_as_float(o[e]) * al);
+                            tmem_st32(oc + c0, o);
+                        }
+                        tmem_wait_st();
+                    }
+                    if (raise) {
+                        lsum *= fast_exp2(mref - mt);
+                        mref = mt;
+                    }
+                    // P = 2^(s - m_ref) into the S buffer's TMEM columns: P_hi (bf16
+                    // truncation) in 0..63, P_lo (the rest, rounded) in 64..127,
+                    // two keys per column, the even key in the low half
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t phi[32], plo[32];
+#pragma unroll
+                        for (int c2 = 0; c2 < 32; ++c2) {
+                            const float p0 = fast_exp2(__uint_as_float(sraw[64 * h + 2 * c2]) - mref);
+                            const float p1 =
+                                fast_exp2(__uint_as_float(sraw[64 * h + 2 * c2 + 1]) - mref);
+                            lsum += p0 + p1;
+                            const uint32_t b0 = __float_as_uint(p0) & 0xffff0000u;
+                            const uint32_t b1 = __float_as_uint(p1) & 0xffff0000u;
+                            phi[c2] = (b0 >> 16) | b1;
+                            plo[c2] = pack_bf16x2(p0 - __uint_as_float(b0), p1 - __uint_as_float(b1));
+                        }
+                        tmem_st32(tl + sb * 128 + 32 * h, phi);
+                        tmem_st32(tl + sb * 128 + 64 + 32 * h, plo);
+                    }
+                    tmem_wait_st();
+                    fence_before_sync();
+                    mbar_arrive(&bars[C::B_PFULL + sb]);
+                }
+                if (!ok) break;
+
+                // ------------------------------------------------ end of item
+                const uint32_t gl = g - 1;  // the item's last tile
+                ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[C::B_PVDONE + (gl & 1)],
+                                                               (gl >> 1) & 1, P.fault,
+                                                               kFaultCopyTimeout));
+                if (!ok) break;
+                fence_after_sync();
+                const uint32_t oc = tl + C::O_COL + ob * D;
+                if (P.splits == 1) {
+                    const float inv = lsum > 0.f ? __frcp_rn(lsum) : 0.f;
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(oc + c0, o);
+                        tmem_wait_ld();
+                        if (live) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(P.out + orow * D + c0);
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4) {
+                                uint4 w;
+                                w.x = pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv,
+                                                  __uint_as_float(o[8 * q4 + 1]) * inv);
+                                w.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv,
+                                                  __uint_as_float(o[8 * q4 + 3]) * inv);
+                                w.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv,
+                                                  __uint_as_float(o[8 * q4 + 5]) * inv);
+                                w.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv,
+                                                  __uint_as_float(o[8 * q4 + 7]) * inv);
+                                dst[q4] = w;
+                            }
+                        }
+                    }
+                    if (live && P.lse != nullptr)
+                        P.lse[orow] = lsum > 0.f ? (mref + __log2f(lsum)) * kLn2 : NEG_INF;
+                } else {
+#pragma unroll 1
+                    for (int c0 = 0; c0 < D; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(oc + c0, o);
+                        tmem_wait_ld();
+                        if (live) {
+                            float4 *dst = reinterpret_cast<float4 *>(P.part_acc + prow * D + c0);
+#pragma unroll
+                            for (int q4 = 0; q4 < 8; ++q4)
+                                dst[q4] = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
+                                                      __uint_as_float(o[4 * q4 + 2]),
+                                                      __uint_as_float(o[4 * q4 + 3]));
+                        }
+                    }
+                    if (live) {
+                        P.part_ml[prow * 2] = lsum > 0.f ? mref : NEG_INF;
+                        P.part_ml[prow * 2 + 1] = lsum;
+                    }
+                }
+                fence_before_sync();
+                mbar_arrive(&bars[C::B_OFREE + ob]);  // O buffer may be reused
+                ++k;
+            }
+            (void)ok;
+        }
+    }
+
+    // ---------------------------------------------------------- teardown
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
+    if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+}  // namespace swa

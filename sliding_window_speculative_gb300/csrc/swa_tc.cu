@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <mutex>
 
+#include "swa_rows.cuh"
 #include "swa_tc.cuh"
 #include "swa_tc_host.h"
 
@@ -58,6 +59,42 @@ cudaError_t launch(const TcLaunch &L, const TcMaps &maps, cudaStream_t stream) {
         attr_done[dev] = true;
     }
     return launch_kernel(kern, dim3(L.grid), dim3(kTcThreads), C::SMEM_BYTES, stream, L.T, maps);
+}
+
+// Rows-major kernel: per (head_dim, Q rows) the ring tiles and Q buffers
+// that fit one CTA per SM.
+template <int D, int QR>
+struct RowsConf {
+    static constexpr int NT = D == 256 ? (QR == 128 ? 2 : 3) : (QR == 128 ? 6 : 6);
+    static constexpr int QB = D == 256 ? (QR == 32 ? 2 : 1) : (QR == 128 ? 1 : 2);
+    using C = RowsCfg<D, QR, NT, QB>;
+};
+
+template <int D, int QR>
+cudaError_t launch_rows(const TcLaunch &L, const TcMaps &maps, cudaStream_t stream) {
+    using Cf = RowsConf<D, QR>;
+    using C = typename Cf::C;
+    auto kern = swa_rows_kernel<D, QR, Cf::NT, Cf::QB>;
+    static bool attr_done[64] = {};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && !attr_done[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             C::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_done[dev] = true;
+    }
+    return launch_kernel(kern, dim3(L.grid), dim3(kRowsThreads), C::SMEM_BYTES, stream, L.T, maps);
+}
+
+template <int D>
+cudaError_t launch_rows_d(const TcLaunch &L, const TcMaps &maps, cudaStream_t s) {
+    switch (L.N) {
+        case 32: return launch_rows<D, 32>(L, maps, s);
+        case 64: return launch_rows<D, 64>(L, maps, s);
+        case 128: return launch_rows<D, 128>(L, maps, s);
+        default: return cudaErrorInvalidConfiguration;
+    }
 }
 
 template <int D>
@@ -149,6 +186,10 @@ cudaError_t tc_launch(const TcLaunch &L, cudaStream_t stream, char *err, size_t 
             snprintf(err, errlen, "cuTensorMapEncodeTiled(q) failed: %d", (int)r);
             return cudaErrorInvalidValue;
         }
+    }
+    if (L.rows_major) {
+        if (D == 256) return launch_rows_d<256>(L, maps, stream);
+        return launch_rows_d<128>(L, maps, stream);
     }
     if (D == 256) return launch_d<256>(L, maps, stream);
     return launch_d<128>(L, maps, stream);

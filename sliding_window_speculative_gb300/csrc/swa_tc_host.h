@@ -41,7 +41,8 @@ struct TcConfInfo {
 
 struct TcLaunch {
     TcParams T;
-    int D, N;   // head_dim, padded rows per item
+    int rows_major;  // 1: the kernel with packed rows as the MMA's M (swa_rows_kernel)
+    int D, N;   // head_dim, padded rows per item (rows kernel: 32, 64 or 128)
     int grid;   // persistent CTAs
     const void *k, *v, *q;
 };

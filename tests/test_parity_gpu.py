@@ -26,11 +26,12 @@ def _built():
     yield
 
 
-@pytest.fixture(params=["simt", "tc"])
+@pytest.fixture(params=["simt", "tc", "rows"])
 def kernel(request, monkeypatch):
-    """Runs the test once per kernel: the CUDA-core chunk kernel and the
-    tensor-core kernel (shapes the tensor-core kernel does not cover,
-    head_dim 64, fall back to the CUDA-core kernel)."""
+    """Runs the test once per kernel: the CUDA-core chunk kernel, the
+    key-major tensor-core kernel and the rows-major tensor-core kernel
+    (shapes the tensor-core kernels do not cover, head_dim 64, fall back to
+    the CUDA-core kernel)."""
     monkeypatch.setenv("SWA_FORCE_KERNEL", request.param)
     return request.param
 
