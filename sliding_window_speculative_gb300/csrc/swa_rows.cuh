@@ -8,12 +8,14 @@
 //   O[128 rows x D]       += P_hi . V_tile + P_lo . V_tile  (TMEM, fp32)
 //
 // The packed rows (G query heads of the KV head times the draft rows) are
-// the TMEM lanes, so a softmax thread owns one row: the row maximum, the
-// weights and the row sum stay inside the thread, and P goes back into the
-// TMEM columns of its S buffer (P_hi = bf16 truncation in columns 0..63,
-// P_lo = the rest rounded to bf16 in 64..127) as the A operand of the two
-// PV MMAs.  P never touches shared memory, and nothing is reduced across
-// threads.
+// the TMEM lanes.  Two softmax threads own a row, one per half of the tile's
+// keys (warps w and w + 4 share a TMEM lane quadrant): each keeps its half's
+// maximum and sum in registers, the pair swaps the half maxima through
+// shared memory once per tile so both use the same reference, and each
+// writes P for its keys back into the TMEM columns of the S buffer (P_hi =
+// bf16 truncation in columns 0..63, P_lo = the rest rounded to bf16 in
+// 64..127) as the A operand of the two PV MMAs.  P never touches shared
+// memory.
 //
 // Q sits in shared memory as [slab][QR rows][128 bytes] (QR = 32, 64 or
 // 128); an MMA reads 128 rows per slab, so with fewer rows it reads past the
@@ -22,11 +24,13 @@
 // ring slots, atoms of [slab][8 rows][128 B]); K is the B operand of the
 // score MMA (K-major), V the B operand of the PV MMAs (MN-major, N = D).
 //
-// Warp roles (192 threads):
+// Warp roles (320 threads):
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM owner and MMA issuer (one lane)
-//   warps 2..5  softmax / epilogue; warp w owns TMEM lanes 32 (w % 4)..,
-//               i.e. packed rows 32 (w % 4)..; warps without rows idle.
+//   warps 2..9  softmax / epilogue; warp w owns TMEM lanes 32 (w % 4)..,
+//               i.e. packed rows 32 (w % 4).., and key half (w - 2) / 4 of
+//               every tile (head-dim half of the output); quadrants without
+//               rows idle.
 //
 // TMEM: S/P buffers at columns 0 and 128, O at 256 (two O buffers at head
 // dim 128).  Every wait is bounded; a wait that gives up sets the fault
@@ -37,7 +41,7 @@
 
 namespace swa {
 
-constexpr int kRowsThreads = 192;
+constexpr int kRowsThreads = 320;
 
 template <int D, int QR, int NT, int QB>
 struct RowsCfg {
@@ -50,7 +54,11 @@ struct RowsCfg {
     static constexpr int RING_OFF = QB * Q_BUF;
     static constexpr int META_OFF = RING_OFF + NT * TILE_BYTES;  // TcItem [kTcMetaItems]
     static constexpr int FTAB_OFF = META_OFF + kTcMetaItems * (int)sizeof(TcItem);
-    static constexpr int BAR_OFF = FTAB_OFF + kFillTab * 4;
+    // the pairs' exchange: half maxima [tile parity][quadrant][half][lane],
+    // half row sums [quadrant][half][lane]
+    static constexpr int XM_OFF = FTAB_OFF + kFillTab * 4;
+    static constexpr int XL_OFF = XM_OFF + 2 * 4 * 2 * 32 * 4;
+    static constexpr int BAR_OFF = XL_OFF + 4 * 2 * 32 * 4;
     static constexpr int OB = D == 128 ? 2 : 1;      // O buffers in TMEM
     // ring full/empty [NT], q full/empty [QB], s full [2], s free [2],
     // p full [2], pv done [2], o free [OB], drain
@@ -118,10 +126,10 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[C::B_SFULL + i], 1);
             mbar_init(&bars[C::B_SFREE + i], 1);
-            mbar_init(&bars[C::B_PFULL + i], n_act);
+            mbar_init(&bars[C::B_PFULL + i], 2 * n_act);
             mbar_init(&bars[C::B_PVDONE + i], 1);
         }
-        for (int i = 0; i < OB; ++i) mbar_init(&bars[C::B_OFREE + i], n_act);
+        for (int i = 0; i < OB; ++i) mbar_init(&bars[C::B_OFREE + i], 2 * n_act);
         mbar_init(&bars[C::B_DRAIN], 1);
         fence_barrier_init();
     }
@@ -417,11 +425,20 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
         }
     } else {
         // ===================================================== softmax
-        const int quad = warp & 3;  // TMEM lane quadrant = packed rows 32 quad ..
+        const int quad = warp & 3;        // TMEM lane quadrant = packed rows 32 quad ..
+        const int half = (warp - 2) >> 2;  // key half of each tile, head-dim half of O
         if (quad < act_q) {
             const int r = quad * 32 + lane;  // packed row within the row tile
             const uint32_t tl = tmem + ((uint32_t)(quad * 32) << 16);
+            float *xm = reinterpret_cast<float *>(sm + C::XM_OFF);
+            float *xl = reinterpret_cast<float *>(sm + C::XL_OFF) + (quad * 2) * 32 + lane;
+            const int kh = 64 * half;  // first key of this thread's half
+            constexpr int DH = D / 2;  // head dims of this thread's half of O
             const float sc = P.qk_scale;
+            // the pair of warps of this quadrant (64 threads), barrier 1 + quad
+            auto pair_sync = [&]() {
+                asm volatile("bar.sync %0, 64;" ::"r"(1 + quad) : "memory");
+            };
             uint32_t g = 0, k = 0;
             bool ok = true;
             int j = 0;
@@ -435,19 +452,21 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                 const size_t prow =
                     (((size_t)it.b * P.Hkv + it.h) * P.splits + it.split) * P.R + rg;
                 if (it.n_tiles == 0) {
-                    // no key in this chunk: empty result
+                    // no key in this chunk: empty result (each half its dims)
                     if (live) {
                         if (P.splits == 1) {
-                            for (int d = 0; d < D; d += 8)
+                            for (int d = half * DH; d < (half + 1) * DH; d += 8)
                                 *reinterpret_cast<uint4 *>(P.out + orow * D + d) =
                                     make_uint4(0, 0, 0, 0);
-                            if (P.lse != nullptr) P.lse[orow] = NEG_INF;
+                            if (half == 0 && P.lse != nullptr) P.lse[orow] = NEG_INF;
                         } else {
-                            for (int d = 0; d < D; d += 4)
+                            for (int d = half * DH; d < (half + 1) * DH; d += 4)
                                 *reinterpret_cast<float4 *>(P.part_acc + prow * D + d) =
                                     make_float4(0.f, 0.f, 0.f, 0.f);
-                            P.part_ml[prow * 2] = NEG_INF;
-                            P.part_ml[prow * 2 + 1] = 0.f;
+                            if (half == 0) {
+                                P.part_ml[prow * 2] = NEG_INF;
+                                P.part_ml[prow * 2 + 1] = 0.f;
+                            }
                         }
                     }
                     continue;
@@ -470,28 +489,42 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                                                                    P.fault, kFaultCopyTimeout));
                     if (!ok) break;
                     fence_after_sync();
-                    const long long j0 = (long long)it.cr.c_lo + (long long)kTcTileKeys * t;
+                    // this thread's 64 scores (keys kh .. kh + 63 of the tile), masked
+                    // to the row's keys, in log2 units
+                    const long long j0 = (long long)it.cr.c_lo + (long long)kTcTileKeys * t + kh;
                     const long long ca_l = jlo - j0, cb_l = jhi - j0;
-                    const int ca = ca_l < 0 ? 0 : (ca_l > 128 ? 128 : (int)ca_l);
-                    const int cb = cb_l < -1 ? -1 : (cb_l > 127 ? 127 : (int)cb_l);
-                    // this row's 128 scores, masked to [ca, cb], scaled into log2 units
-                    uint32_t sraw[128];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        tmem_ld32(tl + sb * 128 + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(sraw + 32 * c));
+                    const int ca = ca_l < 0 ? 0 : (ca_l > 64 ? 64 : (int)ca_l);
+                    const int cb = cb_l < -1 ? -1 : (cb_l > 63 ? 63 : (int)cb_l);
+                    uint32_t sraw[64];
+                    tmem_ld32(tl + sb * 128 + kh, *reinterpret_cast<uint32_t(*)[32]>(sraw));
+                    tmem_ld32(tl + sb * 128 + kh + 32, *reinterpret_cast<uint32_t(*)[32]>(sraw + 32));
                     tmem_wait_ld();
                     float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
+                    if (ca == 0 && cb == 63) {
 #pragma unroll
-                    for (int c = 0; c < 128; ++c) {
-                        const float x =
-                            (c >= ca && c <= cb) ? __uint_as_float(sraw[c]) * sc : NEG_INF;
-                        sraw[c] = __float_as_uint(x);
-                        m4[c & 3] = fmaxf(m4[c & 3], x);
+                        for (int c = 0; c < 64; ++c) {
+                            const float x = __uint_as_float(sraw[c]) * sc;
+                            sraw[c] = __float_as_uint(x);
+                            m4[c & 3] = fmaxf(m4[c & 3], x);
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 64; ++c) {
+                            const float x =
+                                (c >= ca && c <= cb) ? __uint_as_float(sraw[c]) * sc : NEG_INF;
+                            sraw[c] = __float_as_uint(x);
+                            m4[c & 3] = fmaxf(m4[c & 3], x);
+                        }
                     }
-                    const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    // the pair's common tile maximum (one exchange per tile, buffers
+                    // alternate with the tile so a slow partner is never overwritten)
+                    float *xmt = xm + ((sb * 4 + quad) * 2) * 32 + lane;
+                    xmt[half * 32] = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+                    pair_sync();
+                    const float mt = fmaxf(xmt[0], xmt[32]);
                     // raise the reference when a score exceeds it by 2^8 (always on
                     // the row's first scores); O of the item's earlier tiles is then
-                    // rescaled in TMEM once their PVs have completed
+                    // rescaled in TMEM (each half its head dims) once their PVs are done
                     const bool raise = mt > mref + 8.f;
                     if (__any_sync(0xffffffffu, raise && t > 0)) {
                         const uint32_t gp = g - 1;
@@ -501,9 +534,9 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                         if (!ok) break;
                         fence_after_sync();
                         const float al = raise ? fast_exp2(mref - mt) : 1.f;
-                        const uint32_t oc = tl + C::O_COL + ob * D;
+                        const uint32_t oc = tl + C::O_COL + ob * D + half * DH;
 #pragma unroll 1
-                        for (int c0 = 0; c0 < D; c0 += 32) {
+                        for (int c0 = 0; c0 < DH; c0 += 32) {
                             uint32_t o[32];
                             tmem_ld32(oc + c0, o);
                             tmem_wait_ld();
@@ -518,25 +551,26 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                         lsum *= fast_exp2(mref - mt);
                         mref = mt;
                     }
-                    // P = 2^(s - m_ref) into the S buffer's TMEM columns: P_hi (bf16
-                    // truncation) in 0..63, P_lo (the rest, rounded) in 64..127,
-                    // two keys per column, the even key in the low half
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
+                    // P = 2^(s - m_ref) for this half's keys into the S buffer's TMEM
+                    // columns: P_hi (bf16 truncation) in 0..63, P_lo (the rest,
+                    // rounded) in 64..127, two keys per column, even key low
+                    {
                         uint32_t phi[32], plo[32];
+                        float ls0 = 0.f, ls1 = 0.f;
 #pragma unroll
                         for (int c2 = 0; c2 < 32; ++c2) {
-                            const float p0 = fast_exp2(__uint_as_float(sraw[64 * h + 2 * c2]) - mref);
-                            const float p1 =
-                                fast_exp2(__uint_as_float(sraw[64 * h + 2 * c2 + 1]) - mref);
-                            lsum += p0 + p1;
-                            const uint32_t b0 = __float_as_uint(p0) & 0xffff0000u;
-                            const uint32_t b1 = __float_as_uint(p1) & 0xffff0000u;
-                            phi[c2] = (b0 >> 16) | b1;
-                            plo[c2] = pack_bf16x2(p0 - __uint_as_float(b0), p1 - __uint_as_float(b1));
+                            const float p0 = fast_exp2(__uint_as_float(sraw[2 * c2]) - mref);
+                            const float p1 = fast_exp2(__uint_as_float(sraw[2 * c2 + 1]) - mref);
+                            ls0 += p0;
+                            ls1 += p1;
+                            const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+                            phi[c2] = __byte_perm(u0, u1, 0x7632);
+                            plo[c2] = pack_bf16x2(p0 - __uint_as_float(u0 & 0xffff0000u),
+                                                  p1 - __uint_as_float(u1 & 0xffff0000u));
                         }
-                        tmem_st32(tl + sb * 128 + 32 * h, phi);
-                        tmem_st32(tl + sb * 128 + 64 + 32 * h, plo);
+                        lsum += ls0 + ls1;
+                        tmem_st32(tl + sb * 128 + (kh >> 1), phi);
+                        tmem_st32(tl + sb * 128 + 64 + (kh >> 1), plo);
                     }
                     tmem_wait_st();
                     fence_before_sync();
@@ -545,22 +579,26 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                 if (!ok) break;
 
                 // ------------------------------------------------ end of item
+                // the row's sum: this half's plus the partner's
+                xl[half * 32] = lsum;
+                pair_sync();
+                const float ltot = xl[0] + xl[32];
                 const uint32_t gl = g - 1;  // the item's last tile
                 ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[C::B_PVDONE + (gl & 1)],
                                                                (gl >> 1) & 1, P.fault,
                                                                kFaultCopyTimeout));
                 if (!ok) break;
                 fence_after_sync();
-                const uint32_t oc = tl + C::O_COL + ob * D;
+                const uint32_t oc = tl + C::O_COL + ob * D + half * DH;
                 if (P.splits == 1) {
-                    const float inv = lsum > 0.f ? __frcp_rn(lsum) : 0.f;
+                    const float inv = ltot > 0.f ? __frcp_rn(ltot) : 0.f;
 #pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
+                    for (int c0 = 0; c0 < DH; c0 += 32) {
                         uint32_t o[32];
                         tmem_ld32(oc + c0, o);
                         tmem_wait_ld();
                         if (live) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(P.out + orow * D + c0);
+                            uint4 *dst = reinterpret_cast<uint4 *>(P.out + orow * D + half * DH + c0);
 #pragma unroll
                             for (int q4 = 0; q4 < 4; ++q4) {
                                 uint4 w;
@@ -576,16 +614,17 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                             }
                         }
                     }
-                    if (live && P.lse != nullptr)
-                        P.lse[orow] = lsum > 0.f ? (mref + __log2f(lsum)) * kLn2 : NEG_INF;
+                    if (live && half == 0 && P.lse != nullptr)
+                        P.lse[orow] = ltot > 0.f ? (mref + __log2f(ltot)) * kLn2 : NEG_INF;
                 } else {
 #pragma unroll 1
-                    for (int c0 = 0; c0 < D; c0 += 32) {
+                    for (int c0 = 0; c0 < DH; c0 += 32) {
                         uint32_t o[32];
                         tmem_ld32(oc + c0, o);
                         tmem_wait_ld();
                         if (live) {
-                            float4 *dst = reinterpret_cast<float4 *>(P.part_acc + prow * D + c0);
+                            float4 *dst =
+                                reinterpret_cast<float4 *>(P.part_acc + prow * D + half * DH + c0);
 #pragma unroll
                             for (int q4 = 0; q4 < 8; ++q4)
                                 dst[q4] = make_float4(__uint_as_float(o[4 * q4]), __uint_as_float(o[4 * q4 + 1]),
@@ -593,9 +632,9 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                                                       __uint_as_float(o[4 * q4 + 3]));
                         }
                     }
-                    if (live) {
-                        P.part_ml[prow * 2] = lsum > 0.f ? mref : NEG_INF;
-                        P.part_ml[prow * 2 + 1] = lsum;
+                    if (live && half == 0) {
+                        P.part_ml[prow * 2] = ltot > 0.f ? mref : NEG_INF;
+                        P.part_ml[prow * 2 + 1] = ltot;
                     }
                 }
                 fence_before_sync();

@@ -65,8 +65,8 @@ cudaError_t launch(const TcLaunch &L, const TcMaps &maps, cudaStream_t stream) {
 // that fit one CTA per SM.
 template <int D, int QR>
 struct RowsConf {
-    static constexpr int NT = D == 256 ? (QR == 128 ? 2 : 3) : (QR == 128 ? 6 : 6);
-    static constexpr int QB = D == 256 ? (QR == 32 ? 2 : 1) : (QR == 128 ? 1 : 2);
+    static constexpr int NT = D == 256 ? (QR == 32 ? 3 : 2) : (QR == 128 ? 5 : 6);
+    static constexpr int QB = D == 256 ? (QR == 64 ? 2 : 1) : (QR == 32 ? 2 : 1);
     using C = RowsCfg<D, QR, NT, QB>;
 };
 
