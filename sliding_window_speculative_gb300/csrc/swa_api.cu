@@ -97,6 +97,8 @@ int forced_kernel() {
 
 // Split heuristic.  Host-only: seq_lens live on the device, so the
 // worst-case span W + q_len - 1 (bounded by the cache length) is used.
+//  - Rows-major tensor-core kernel for more than 32 packed rows, up to 128
+//    rows per item; same chunking as below.
 //  - Tensor-core path (head_dim 128/256; >= 16 packed rows, or a batch whose
 //    (sequence, KV head) units cover half the SMs): one chunk per (sequence,
 //    KV head, row tile) once those units cover half the SMs or the span is at
@@ -128,7 +130,11 @@ Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
     const bool big_batch = (long long)d->batch * d->num_kv_heads * 2 >= num_sms;
     const bool use_tc = tc_shape && (force == 2 || (force == 0 && (R >= 16 || big_batch)));
     int splits;
-    const bool use_rows = tc_shape && force == 3;
+    // More than 32 packed rows (q_len > 8 at 4:1 GQA) go to the rows-major
+    // kernel: its softmax keeps a row in one thread pair and P in TMEM, and
+    // an item holds up to 128 rows, so K/V are re-read less often; up to 32
+    // rows the key-major kernel's eight warps share the work better.
+    const bool use_rows = tc_shape && (force == 3 || (force == 0 && R > 32));
     if (use_rows) {
         // rows-major kernel: up to 128 packed rows per item (the MMA's M)
         p.kernel = 3;

@@ -58,7 +58,11 @@ struct RowsCfg {
     // half row sums [quadrant][half][lane]
     static constexpr int XM_OFF = FTAB_OFF + kFillTab * 4;
     static constexpr int XL_OFF = XM_OFF + 2 * 4 * 2 * 32 * 4;
-    static constexpr int BAR_OFF = XL_OFF + 4 * 2 * 32 * 4;
+    static constexpr int STG_OFF = XL_OFF + 4 * 2 * 32 * 4;
+    // output staging, 2 KB per softmax warp (32 rows x 64 bytes), where it fits
+    static constexpr int STG_NEED = 8 * 2048;
+    static constexpr bool STAGE = STG_OFF + STG_NEED + 1024 + 512 <= 227 * 1024;
+    static constexpr int BAR_OFF = STG_OFF + (STAGE ? STG_NEED : 0);
     static constexpr int OB = D == 128 ? 2 : 1;      // O buffers in TMEM
     // ring full/empty [NT], q full/empty [QB], s full [2], s free [2],
     // p full [2], pv done [2], o free [OB], drain
@@ -590,7 +594,56 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                 if (!ok) break;
                 fence_after_sync();
                 const uint32_t oc = tl + C::O_COL + ob * D + half * DH;
-                if (P.splits == 1) {
+                if (P.splits == 1 && C::STAGE) {
+                    // 32 dims of the warp's 32 rows at a time through a 2 KB staging
+                    // buffer ([row][4 x 16 B], chunk index XOR (row >> 1) & 3 against
+                    // bank conflicts), then stored as 8 rows x 64 B per instruction
+                    const float inv = ltot > 0.f ? __frcp_rn(ltot) : 0.f;
+                    uint8_t *stg = sm + C::STG_OFF + (warp - 2) * 2048;
+                    const int wr = lane >> 2, wc = lane & 3;  // write-back row (+ 8 s), chunk
+                    size_t wrow[4];
+                    bool wlive[4];
+#pragma unroll
+                    for (int s2 = 0; s2 < 4; ++s2) {
+                        const int rr = quad * 32 + wr + 8 * s2;
+                        const int rg2 = it.row0 + rr;
+                        const int i2 = rg2 / P.G, gg2 = rg2 - i2 * P.G;
+                        wlive[s2] = rr < it.rows;
+                        wrow[s2] = (((size_t)it.b * P.q_len + i2) * P.Hq + (size_t)it.h * P.G + gg2) * D;
+                    }
+#pragma unroll 1
+                    for (int c0 = 0; c0 < DH; c0 += 32) {
+                        uint32_t o[32];
+                        tmem_ld32(oc + c0, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            uint4 w;
+                            w.x = pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv,
+                                              __uint_as_float(o[8 * q4 + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv,
+                                              __uint_as_float(o[8 * q4 + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv,
+                                              __uint_as_float(o[8 * q4 + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv,
+                                              __uint_as_float(o[8 * q4 + 7]) * inv);
+                            *reinterpret_cast<uint4 *>(stg + lane * 64 +
+                                                       ((q4 ^ ((lane >> 1) & 3)) << 4)) = w;
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int s2 = 0; s2 < 4; ++s2) {
+                            const int rr = wr + 8 * s2;
+                            const uint4 w = *reinterpret_cast<const uint4 *>(
+                                stg + rr * 64 + ((wc ^ ((rr >> 1) & 3)) << 4));
+                            if (wlive[s2])
+                                *reinterpret_cast<uint4 *>(P.out + wrow[s2] + half * DH + c0 + wc * 8) = w;
+                        }
+                        __syncwarp();
+                    }
+                    if (live && half == 0 && P.lse != nullptr)
+                        P.lse[orow] = ltot > 0.f ? (mref + __log2f(ltot)) * kLn2 : NEG_INF;
+                } else if (P.splits == 1) {
                     const float inv = ltot > 0.f ? __frcp_rn(ltot) : 0.f;
 #pragma unroll 1
                     for (int c0 = 0; c0 < DH; c0 += 32) {

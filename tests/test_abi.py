@@ -111,8 +111,9 @@ def test_plan_invariants(lib, B, q_len, Hq, Hkv, D, L, W, sms):
     if p["kernel"] == 1:
         assert p["grid_ctas"] == units
     else:                                   # persistent grid over the work items
-        assert p["kernel"] == 2 and 1 <= p["grid_ctas"] <= min(units, sms)
-        assert p["rows_per_tile"] <= 64
+        assert p["kernel"] in (2, 3) and 1 <= p["grid_ctas"] <= min(units, sms)
+        assert p["kernel"] == (3 if R > 32 else 2)   # rows-major above 32 packed rows
+        assert p["rows_per_tile"] <= (128 if p["kernel"] == 3 else 64)
         assert p["rows_per_tile"] % (Hq // Hkv) == 0
     assert p["merge"] == (1 if p["num_splits"] > 1 else 0)
     assert p["workspace_bytes"] <= swa.swa_workspace_bytes(dims, W)
@@ -132,7 +133,9 @@ def test_plan_kernel_choice(lib, monkeypatch):
     d64 = swa.make_dims(1, 8, 2, 1, 64, 40)
     assert swa.swa_plan(d64, 16, 152)["kernel"] == 1            # head_dim 64: CUDA cores
     q64 = swa.swa_plan(swa.make_dims(512, 64, 8, 2, 256, 32768), 1024, 152)
-    assert q64["kernel"] == 2 and q64["row_tiles"] == 4 and q64["rows_per_tile"] == 64
+    assert q64["kernel"] == 3 and q64["row_tiles"] == 2 and q64["rows_per_tile"] == 128
+    q16 = swa.swa_plan(swa.make_dims(64, 16, 8, 2, 256, 4096), 188, 152)
+    assert q16["kernel"] == 3 and q16["row_tiles"] == 1 and q16["rows_per_tile"] == 64
     monkeypatch.setenv("SWA_FORCE_KERNEL", "simt")
     assert swa.swa_plan(q8, 188, 152)["kernel"] == 1
     monkeypatch.setenv("SWA_FORCE_KERNEL", "tc")
