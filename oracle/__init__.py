@@ -39,6 +39,8 @@ def _bind(path):
     lib.oracle_swa_partial.restype = ctypes.c_int
     lib.oracle_lse_merge.argtypes = [dp, dp, dp, i64, i64, i64, dp, dp]
     lib.oracle_lse_merge.restype = ctypes.c_int
+    lib.oracle_greedy_accept.argtypes = [dp, ip, ip, i64, i64, i64, ip, ip]
+    lib.oracle_greedy_accept.restype = ctypes.c_int
     return lib
 
 
@@ -142,3 +144,26 @@ def lse_merge(m, l, acc):
     rc = _load().oracle_lse_merge(_dp(m), _dp(l), _dp(acc), n, rows, D, _dp(out), _dp(lse))
     _check(rc, "lse_merge")
     return out, lse
+
+
+def greedy_accept(logits, draft, keep=None):
+    """Greedy verification of draft blocks.
+
+    logits [B, q_len, V] (any real dtype, widened to float64), draft
+    [B, q_len - 1] token ids, keep [V] token ids of the logits' columns or
+    None.  Returns (argmax [B, q_len], accepted [B]) as int64: the first
+    column of the largest logit per row (mapped through keep), and the length
+    of the longest prefix of rows whose argmax equals the drafted token.
+    """
+    logits = _f64(logits)
+    B, q_len, V = logits.shape
+    draft = _i64(np.asarray(draft).reshape(B, max(q_len - 1, 0)))
+    keep_a = None if keep is None else _i64(keep)
+    if keep_a is not None and keep_a.shape != (V,):
+        raise ValueError("keep must have one token id per logit column")
+    argmax = np.zeros((B, q_len), dtype=np.int64)
+    accepted = np.zeros(B, dtype=np.int64)
+    rc = _load().oracle_greedy_accept(_dp(logits), _ip(keep_a) if keep_a is not None else None,
+                                      _ip(draft), B, q_len, V, _ip(argmax), _ip(accepted))
+    _check(rc, "greedy_accept")
+    return argmax, accepted

@@ -247,3 +247,40 @@ int oracle_lse_merge(const double *m, const double *l, const double *acc,
     }
     return 0;
 }
+
+/* Greedy verification of a draft block, after the manifest entries
+ * FUSED_SPARSE_ARGMAX (argmax sampling over the LM head's logits, possibly a
+ * pruned keep set of the vocabulary) and SPECULATIVE_CONFIG (seven drafted
+ * tokens per step) of "The Fast Gemma Challenge: our verified-SOTA recipe, in
+ * full".  Per sequence b and verify row i (the row at position q_pos + i
+ * scores the token that follows it):
+ *   argmax[b][i] = keep[j*], j* = the first column j of logits[b][i] whose
+ *                  value is the largest (a NaN is never larger; a row with
+ *                  no value above -inf gives j* = 0); keep == NULL: j*;
+ *   accepted[b]  = the largest n <= q_len - 1 with argmax[b][i] == draft[b][i]
+ *                  for every i < n (draft[b][i] is the token fed as row i + 1).
+ * Layouts: logits [B, q_len, V]; keep [V] or NULL; draft [B, q_len - 1];
+ * argmax [B, q_len]; accepted [B]. */
+int oracle_greedy_accept(const double *logits, const int64_t *keep, const int64_t *draft,
+                         int64_t B, int64_t q_len, int64_t V, int64_t *argmax,
+                         int64_t *accepted)
+{
+    if (B < 0 || q_len < 1 || V < 1) return 1;
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t i = 0; i < q_len; ++i) {
+            const double *row = logits + (b * q_len + i) * V;
+            double best = -INFINITY;
+            int64_t jbest = 0;
+            for (int64_t j = 0; j < V; ++j)
+                if (row[j] > best) {
+                    best = row[j];
+                    jbest = j;
+                }
+            argmax[b * q_len + i] = keep ? keep[jbest] : jbest;
+        }
+        int64_t n = 0;
+        while (n < q_len - 1 && argmax[b * q_len + n] == draft[b * (q_len - 1) + n]) ++n;
+        accepted[b] = n;
+    }
+    return 0;
+}

@@ -28,6 +28,11 @@ MUTATIONS = {
     "merge_sign": ("const double w = exp(mk - M);", "const double w = exp(M - mk);"),
     # q and k dims transposed in the score (reads k at the wrong stride)
     "score_operand": ("dot += qr[d] * kr[d];", "dot += qr[d] * kr[(d * 7) % D];"),
+    # argmax ties go to the last column instead of the first
+    "argmax_last_tie": ("if (row[j] > best) {", "if (row[j] >= best) {"),
+    # the acceptance compares a draft with the next row's token
+    "accept_wrong_row": ("while (n < q_len - 1 && argmax[b * q_len + n] == draft[b * (q_len - 1) + n]) ++n;",
+                         "while (n < q_len - 1 && argmax[b * q_len + n + 1] == draft[b * (q_len - 1) + n]) ++n;"),
 }
 
 PIN_CHECKS = [
@@ -37,6 +42,8 @@ PIN_CHECKS = [
     lambda: pins.test_full_window_is_causal_attention(64, 2, 1, 40, 8),
     lambda: [pins.test_split_merge_identity(n) for n in (2, 3)],
     lambda: pins.test_zero_keys_closed_form(),
+    lambda: [pins.test_accept_hand_worked_examples(c) for c in pins._load_accept_golden()],
+    lambda: pins.test_accept_matches_numpy_argmax_and_prefix_count(),
 ]
 
 

@@ -290,3 +290,51 @@ def test_threads_do_not_change_result():
     b = oracle_case(case, threads=5)
     np.testing.assert_array_equal(a[0], b[0])
     np.testing.assert_array_equal(a[1], b[1])
+
+
+# ------------------------------------------------- greedy verification (accept)
+
+def _load_accept_golden():
+    path = os.path.join(os.path.dirname(__file__), "golden", "accept_cases.json")
+    with open(path) as f:
+        return json.load(f)["cases"]
+
+
+def _num(x):
+    return float(x) if not isinstance(x, str) else {"nan": np.nan, "-inf": -np.inf,
+                                                     "inf": np.inf}[x]
+
+
+@pytest.mark.parametrize("case", _load_accept_golden(), ids=lambda c: c["name"])
+def test_accept_hand_worked_examples(case):
+    logits = np.array([[[_num(x) for x in row] for row in seq] for seq in case["logits"]])
+    B, q_len, _ = logits.shape
+    draft = np.array(case["draft"], dtype=np.int64).reshape(B, q_len - 1)
+    am, acc = oracle.greedy_accept(logits, draft, case["keep"])
+    assert am.tolist() == case["argmax"], case["derivation"]
+    assert acc.tolist() == case["accepted"], case["derivation"]
+
+
+def test_accept_matches_numpy_argmax_and_prefix_count():
+    # NaN-free rows reduce to numpy's argmax (first maximum) and a plain
+    # prefix count; ties are forced by drawing small integers
+    rng = np.random.default_rng(7)
+    for B, q_len, V in [(3, 8, 50), (2, 1, 7), (1, 64, 300), (4, 5, 1)]:
+        logits = rng.integers(-3, 4, size=(B, q_len, V)).astype(np.float64)
+        ref_am = np.argmax(logits, axis=2)
+        for k in range(q_len):
+            draft = np.where(np.arange(q_len - 1)[None, :] < k, ref_am[:, :-1],
+                             ref_am[:, :-1] + 1 if V > 1 else ref_am[:, :-1] - 1)
+            am, acc = oracle.greedy_accept(logits, draft)
+            assert np.array_equal(am, ref_am)
+            assert np.all(acc == min(k, q_len - 1))
+
+
+def test_accept_keep_set_is_a_relabelling():
+    rng = np.random.default_rng(8)
+    logits = rng.standard_normal((2, 8, 40))
+    keep = rng.permutation(1000)[:40]
+    am0, _ = oracle.greedy_accept(logits, np.zeros((2, 7), dtype=np.int64))
+    am1, acc1 = oracle.greedy_accept(logits, keep[am0[:, :-1]], keep)
+    assert np.array_equal(am1, keep[am0])
+    assert np.all(acc1 == 7)                 # drafts taken from the argmax: all accepted
