@@ -146,6 +146,39 @@ swa_status swa_read_device_errors(uint32_t *flags);
 const char *swa_version(void);
 
 /* Bytes of the fixed device scratch used by swa_verify_attn_noalloc. */
+/* Greedy verification of a draft block: the argmax of every verify row's
+ * logits (FUSED_SPARSE_ARGMAX, with the keep set of a pruned LM head) and
+ * the number of drafted tokens accepted (SPECULATIVE_CONFIG's drafts), in
+ * one launch ("The Fast Gemma Challenge: our verified-SOTA recipe, in full",
+ * manifest entries FUSED_SPARSE_ARGMAX / FUSED_SPARSE_ARGMAX_BLOCK and
+ * SPECULATIVE_CONFIG; section "What each piece does, and why": the fused
+ * sparse argmax removes sampling overhead).
+ *
+ *   logits     bf16 [batch, q_len, vocab]  device, 2-byte aligned; row i of a
+ *              sequence scores the token after its position q_pos + i
+ *   keep_ids   int32 [vocab]  device or NULL: column j scores token keep_ids[j]
+ *              (NULL: token j)
+ *   draft      int32 [batch, q_len - 1]  device (may be NULL when q_len == 1):
+ *              the drafted tokens that were fed as rows 1 .. q_len - 1
+ *   argmax_out int32 [batch, q_len]  device, written: per row the token of the
+ *              largest logit; among equal maxima the first column; a NaN is
+ *              never the largest; a row with nothing above -inf gives column 0
+ *   accepted   int32 [batch]  device, written: n = the largest n <= q_len - 1
+ *              with argmax_out[b][i] == draft[b][i] for every i < n; the step
+ *              emits draft[b][0 .. n) and then argmax_out[b][n]
+ *   batch 1..65535, q_len 1..64, vocab >= 1.
+ *
+ * Asynchronous on `stream`; returns SWA_ERR_INVALID_ARG on bad arguments
+ * before any CUDA call.  The library keeps a small per-device scratch
+ * (8 bytes per row and 4 per sequence, zero between calls): the first call
+ * with a larger batch * q_len allocates and zeroes it, which is refused
+ * with SWA_ERR_WORKSPACE while the stream is capturing (make one call of
+ * the largest size before capture).  Calls that overlap on one device race
+ * on that scratch; order them (one stream, or events). */
+swa_status swa_greedy_accept(const void *logits, const int32_t *keep_ids, const int32_t *draft,
+                             int32_t *argmax_out, int32_t *accepted, int32_t batch,
+                             int32_t q_len, int32_t vocab, swa_stream_t stream);
+
 #define SWA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 
 /* Allocation-free variant of swa_verify_attn (no counterpart on the pages:

@@ -74,6 +74,8 @@ def load_library(path=LIB_PATH):
     lib.swa_version.restype = ctypes.c_char_p
     lib.swa_verify_attn_noalloc.argtypes = lib.swa_verify_attn.argtypes
     lib.swa_verify_attn_noalloc.restype = ctypes.c_int
+    lib.swa_greedy_accept.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp]
+    lib.swa_greedy_accept.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -165,6 +167,43 @@ def swa_verify_attn_noalloc(q, k_cache, v_cache, seq_lens, q_pos, window, scale,
     return swa_verify_attn(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out=out,
                            lse=lse, num_splits=num_splits, stream=stream, want_lse=False,
                            _entry="swa_verify_attn_noalloc")
+
+
+def swa_greedy_accept(logits, draft=None, keep_ids=None, argmax=None, accepted=None,
+                      stream=None):
+    """Greedy verification through the C entry point swa_greedy_accept.
+
+    logits bf16 [B, q_len, V]; draft int32 [B, q_len - 1] (None when
+    q_len == 1); keep_ids int32 [V] or None.  Returns (argmax int32
+    [B, q_len], accepted int32 [B]), allocated if not given.  Enqueued on
+    `stream` (default: torch's current stream); does not synchronise.
+    """
+    lib = load_library()
+    pl = _dev_tensor(logits, "logits", torch.bfloat16, 3)
+    B, q_len, V = logits.shape
+    pd = None
+    if q_len > 1 or draft is not None:
+        pd = _dev_tensor(draft, "draft", torch.int32, 2)
+        if tuple(draft.shape) != (B, q_len - 1):
+            raise ValueError("draft must be [B, q_len - 1]")
+    pk = None
+    if keep_ids is not None:
+        pk = _dev_tensor(keep_ids, "keep_ids", torch.int32, 1)
+        if keep_ids.numel() != V:
+            raise ValueError("keep_ids needs one token id per logit column")
+    if argmax is None:
+        argmax = torch.empty((B, q_len), dtype=torch.int32, device=logits.device)
+    if accepted is None:
+        accepted = torch.empty((B,), dtype=torch.int32, device=logits.device)
+    pa = _dev_tensor(argmax, "argmax", torch.int32, 2)
+    pc = _dev_tensor(accepted, "accepted", torch.int32, 1)
+    if tuple(argmax.shape) != (B, q_len) or accepted.numel() != B:
+        raise ValueError("argmax must be [B, q_len] and accepted [B]")
+    if stream is None:
+        stream = torch.cuda.current_stream(logits.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _check(lib.swa_greedy_accept(pl, pk, pd, pa, pc, B, q_len, V, handle))
+    return argmax, accepted
 
 
 def swa_workspace_bytes(dims, window):

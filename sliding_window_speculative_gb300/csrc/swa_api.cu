@@ -12,6 +12,7 @@
 
 #include "../../include/swa.h"
 #include "swa_simt.cuh"
+#include "swa_accept.cuh"
 #include "swa_tc_host.h"
 
 // Fault word of each device that loads the library; kernels receive its
@@ -508,6 +509,112 @@ swa_status swa_read_device_errors(uint32_t *flags) {
 }
 
 const char *swa_version(void) { return "swa 0.1.0 sm_103a"; }
+
+}  // extern "C"
+
+// ------------------------------------------------ greedy verification
+
+namespace {
+
+struct AcceptScratch {
+    void *ptr = nullptr;
+    size_t rows = 0, seqs = 0;  // capacity: best slots, arrival counters
+};
+std::mutex g_acc_mutex;
+AcceptScratch g_acc[kMaxDevices];
+
+// Zero-filled scratch of >= rows 64-bit slots and >= seqs counters; every
+// call leaves it zero again.  Grown (and zeroed on `stream`) outside stream
+// capture only.
+swa_status ensure_accept_scratch(int dev, size_t rows, size_t seqs, cudaStream_t stream,
+                                 unsigned long long **best, uint32_t **done) {
+    std::lock_guard<std::mutex> lock(g_acc_mutex);
+    AcceptScratch &a = g_acc[dev];
+    if (a.rows < rows || a.seqs < seqs) {
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+        if (cap != cudaStreamCaptureStatusNone)
+            return fail(SWA_ERR_WORKSPACE,
+                        "stream is capturing and the acceptance scratch (%zu rows, %zu sequences) "
+                        "is below the %zu rows, %zu sequences needed; run one call outside capture "
+                        "first", a.rows, a.seqs, rows, seqs);
+        if (a.ptr) {
+            e = cudaFree(a.ptr);
+            a.ptr = nullptr;
+            a.rows = a.seqs = 0;
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFree(acceptance scratch)");
+        }
+        const size_t nr = rows + rows / 4, ns = seqs + seqs / 4;
+        const size_t bytes = nr * 8 + ns * 4;
+        e = cudaMalloc(&a.ptr, bytes);
+        if (e != cudaSuccess) {
+            a.ptr = nullptr;
+            return cuda_fail(e, "cudaMalloc(acceptance scratch)");
+        }
+        e = cudaMemsetAsync(a.ptr, 0, bytes, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(acceptance scratch)");
+        a.rows = nr;
+        a.seqs = ns;
+    }
+    *best = static_cast<unsigned long long *>(a.ptr);
+    *done = reinterpret_cast<uint32_t *>(static_cast<unsigned long long *>(a.ptr) + a.rows);
+    return SWA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+swa_status swa_greedy_accept(const void *logits, const int32_t *keep_ids, const int32_t *draft,
+                             int32_t *argmax_out, int32_t *accepted, int32_t batch,
+                             int32_t q_len, int32_t vocab, swa_stream_t stream) {
+    if (batch < 1 || batch > 65535)
+        return fail(SWA_ERR_INVALID_ARG, "batch %d outside [1, 65535]", batch);
+    if (q_len < 1 || q_len > kMaxQLen)
+        return fail(SWA_ERR_INVALID_ARG, "q_len %d outside [1, %d]", q_len, kMaxQLen);
+    if (vocab < 1) return fail(SWA_ERR_INVALID_ARG, "vocab %d < 1", vocab);
+    if (!logits || !argmax_out || !accepted || (q_len > 1 && !draft))
+        return fail(SWA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if ((reinterpret_cast<uintptr_t>(logits) & 1u) || (reinterpret_cast<uintptr_t>(argmax_out) & 3u) ||
+        (reinterpret_cast<uintptr_t>(accepted) & 3u) || (reinterpret_cast<uintptr_t>(draft) & 3u) ||
+        (reinterpret_cast<uintptr_t>(keep_ids) & 3u))
+        return fail(SWA_ERR_INVALID_ARG, "logits must be 2-byte and the int32 arrays 4-byte aligned");
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev >= kMaxDevices) return fail(SWA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    swa::AcceptParams A{};
+    swa_status st = ensure_accept_scratch(dev, (size_t)batch * q_len, (size_t)batch, s, &A.best,
+                                          &A.done);
+    if (st != SWA_OK) return st;
+    // about two CTAs per SM over all rows, chunks of >= 4096 logits
+    const long long rows = (long long)batch * q_len;
+    long long nsplit = (2LL * device_sms(dev) + rows - 1) / rows;
+    const long long by_len = ((long long)vocab + 4095) / 4096;
+    if (nsplit > by_len) nsplit = by_len;
+    if (nsplit < 1) nsplit = 1;
+    long long chunk = ((long long)vocab + nsplit - 1) / nsplit;
+    chunk = (chunk + 7) / 8 * 8;
+    nsplit = ((long long)vocab + chunk - 1) / chunk;
+    A.logits = static_cast<const uint16_t *>(logits);
+    A.keep = keep_ids;
+    A.draft = draft;
+    A.argmax = argmax_out;
+    A.accepted = accepted;
+    A.B = batch;
+    A.q_len = q_len;
+    A.V = vocab;
+    A.nsplit = (int)nsplit;
+    A.chunk = (int)chunk;
+    e = swa::launch_kernel(swa::swa_accept_kernel, dim3((unsigned)nsplit, (unsigned)q_len,
+                                                        (unsigned)batch),
+                           dim3(swa::kAcceptThreads), 0, s, A);
+    if (e != cudaSuccess) return cuda_fail(e, "acceptance kernel launch");
+    t_last_error[0] = '\0';
+    return SWA_OK;
+}
 
 }  // extern "C"
 

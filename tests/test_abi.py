@@ -172,3 +172,23 @@ def test_binding_rejects_cpu_tensors(lib):
     with pytest.raises(ValueError):
         swa.swa_verify_attn(q, k, k, torch.zeros(1, dtype=torch.int32),
                             torch.zeros(1, dtype=torch.int32), 188, 0.0625)
+
+
+def test_greedy_accept_rejects_bad_arguments(lib):
+    # validated on the host before any CUDA call
+    vp = ctypes.c_void_p
+    dummy = vp(16)
+    cases = [
+        (None, None, dummy, dummy, dummy, 1, 8, 100),       # logits NULL
+        (dummy, None, None, dummy, dummy, 1, 8, 100),       # draft NULL with q_len 8
+        (dummy, None, dummy, None, dummy, 1, 8, 100),       # argmax NULL
+        (dummy, None, dummy, dummy, dummy, 0, 8, 100),      # batch 0
+        (dummy, None, dummy, dummy, dummy, 1, 65, 100),     # q_len above 64
+        (dummy, None, dummy, dummy, dummy, 1, 8, 0),        # empty vocabulary
+        (vp(17), None, dummy, dummy, dummy, 1, 8, 100),     # logits not 2-byte aligned
+        (dummy, vp(18), dummy, dummy, dummy, 1, 8, 100),    # keep_ids not 4-byte aligned
+    ]
+    for args in cases:
+        st = lib.swa_greedy_accept(*args, None)
+        assert st == swa.SWA_ERR_INVALID_ARG, args
+        assert swa.swa_last_error()
