@@ -320,6 +320,46 @@ def time_e2e(case, steps, warmup):
 
 # ------------------------------------------------------------ CPU oracle
 
+def time_accept(B, q_len, V, steps=2000, warmup=5, seed=0, graph_len=1000):
+    """Device time of swa_greedy_accept on bf16 N(0,1) logits [B, q_len, V]
+    (graph replays, L2 defeated by logit replicas)."""
+    from sliding_window_speculative_gb300 import swa_greedy_accept
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    nbytes = B * q_len * V * 2
+    l2 = getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 0) or (126 << 20)
+    nrep = 1 if nbytes >= l2 else max(2, min(512, math.ceil(2 * l2 / nbytes)))
+    logits = torch.randn((nrep, B, q_len, V), generator=g, device="cuda").to(torch.bfloat16)
+    draft = torch.randint(0, V, (B, max(q_len - 1, 1)), generator=g, device="cuda",
+                          dtype=torch.int32)[:, :q_len - 1].contiguous()
+    am = torch.empty((B, q_len), dtype=torch.int32, device="cuda")
+    acc = torch.empty((B,), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3)):
+            swa_greedy_accept(logits[i % nrep], draft, None, am, acc)
+    stream.synchronize()
+    n = max(1, min(graph_len, steps))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(n):
+            swa_greedy_accept(logits[i % nrep], draft, None, am, acc)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    stream.synchronize()
+    reps = max(1, steps // n)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    us = start.elapsed_time(end) * 1e3 / (reps * n)
+    return {"batch": B, "q_len": q_len, "vocab": V, "us_per_call": round(us, 3),
+            "logit_gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "replicas": nrep}
+
+
 def oracle_sample(case, budget_s=10.0, max_calls=None, threads=None):
     """Times the fp64 oracle on whole calls of the workload (sequences
     sampled if one call is too long).  Returns per-call seconds scaled to the
@@ -545,6 +585,9 @@ def main():
             del c2
             torch.cuda.empty_cache()
         line["also"] = also
+        # greedy verification of the draft block over a Gemma-size vocabulary
+        # (one sequence, and a 64-sequence batch)
+        line["accept"] = [time_accept(1, 8, 262144), time_accept(64, 8, 262144, steps=500)]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = oracle_sample(case, args.cpu_budget)
         line["cpu_baseline"] = {"value": round(cb["kv_gbs"], 6), "unit": UNIT,
