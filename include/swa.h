@@ -100,6 +100,36 @@ swa_status swa_verify_attn(const void *q, const void *k_cache, const void *v_cac
                            float scale, void *out, float *lse, const swa_dims *dims,
                            swa_stream_t stream);
 
+/* Paged KV cache (vLLM-style block tables): the cache is a pool of pages,
+ * each holding page_size consecutive key positions of one sequence for
+ * every KV head, and a sequence's block table lists its pages in position
+ * order.  The pages mention a reduced KV cache and the window as its reason
+ * ("What each piece does, and why"); a pool lets a server hold only the
+ * pages a window still needs. */
+typedef struct {
+    const int32_t *block_table;  /* device int32 [batch, max_blocks], 4-byte aligned: block k of
+                                    sequence b (positions k*page_size ..) is page block_table[b][k] */
+    int32_t max_blocks;          /* row length of block_table; dims->max_len must equal
+                                    max_blocks * page_size (a sequence's logical capacity) */
+    int32_t page_size;           /* key positions per page, a positive multiple of 8 */
+    int32_t num_pages;           /* pages in the pool */
+} swa_paged;
+
+/* swa_verify_attn on a paged cache:
+ *   k_pages, v_pages  bf16 [num_pages, Hkv, page_size, D], device, 16-byte aligned
+ * and everything else as for swa_verify_attn.  Results equal the contiguous
+ * call on the cache the block tables describe, up to fp32 summation order.
+ * Device preconditions (not checked): for every sequence, block_table[b][k]
+ * is a valid page (0 <= page < num_pages) for each block holding positions
+ * below seq_lens[b]; entries past that are never read.  Returns
+ * SWA_ERR_INVALID_ARG for a NULL or misaligned table, a page size that is not
+ * a positive multiple of 8, or dims->max_len != max_blocks * page_size;
+ * SWA_ERR_UNSUPPORTED if the pool holds 2^31 or more rows. */
+swa_status swa_verify_attn_paged(const void *q, const void *k_pages, const void *v_pages,
+                                 const swa_paged *paged, const int32_t *seq_lens,
+                                 const int32_t *q_pos, int32_t window, float scale, void *out,
+                                 float *lse, const swa_dims *dims, swa_stream_t stream);
+
 /* Upper bound, in bytes, of the split-partial workspace any call with these
  * dims and window may need on any device (pure host arithmetic; 0 if the
  * arguments are invalid).  Layout: fp32 acc [B, Hkv, splits, R, D] followed

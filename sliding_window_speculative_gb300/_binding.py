@@ -74,6 +74,9 @@ def load_library(path=LIB_PATH):
     lib.swa_version.restype = ctypes.c_char_p
     lib.swa_verify_attn_noalloc.argtypes = lib.swa_verify_attn.argtypes
     lib.swa_verify_attn_noalloc.restype = ctypes.c_int
+    lib.swa_verify_attn_paged.argtypes = [vp, vp, vp, ctypes.POINTER(SwaPaged), vp, vp, i32,
+                                          ctypes.c_float, vp, vp, ctypes.POINTER(SwaDims), vp]
+    lib.swa_verify_attn_paged.restype = ctypes.c_int
     lib.swa_greedy_accept.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp]
     lib.swa_greedy_accept.restype = ctypes.c_int
     _lib = lib
@@ -83,6 +86,51 @@ def load_library(path=LIB_PATH):
 def _check(status):
     if status != SWA_OK:
         raise SwaError(status, swa_last_error())
+
+
+class SwaPaged(ctypes.Structure):
+    """swa_paged of include/swa.h."""
+    _fields_ = [("block_table", ctypes.c_void_p), ("max_blocks", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32)]
+
+
+def swa_verify_attn_paged(q, k_pages, v_pages, block_table, seq_lens, q_pos, window, scale,
+                          out=None, lse=None, num_splits=0, stream=None):
+    """Windowed verify attention over a paged cache (C entry point
+    swa_verify_attn_paged).
+
+    k_pages, v_pages bf16 [num_pages, Hkv, page_size, D]; block_table int32
+    [B, max_blocks] (device): block k of sequence b is page
+    block_table[b, k].  Everything else as swa_verify_attn.
+    """
+    lib = load_library()
+    B, q_len, Hq, D = q.shape
+    pq = _dev_tensor(q, "q", torch.bfloat16, 4)
+    pk = _dev_tensor(k_pages, "k_pages", torch.bfloat16, 4)
+    pv = _dev_tensor(v_pages, "v_pages", torch.bfloat16, 4)
+    if v_pages.shape != k_pages.shape or k_pages.shape[3] != D:
+        raise ValueError("k_pages / v_pages shapes do not match each other or q")
+    pt = _dev_tensor(block_table, "block_table", torch.int32, 2)
+    if block_table.shape[0] != B:
+        raise ValueError("block_table needs one row per sequence")
+    ps = _dev_tensor(seq_lens, "seq_lens", torch.int32, 1)
+    pp = _dev_tensor(q_pos, "q_pos", torch.int32, 1)
+    if out is None:
+        out = torch.empty_like(q)
+    po = _dev_tensor(out, "out", torch.bfloat16, 4)
+    if lse is None:
+        lse = torch.empty((B, q_len, Hq), dtype=torch.float32, device=q.device)
+    pl = _dev_tensor(lse, "lse", torch.float32, 3)
+    num_pages, Hkv, page_size = k_pages.shape[0], k_pages.shape[1], k_pages.shape[2]
+    max_blocks = block_table.shape[1]
+    paged = SwaPaged(pt, max_blocks, page_size, num_pages)
+    dims = make_dims(B, q_len, Hq, Hkv, D, max_blocks * page_size, num_splits)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _check(lib.swa_verify_attn_paged(pq, pk, pv, ctypes.byref(paged), ps, pp, int(window),
+                                     float(scale), po, pl, ctypes.byref(dims), handle))
+    return out, lse
 
 
 def make_dims(batch, q_len, num_q_heads, num_kv_heads, head_dim, max_len, num_splits=0):

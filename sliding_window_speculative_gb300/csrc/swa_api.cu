@@ -297,7 +297,8 @@ cudaError_t launch_merge(const swa::AttnParams &P, cudaStream_t s) {
 // Launches the attention kernel of `pl` (and the merge kernel when the
 // plan splits the keys).  P carries every pointer, including the partials.
 swa_status launch_plan(const Plan &pl, const swa_dims *dims, const swa::AttnParams &P,
-                       const void *q, const void *k_cache, const void *v_cache, cudaStream_t s) {
+                       const void *q, const void *k_cache, const void *v_cache, cudaStream_t s,
+                       long long cache_rows = -1) {
     cudaError_t e;
     if (pl.kernel >= 2) {
         swa::TcLaunch L{};
@@ -309,6 +310,7 @@ swa_status launch_plan(const Plan &pl, const swa_dims *dims, const swa::AttnPara
         L.N = pl.tc_n;
         L.rows_major = pl.kernel == 3;
         L.grid = (int)pl.grid;
+        L.cache_rows = cache_rows >= 0 ? cache_rows : (long long)P.B * P.Hkv * P.L;
         L.q = q;
         L.k = k_cache;
         L.v = v_cache;
@@ -356,20 +358,18 @@ int device_sms(int dev) {
     return cache[dev];
 }
 
-}  // namespace
-
-extern "C" {
-
-swa_status swa_verify_attn(const void *q, const void *k_cache, const void *v_cache,
-                           const int32_t *seq_lens, const int32_t *q_pos, int32_t window,
-                           float scale, void *out, float *lse, const swa_dims *dims,
-                           swa_stream_t stream) {
+// The windowed verify attention of swa_verify_attn, on a contiguous cache
+// (paged == NULL) or a paged one.
+swa_status verify_impl(const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *seq_lens, const int32_t *q_pos, int32_t window, float scale,
+                       void *out, float *lse, const swa_dims *dims, swa_stream_t stream,
+                       const swa_paged *paged) {
     swa_status st = validate_dims(dims, window);
     if (st != SWA_OK) return st;
     if (!q || !k_cache || !v_cache || !seq_lens || !q_pos || !out)
         return fail(SWA_ERR_INVALID_ARG, "a required pointer is NULL");
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-        return fail(SWA_ERR_INVALID_ARG, "q, k_cache, v_cache and out must be 16-byte aligned");
+        return fail(SWA_ERR_INVALID_ARG, "q, the K and V caches and out must be 16-byte aligned");
     if ((reinterpret_cast<uintptr_t>(seq_lens) & 3u) || (reinterpret_cast<uintptr_t>(q_pos) & 3u) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u))
         return fail(SWA_ERR_INVALID_ARG, "seq_lens, q_pos and lse must be 4-byte aligned");
@@ -406,6 +406,13 @@ swa_status swa_verify_attn(const void *q, const void *k_cache, const void *v_cac
     P.rows_per_tile = pl.rows_per_tile;
     P.qk_scale = scale * swa::kLog2e;
     P.fault = fault;
+    long long cache_rows = (long long)P.B * P.Hkv * P.L;
+    if (paged != nullptr) {
+        P.block_table = paged->block_table;
+        P.page_size = paged->page_size;
+        P.max_blocks = paged->max_blocks;
+        cache_rows = (long long)paged->num_pages * P.Hkv * paged->page_size;
+    }
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (pl.splits > 1) {
@@ -415,10 +422,46 @@ swa_status swa_verify_attn(const void *q, const void *k_cache, const void *v_cac
         P.part_acc = static_cast<float *>(ws);
         P.part_ml = P.part_acc + (size_t)P.B * P.Hkv * P.splits * P.R * dims->head_dim;
     }
-    st = launch_plan(pl, dims, P, q, k_cache, v_cache, s);
+    st = launch_plan(pl, dims, P, q, k_cache, v_cache, s, cache_rows);
     if (st != SWA_OK) return st;
     t_last_error[0] = '\0';
     return SWA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+swa_status swa_verify_attn(const void *q, const void *k_cache, const void *v_cache,
+                           const int32_t *seq_lens, const int32_t *q_pos, int32_t window,
+                           float scale, void *out, float *lse, const swa_dims *dims,
+                           swa_stream_t stream) {
+    return verify_impl(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out, lse, dims, stream,
+                       nullptr);
+}
+
+swa_status swa_verify_attn_paged(const void *q, const void *k_pages, const void *v_pages,
+                                 const swa_paged *paged, const int32_t *seq_lens,
+                                 const int32_t *q_pos, int32_t window, float scale, void *out,
+                                 float *lse, const swa_dims *dims, swa_stream_t stream) {
+    if (paged == nullptr || paged->block_table == nullptr)
+        return fail(SWA_ERR_INVALID_ARG, "paged cache description or its block table is NULL");
+    if (reinterpret_cast<uintptr_t>(paged->block_table) & 3u)
+        return fail(SWA_ERR_INVALID_ARG, "block_table must be 4-byte aligned");
+    if (paged->page_size < 8 || paged->page_size % 8 != 0)
+        return fail(SWA_ERR_INVALID_ARG, "page_size %d is not a positive multiple of 8",
+                    paged->page_size);
+    if (paged->max_blocks < 1 || paged->num_pages < 1)
+        return fail(SWA_ERR_INVALID_ARG, "max_blocks %d and num_pages %d must be >= 1",
+                    paged->max_blocks, paged->num_pages);
+    if (dims != nullptr && (long long)dims->max_len != (long long)paged->max_blocks * paged->page_size)
+        return fail(SWA_ERR_INVALID_ARG, "dims->max_len %d != max_blocks * page_size = %lld",
+                    dims->max_len, (long long)paged->max_blocks * paged->page_size);
+    if (dims != nullptr &&
+        (long long)paged->num_pages * dims->num_kv_heads * paged->page_size >= (1LL << 31))
+        return fail(SWA_ERR_UNSUPPORTED, "the page pool holds 2^31 or more rows");
+    return verify_impl(q, k_pages, v_pages, seq_lens, q_pos, window, scale, out, lse, dims, stream,
+                       paged);
 }
 
 size_t swa_workspace_bytes(const swa_dims *dims, int32_t window) {

@@ -56,9 +56,9 @@ struct RowsCfg {
     static constexpr int FTAB_OFF = META_OFF + kTcMetaItems * (int)sizeof(TcItem);
     // the pairs' exchange: half maxima [tile parity][quadrant][half][lane],
     // half row sums [quadrant][half][lane]
-    static constexpr int XM_OFF = FTAB_OFF + kFillTab * 4;
+    static constexpr int XM_OFF = (FTAB_OFF + kFillTab * 4 + 15) & ~15;
     static constexpr int XL_OFF = XM_OFF + 2 * 4 * 2 * 32 * 4;
-    static constexpr int STG_OFF = XL_OFF + 4 * 2 * 32 * 4;
+    static constexpr int STG_OFF = (XL_OFF + 4 * 2 * 32 * 4 + 15) & ~15;  // 16-byte stores
     // output staging, 2 KB per softmax warp (32 rows x 64 bytes), where it fits
     static constexpr int STG_NEED = 8 * 2048;
     static constexpr bool STAGE = STG_OFF + STG_NEED + 1024 + 512 <= 227 * 1024;
@@ -81,6 +81,7 @@ struct RowsCfg {
     static_assert(QB * Q_BUF - Q_SLAB + 128 * 128 <= RING_OFF + NT * TILE_BYTES,
                   "an MMA's 128-row read of the last Q slab stays in shared memory");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+    static_assert(STG_OFF % 16 == 0 && BAR_OFF % 8 == 0 && META_OFF % 8 == 0, "alignment");
 };
 
 template <int D, int QR, int NT, int QB>
@@ -157,30 +158,6 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
         // ======================================================= producer
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();
-            // the copies of one K or V tile of n_valid keys starting at cache row y
-            auto tile_copies = [&](int kv, int y, int n_valid, uint8_t *dst, uint64_t *bar) {
-                const int atoms = n_valid >> 3, rem = n_valid & 7;
-                const CUtensorMap *m4 = kv ? M.v_atoms : M.k_atoms;
-                const CUtensorMap *m1 = kv ? &M.v_atom : &M.k_atom;
-                if (atoms == 16) {
-                    tma_load_4d_hint(dst, &m4[0], 0, y, 0, 0, bar, policy);
-                    return;
-                }
-                // whole atoms lie inside the chunk (4D boxes); the last, partial
-                // atom goes through the bounds-checked one-atom box
-                int a = 0;
-#pragma unroll
-                for (int bi = 1; bi < 4; ++bi) {
-                    const int na = 16 >> bi;
-                    if (atoms & na) {
-                        tma_load_4d_hint(dst + a * C::ATOM_BYTES, &m4[bi], 0, y + 8 * a, 0, 0, bar,
-                                         policy);
-                        a += na;
-                    }
-                }
-                for (int e = 0; e < (atoms & 1) + (rem != 0); ++e, ++a)
-                    tma_load_3d_hint(dst + a * C::ATOM_BYTES, m1, 0, y + 8 * a, 0, bar, policy);
-            };
             uint32_t f = 0, k = 0;  // fills (two per tile: K then V), items with keys
             uint32_t uses[NT];      // fills handed to each slot so far
 #pragma unroll
@@ -204,12 +181,9 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                     return true;
                 };
                 ++k;
-                const int y0 = (it.b * P.Hkv + it.h) * P.L + it.cr.c_lo;
                 for (int t = 0; t < it.n_tiles && ok; ++t) {
-                    const int n_valid =
-                        min(kTcTileKeys, it.cr.c_hi - it.cr.c_lo - kTcTileKeys * t);
-                    const int atoms = n_valid >> 3, rem = n_valid & 7;
-                    const int y = y0 + kTcTileKeys * t;
+                    const int p = it.t0 + kTcTileKeys * t;
+                    const int n_valid = min(kTcTileKeys, it.cr.c_hi - p);
                     for (int kv = 0; kv < 2 && ok; ++kv) {
                         if (t == 0 && kv == 1) {
                             ok = load_q();
@@ -240,8 +214,9 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                         if (!ok) break;
                         ftab[f % kFillTab] = (f << 8) | (par << 4) | (uint32_t)slot;
                         uint64_t *bar = &bars[C::B_FULL + slot];
-                        mbar_arrive_expect_tx(bar, (uint32_t)(atoms + (rem != 0)) * C::ATOM_BYTES);
-                        tile_copies(kv, y, n_valid, ring + slot * C::TILE_BYTES, bar);
+                        mbar_arrive_expect_tx(bar, (uint32_t)((n_valid + 7) >> 3) * C::ATOM_BYTES);
+                        tile_copies<C::ATOM_BYTES>(P, M, kv, it.b, it.h, p, n_valid,
+                                                   ring + slot * C::TILE_BYTES, bar, policy);
                         ++f;
                     }
                 }
@@ -274,6 +249,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
             struct Cursor {
                 int item, j, t, n_tiles;
                 int last_keys;  // keys of the item's last tile
+                int head;       // key rows before the chunk in its first tile (paged cache)
                 uint32_t k, g;
                 bool valid;
                 int slot;       // this cursor's fill: slot, parity (-1: not yet looked up)
@@ -292,7 +268,8 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                     const TcItem it = tc_decode(T, c.item, c.j, meta);
                     if (it.n_tiles > 0) {
                         c.n_tiles = it.n_tiles;
-                        c.last_keys = it.cr.c_hi - it.cr.c_lo - kTcTileKeys * (it.n_tiles - 1);
+                        c.last_keys = it.cr.c_hi - it.t0 - kTcTileKeys * (it.n_tiles - 1);
+                        c.head = it.cr.c_lo - it.t0;
                         c.t = 0;
                         c.valid = true;
                         return;
@@ -309,7 +286,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                 ++c.j;
                 seek(c);
             };
-            Cursor qc{(int)blockIdx.x, 0, 0, 0, 0, 0u, 0u, false, -1, 0u};
+            Cursor qc{(int)blockIdx.x, 0, 0, 0, 0, 0, 0u, 0u, false, -1, 0u};
             seek(qc);
             Cursor pc = qc;
             bool ok = true;
@@ -347,6 +324,20 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                                             make_uint4(0, 0, 0, 0);
                                 }
                             }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                        }
+                        if (pc.t == 0 && pc.head > 0) {
+                            // (paged cache) the rows before the chunk in its first
+                            // tile: P is 0 there, but they may hold anything
+                            const int row = lane >> 3, q = lane & 7;
+#pragma unroll
+                            for (int s = 0; s < SLABS; ++s)
+#pragma unroll
+                                for (int r4 = 0; r4 < 8; r4 += 4)
+                                    if (row + r4 < pc.head)
+                                        reinterpret_cast<uint4 *>(vt + s * 1024 + (row + r4) * 128)[q] =
+                                            make_uint4(0, 0, 0, 0);
                             fence_proxy_async_smem();
                             __syncwarp();
                         }
@@ -495,7 +486,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
                     fence_after_sync();
                     // this thread's 64 scores (keys kh .. kh + 63 of the tile), masked
                     // to the row's keys, in log2 units
-                    const long long j0 = (long long)it.cr.c_lo + (long long)kTcTileKeys * t + kh;
+                    const long long j0 = (long long)it.t0 + (long long)kTcTileKeys * t + kh;
                     const long long ca_l = jlo - j0, cb_l = jhi - j0;
                     const int ca = ca_l < 0 ? 0 : (ca_l > 64 ? 64 : (int)ca_l);
                     const int cb = cb_l < -1 ? -1 : (cb_l > 63 ? 63 : (int)cb_l);

@@ -36,6 +36,10 @@ struct AttnParams {
     float *part_acc;  // [B*Hkv, splits, R, D]  (splits > 1)
     float *part_ml;   // [B*Hkv, splits, R, 2]
     uint32_t *fault;  // device fault word (bounded waits that gave up)
+    // paged cache (block_table non-null): k/v are [pages, Hkv, page_size, D]
+    // and key position j of sequence b lives in page block_table[b][j / page_size]
+    const int32_t *block_table;  // [B, max_blocks]
+    int page_size, max_blocks;
     int B, q_len, Hq, Hkv, G, L, window, R;
     int splits, chunk, row_tiles, rows_per_tile;
     float qk_scale;   // scale * log2(e)
@@ -73,6 +77,14 @@ __device__ __forceinline__ ChunkRange chunk_range_of(const AttnParams &P, long l
 
 __device__ __forceinline__ ChunkRange chunk_range(const AttnParams &P, int b, int split) {
     return chunk_range_of(P, P.q_pos[b], P.seq_lens[b], split);
+}
+
+// Cache row (in rows of D elements) of key position j of (sequence b, KV
+// head h): contiguous [B, Hkv, L] or, with a block table, the page's row.
+__device__ __forceinline__ long long cache_row(const AttnParams &P, int b, int h, int j) {
+    if (P.block_table == nullptr) return ((long long)b * P.Hkv + h) * P.L + j;
+    const int page = P.block_table[(long long)b * P.max_blocks + j / P.page_size];
+    return ((long long)page * P.Hkv + h) * P.page_size + (j % P.page_size);
 }
 
 template <int D>
@@ -157,9 +169,6 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
     const int n_keys = cr.c_hi - cr.c_lo;
     const int n_tiles = n_keys > 0 ? (n_keys + kSimtTileKeys - 1) / kSimtTileKeys : 0;
 
-    const size_t slab = ((size_t)b * P.Hkv + h) * (size_t)P.L;  // first row of this (b, h)
-    const __nv_bfloat16 *kslab = P.k + slab * D;
-    const __nv_bfloat16 *vslab = P.v + slab * D;
 
     if (tid == 0) {
         for (int s = 0; s < C::STAGES; ++s) mbar_init(&full[s], 1);
@@ -174,8 +183,20 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
         const uint32_t bytes = (uint32_t)n * D * 2;
         uint8_t *dst = ring + s * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&full[s], 2 * bytes);
-        bulk_copy_g2s(dst, kslab + (size_t)j0 * D, bytes, &full[s]);
-        bulk_copy_g2s(dst + C::TILE_BYTES, vslab + (size_t)j0 * D, bytes, &full[s]);
+        // one copy per run of rows contiguous in the cache (a page's rows, or
+        // the whole tile of a contiguous cache)
+        for (int j = j0; j < j0 + n;) {
+            int run = j0 + n - j;
+            if (P.block_table != nullptr) {
+                const int left = P.page_size - j % P.page_size;
+                run = run < left ? run : left;
+            }
+            const size_t row = (size_t)cache_row(P, b, h, j);
+            const uint32_t rb = (uint32_t)run * D * 2, off = (uint32_t)(j - j0) * D * 2;
+            bulk_copy_g2s(dst + off, P.k + row * D, rb, &full[s]);
+            bulk_copy_g2s(dst + C::TILE_BYTES + off, P.v + row * D, rb, &full[s]);
+            j += run;
+        }
     };
     if (tid == 0) {
         for (int t = 0; t < C::STAGES - 1 && t < n_tiles; ++t) issue(t);

@@ -142,13 +142,14 @@ cudaError_t tc_launch(const TcLaunch &L, cudaStream_t stream, char *err, size_t 
     }
     const AttnParams &P = L.T.a;
     const int D = L.D;
-    // K and V cache viewed as rows of D bf16 (B * Hkv * L rows).  4D maps
+    // K and V cache viewed as rows of D bf16 (B * Hkv * L rows, or every
+    // page's rows of a paged cache).  4D maps
     // (x = 64 dims, y = row, z = 64-dim slab, w = 8-row atom; strides D*2,
     // 128 and 8*D*2 bytes) with boxes of 16, 8, 4 and 2 atoms, and a 3D
     // one-atom map (x, y, z) whose rows are bounds-checked one by one.
     // Both land as [atom][slab][8 rows][128 bytes], 128-byte swizzled.
     TcMaps maps;
-    const cuuint64_t rows = (cuuint64_t)P.B * P.Hkv * (cuuint64_t)P.L;
+    const cuuint64_t rows = (cuuint64_t)L.cache_rows;
     const cuuint32_t slabs = (cuuint32_t)(D / 64);
     for (int kv = 0; kv < 2; ++kv) {
         const void *base = kv ? L.v : L.k;

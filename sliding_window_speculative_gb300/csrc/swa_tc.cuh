@@ -61,7 +61,7 @@ namespace swa {
 constexpr int kTcThreads = 320;
 constexpr int kTcTileKeys = 128;
 constexpr int kTcTailBox = 32;    // keys per box of a partial tile
-constexpr int kTcMetaItems = 8;   // items per CTA decoded once into shared memory
+constexpr int kTcMetaItems = 7;   // items per CTA decoded once into shared memory
 // Ring slots are handed out in any order (the first free one), so a K tile,
 // consumed as soon as its scores are computed, frees its slot long before
 // the V tiles around it; a table of the recent fills tells the MMA lane
@@ -75,6 +75,8 @@ constexpr float kNoRef = -1.0e30f;
 struct TcItem {
     int b, h, split, rt;
     ChunkRange cr;
+    int t0;    // key position of tile 0: the chunk start, or (paged cache) that
+               // rounded down to 8 so every 8-key atom lies inside one page
     int n_tiles;
     int row0;  // first packed row of the item
     int rows;  // packed rows of the item
@@ -124,6 +126,7 @@ struct TcCfg {
     static_assert(TMEM_USED <= 512, "TMEM");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
     static_assert(PB * P_BUF >= N * 512, "epilogue staging fits in the P buffers");
+    static_assert(RED_OFF % 16 == 0 && BAR_OFF % 8 == 0 && META_OFF % 8 == 0, "alignment");
 };
 
 
@@ -139,8 +142,9 @@ __device__ __forceinline__ TcItem tc_decode_global(const TcParams &T, int item) 
     it.h = rest % P.Hkv;
     it.b = rest / P.Hkv;
     it.cr = chunk_range(P, it.b, it.split);
-    const int nk = it.cr.c_hi - it.cr.c_lo;
-    it.n_tiles = nk > 0 ? (nk + kTcTileKeys - 1) / kTcTileKeys : 0;
+    it.t0 = P.block_table != nullptr ? (it.cr.c_lo & ~7) : it.cr.c_lo;
+    const int nk = it.cr.c_hi - it.t0;
+    it.n_tiles = it.cr.c_hi > it.cr.c_lo ? (nk + kTcTileKeys - 1) / kTcTileKeys : 0;
     it.row0 = it.rt * T.rows_per_tile;
     it.rows = min(P.R - it.row0, T.rows_per_tile);
     it.i0 = it.rt * T.q_rows_per_tile;
@@ -219,6 +223,57 @@ __device__ __forceinline__ void tmem_store(uint32_t taddr, const uint32_t *r) {
     } else {
         static_assert(W == 8, "store width");
         tc::tmem_st8(taddr, r);
+    }
+}
+
+// The copies of one K or V tile: key positions [p, p + n_valid) of
+// (sequence b, KV head h) into ceil(n_valid / 8) atoms of AB bytes at dst,
+// completing on `bar`.  Whole atoms go through the 4D boxes (16, 8, 4 or 2
+// atoms: the rows of a run are consecutive cache rows); a single or a
+// partial atom through the 3D one-atom box, whose rows past the cache the
+// TMA zero-fills.  A contiguous cache is one run; a paged cache breaks runs
+// at page ends (pages hold a multiple of 8 rows and its tiles start on an
+// 8-key boundary, so no atom straddles two pages).
+template <int AB>
+__device__ __forceinline__ void tile_copies(const AttnParams &P, const TcMaps &M, int kv, int b,
+                                            int h, int p, int n_valid, uint8_t *dst, uint64_t *bar,
+                                            uint64_t policy) {
+    using namespace tc;
+    const CUtensorMap *m4 = kv ? M.v_atoms : M.k_atoms;
+    const CUtensorMap *m1 = kv ? &M.v_atom : &M.k_atom;
+    const int full = n_valid >> 3, natoms = (n_valid + 7) >> 3;
+    int a = 0;
+    while (a < natoms) {
+        const int pos = p + 8 * a;
+        int run = natoms - a;
+        if (P.block_table != nullptr) {
+            const int left = (P.page_size - pos % P.page_size) >> 3;
+            run = run < left ? run : left;
+        }
+        const int y = (int)cache_row(P, b, h, pos);
+        int whole = full - a;
+        whole = whole < 0 ? 0 : (whole > run ? run : whole);
+        int w = 0;
+        if (whole == 16) {
+            tma_load_4d_hint(dst + a * AB, &m4[0], 0, y, 0, 0, bar, policy);
+            w = 16;
+        } else {
+#pragma unroll
+            for (int bi = 1; bi < 4; ++bi) {
+                const int na = 16 >> bi;
+                if (whole & na) {
+                    tma_load_4d_hint(dst + (a + w) * AB, &m4[bi], 0, y + 8 * w, 0, 0, bar, policy);
+                    w += na;
+                }
+            }
+            if (whole & 1) {
+                tma_load_3d_hint(dst + (a + w) * AB, m1, 0, y + 8 * w, 0, bar, policy);
+                ++w;
+            }
+        }
+        if (run > whole)  // the tile's last, partial atom
+            tma_load_3d_hint(dst + (a + w) * AB, m1, 0, y + 8 * w, 0, bar, policy);
+        a += run;
     }
 }
 
@@ -309,32 +364,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ======================================================= producer
         if (lane == 0) {
             const uint64_t policy = l2_policy_evict_first();
-            // The copies of one tile (K or V) of n_valid keys starting at cache
-            // row y into `dst`, completing on `bar`.
-            auto tile_copies = [&](int kv, int y, int n_valid, uint8_t *dst, uint64_t *bar) {
-                const int atoms = n_valid >> 3, rem = n_valid & 7;
-                const CUtensorMap *m4 = kv ? M.v_atoms : M.k_atoms;
-                const CUtensorMap *m1 = kv ? &M.v_atom : &M.k_atom;
-                if (atoms == 16) {
-                    tma_load_4d_hint(dst, &m4[0], 0, y, 0, 0, bar, policy);
-                    return;
-                }
-                // whole atoms lie inside the chunk, so the 4D boxes (whose rows
-                // span two coordinates) stay inside the cache; the last, partial
-                // atom goes through the bounds-checked one-atom box
-                int a = 0;
-#pragma unroll
-                for (int bi = 1; bi < 4; ++bi) {
-                    const int na = 16 >> bi;
-                    if (atoms & na) {
-                        tma_load_4d_hint(dst + a * C::ATOM_BYTES, &m4[bi], 0, y + 8 * a, 0, 0, bar,
-                                         policy);
-                        a += na;
-                    }
-                }
-                for (int e = 0; e < (atoms & 1) + (rem != 0); ++e, ++a)
-                    tma_load_3d_hint(dst + a * C::ATOM_BYTES, m1, 0, y + 8 * a, 0, bar, policy);
-            };
             uint32_t f = 0, k = 0;  // fills (two per tile: K then V), items with keys
             uint32_t uses[NT];      // fills handed to each slot so far
 #pragma unroll
@@ -358,12 +387,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     return true;
                 };
                 ++k;
-                const int y0 = (it.b * P.Hkv + it.h) * P.L + it.cr.c_lo;
                 for (int t = 0; t < it.n_tiles && ok; ++t) {
-                    const int n_valid =
-                        min(kTcTileKeys, it.cr.c_hi - it.cr.c_lo - kTcTileKeys * t);
-                    const int atoms = n_valid >> 3, rem = n_valid & 7;
-                    const int y = y0 + kTcTileKeys * t;
+                    const int p = it.t0 + kTcTileKeys * t;
+                    const int n_valid = min(kTcTileKeys, it.cr.c_hi - p);
                     for (int kv = 0; kv < 2 && ok; ++kv) {
                         if (t == 0 && kv == 1) {
                             ok = load_q();
@@ -394,8 +420,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         if (!ok) break;
                         ftab[f % kFillTab] = (f << 8) | (par << 4) | (uint32_t)slot;
                         uint64_t *bar = &bars[C::B_FULL + slot];
-                        mbar_arrive_expect_tx(bar, (uint32_t)(atoms + (rem != 0)) * C::ATOM_BYTES);
-                        tile_copies(kv, y, n_valid, ring + slot * C::TILE_BYTES, bar);
+                        mbar_arrive_expect_tx(bar, (uint32_t)((n_valid + 7) >> 3) * C::ATOM_BYTES);
+                        tile_copies<C::ATOM_BYTES>(P, M, kv, it.b, it.h, p, n_valid,
+                                                   ring + slot * C::TILE_BYTES, bar, policy);
                         ++f;
                     }
                 }
@@ -432,6 +459,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             struct Cursor {
                 int item, j, t, n_tiles;
                 int last_keys;  // keys of the item's last tile
+                int head;       // key rows before the chunk in its first tile (paged cache)
                 uint32_t k, g;
                 bool valid;
                 int slot;       // this cursor's fill: slot, parity (-1: not yet looked up)
@@ -451,7 +479,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     const TcItem it = tc_decode(T, c.item, c.j, meta);
                     if (it.n_tiles > 0) {
                         c.n_tiles = it.n_tiles;
-                        c.last_keys = it.cr.c_hi - it.cr.c_lo - kTcTileKeys * (it.n_tiles - 1);
+                        c.last_keys = it.cr.c_hi - it.t0 - kTcTileKeys * (it.n_tiles - 1);
+                        c.head = it.cr.c_lo - it.t0;
                         c.t = 0;
                         c.valid = true;
                         return;
@@ -468,7 +497,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ++c.j;
                 seek(c);
             };
-            Cursor qc{(int)blockIdx.x, 0, 0, 0, 0, 0u, 0u, false, -1, 0u};
+            Cursor qc{(int)blockIdx.x, 0, 0, 0, 0, 0, 0u, 0u, false, -1, 0u};
             seek(qc);
             Cursor pc = qc;
             bool ok = true;
@@ -509,6 +538,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                             make_uint4(0, 0, 0, 0);
                                 }
                             }
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                        }
+                        if (pc.t == 0 && pc.head > 0) {
+                            // (paged cache) the rows before the chunk in its first
+                            // tile: P is 0 there, but they may hold anything
+                            const int row = lane >> 3, q = lane & 7;
+#pragma unroll
+                            for (int s = 0; s < SLABS; ++s)
+#pragma unroll
+                                for (int r4 = 0; r4 < 8; r4 += 4)
+                                    if (row + r4 < pc.head)
+                                        reinterpret_cast<uint4 *>(vt + s * 1024 + (row + r4) * 128)[q] =
+                                            make_uint4(0, 0, 0, 0);
                             fence_proxy_async_smem();
                             __syncwarp();
                         }
@@ -668,14 +711,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                                        P.fault, kFaultCopyTimeout));
                 if (!ok) break;
                 fence_after_sync();
-                const int j0 = it.cr.c_lo + kTcTileKeys * t;
+                const int j0 = it.t0 + kTcTileKeys * t;
                 const int n_valid = min(kTcTileKeys, it.cr.c_hi - j0);
                 const int jk = j0 + lk;
                 // packed rows [ra, rb) of this item whose window holds key jk:
                 // draft row i sees jk iff p_i - W < jk <= p_i, p_i = qp_i0 + i;
                 // shifted to this group's rows
                 int ra = 0, rb = 0;
-                if (lk < n_valid) {
+                if (lk < n_valid && jk >= it.cr.c_lo) {
                     const long long lo_i = (long long)jk - qp_i0;
                     const long long hi_i = (long long)jk + P.window - qp_i0;
                     const long long a = lo_i < 0 ? 0 : lo_i * P.G;

@@ -44,6 +44,7 @@ struct TcLaunch {
     int rows_major;  // 1: the kernel with packed rows as the MMA's M (swa_rows_kernel)
     int D, N;   // head_dim, padded rows per item (rows kernel: 32, 64 or 128)
     int grid;   // persistent CTAs
+    long long cache_rows;  // rows of D elements in each of the K and V tensors
     const void *k, *v, *q;
 };
 
