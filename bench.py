@@ -320,6 +320,57 @@ def time_e2e(case, steps, warmup):
 
 # ------------------------------------------------------------ CPU oracle
 
+def time_paged(name, page_size, steps=50, warmup=5, seed=0):
+    """Device time of swa_verify_attn_paged on workload `name` whose cache is
+    scattered over a shuffled page pool (pages of `page_size` rows)."""
+    from sliding_window_speculative_gb300 import swa_verify_attn_paged
+    case = make_workload(name, torch.device("cuda"), seed=seed)
+    B, Hkv, L, D = case.k_cache.shape
+    nb = L // page_size
+    g = torch.Generator().manual_seed(seed)
+    table = torch.randperm(B * nb, generator=g).view(B, nb).to(torch.int32)
+    inv = torch.empty_like(table.view(-1))
+    inv[table.view(-1).long()] = torch.arange(B * nb, dtype=torch.int32)
+    # page table[b, k] holds rows [k*page_size, (k+1)*page_size) of sequence b
+    src_k = case.k_cache.view(B, Hkv, nb, page_size, D).permute(0, 2, 1, 3, 4).reshape(B * nb, Hkv, page_size, D)
+    src_v = case.v_cache.view(B, Hkv, nb, page_size, D).permute(0, 2, 1, 3, 4).reshape(B * nb, Hkv, page_size, D)
+    kp = src_k[inv.long().cuda()].contiguous()
+    vp = src_v[inv.long().cuda()].contiguous()
+    table = table.cuda()
+    kv, total = workload_bytes(case)
+    out = torch.empty_like(case.q)
+    lse = torch.empty(case.q.shape[:3], dtype=torch.float32, device="cuda")
+    del src_k, src_v
+    case.k_cache = case.v_cache = None
+    torch.cuda.empty_cache()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(max(warmup, 3)):
+            swa_verify_attn_paged(case.q, kp, vp, table, case.seq_lens, case.q_pos, case.window,
+                                  case.scale, out=out, lse=lse)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(steps):
+            swa_verify_attn_paged(case.q, kp, vp, table, case.seq_lens, case.q_pos, case.window,
+                                  case.scale, out=out, lse=lse)
+    with torch.cuda.stream(stream):
+        graph.replay()
+    stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        graph.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    us = start.elapsed_time(end) * 1e3 / steps
+    del kp, vp, graph
+    torch.cuda.empty_cache()
+    return {"workload": name, "page_size": page_size, "us_per_call": round(us, 3),
+            "achieved_gbs": round(total / (us * 1e-6) / 1e9, 2)}
+
+
 def time_accept(B, q_len, V, steps=2000, warmup=5, seed=0, graph_len=1000):
     """Device time of swa_greedy_accept on bf16 N(0,1) logits [B, q_len, V]
     (graph replays, L2 defeated by logit replicas)."""
@@ -588,6 +639,8 @@ def main():
         # greedy verification of the draft block over a Gemma-size vocabulary
         # (one sequence, and a 64-sequence batch)
         line["accept"] = [time_accept(1, 8, 262144), time_accept(64, 8, 262144, steps=500)]
+        # the bandwidth-stress batch (inputs larger than L2) on a paged cache
+        line["paged"] = [time_paged("stress_w188_q8", 16), time_paged("stress_w188_q8", 64)]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = oracle_sample(case, args.cpu_budget)
         line["cpu_baseline"] = {"value": round(cb["kv_gbs"], 6), "unit": UNIT,

@@ -234,46 +234,71 @@ __device__ __forceinline__ void tmem_store(uint32_t taddr, const uint32_t *r) {
 // TMA zero-fills.  A contiguous cache is one run; a paged cache breaks runs
 // at page ends (pages hold a multiple of 8 rows and its tiles start on an
 // 8-key boundary, so no atom straddles two pages).
+// Whole atoms [0, whole) and, if `partial`, one more through the 3D box: a
+// run of consecutive cache rows starting at row y into dst.
+template <int AB>
+__device__ __forceinline__ void atom_run(const CUtensorMap *m4, const CUtensorMap *m1, int y,
+                                         int whole, bool partial, uint8_t *dst, uint64_t *bar,
+                                         uint64_t policy) {
+    using namespace tc;
+    int w = 0;
+    if (whole == 16) {
+        tma_load_4d_hint(dst, &m4[0], 0, y, 0, 0, bar, policy);
+        return;
+    }
+#pragma unroll
+    for (int bi = 1; bi < 4; ++bi) {
+        const int na = 16 >> bi;
+        if (whole & na) {
+            tma_load_4d_hint(dst + w * AB, &m4[bi], 0, y + 8 * w, 0, 0, bar, policy);
+            w += na;
+        }
+    }
+    if (whole & 1) {
+        tma_load_3d_hint(dst + w * AB, m1, 0, y + 8 * w, 0, bar, policy);
+        ++w;
+    }
+    if (partial) tma_load_3d_hint(dst + w * AB, m1, 0, y + 8 * w, 0, bar, policy);
+}
+
+// The copies of one K or V tile: key positions [p, p + n_valid) of
+// (sequence b, KV head h) into ceil(n_valid / 8) atoms of AB bytes at dst,
+// completing on `bar`.  Whole atoms go through the 4D boxes (16, 8, 4 or 2
+// atoms: the rows of a run are consecutive cache rows); a single or a
+// partial atom through the 3D one-atom box, whose rows past the cache the
+// TMA zero-fills.  A contiguous cache is one run; a paged cache breaks runs
+// at page ends (pages hold a multiple of 8 rows and its tiles start on an
+// 8-key boundary, so no atom straddles two pages), and the tile's page ids
+// are read from the block table together, before the first copy.
 template <int AB>
 __device__ __forceinline__ void tile_copies(const AttnParams &P, const TcMaps &M, int kv, int b,
                                             int h, int p, int n_valid, uint8_t *dst, uint64_t *bar,
                                             uint64_t policy) {
-    using namespace tc;
     const CUtensorMap *m4 = kv ? M.v_atoms : M.k_atoms;
     const CUtensorMap *m1 = kv ? &M.v_atom : &M.k_atom;
     const int full = n_valid >> 3, natoms = (n_valid + 7) >> 3;
-    int a = 0;
-    while (a < natoms) {
-        const int pos = p + 8 * a;
-        int run = natoms - a;
-        if (P.block_table != nullptr) {
-            const int left = (P.page_size - pos % P.page_size) >> 3;
-            run = run < left ? run : left;
-        }
-        const int y = (int)cache_row(P, b, h, pos);
+    if (P.block_table == nullptr) {
+        atom_run<AB>(m4, m1, (int)cache_row(P, b, h, p), full, natoms > full, dst, bar, policy);
+        return;
+    }
+    constexpr int kMaxRuns = kTcTileKeys / 8 + 1;  // pages of >= 8 rows
+    const int ps = P.page_size, pa = ps >> 3;       // rows, atoms per page
+    const int k0 = p / ps, first = (ps - p % ps) >> 3;  // first page, its atoms
+    const int32_t *trow = P.block_table + (long long)b * P.max_blocks + k0;
+    int pg[kMaxRuns];
+#pragma unroll
+    for (int k = 0; k < kMaxRuns; ++k)
+        if (k == 0 || first + (k - 1) * pa < natoms) pg[k] = __ldg(trow + k);
+#pragma unroll
+    for (int k = 0; k < kMaxRuns; ++k) {
+        const int a = k == 0 ? 0 : first + (k - 1) * pa;  // first atom of run k
+        if (a >= natoms) break;
+        int run = k == 0 ? first : pa;
+        run = run < natoms - a ? run : natoms - a;
         int whole = full - a;
         whole = whole < 0 ? 0 : (whole > run ? run : whole);
-        int w = 0;
-        if (whole == 16) {
-            tma_load_4d_hint(dst + a * AB, &m4[0], 0, y, 0, 0, bar, policy);
-            w = 16;
-        } else {
-#pragma unroll
-            for (int bi = 1; bi < 4; ++bi) {
-                const int na = 16 >> bi;
-                if (whole & na) {
-                    tma_load_4d_hint(dst + (a + w) * AB, &m4[bi], 0, y + 8 * w, 0, 0, bar, policy);
-                    w += na;
-                }
-            }
-            if (whole & 1) {
-                tma_load_3d_hint(dst + (a + w) * AB, m1, 0, y + 8 * w, 0, bar, policy);
-                ++w;
-            }
-        }
-        if (run > whole)  // the tile's last, partial atom
-            tma_load_3d_hint(dst + (a + w) * AB, m1, 0, y + 8 * w, 0, bar, policy);
-        a += run;
+        const int y = (pg[k] * P.Hkv + h) * ps + (k == 0 ? p % ps : 0);
+        atom_run<AB>(m4, m1, y, whole, run > whole, dst + a * AB, bar, policy);
     }
 }
 
