@@ -105,7 +105,12 @@ swa_status swa_verify_attn(const void *q, const void *k_cache, const void *v_cac
  * every KV head, and a sequence's block table lists its pages in position
  * order.  The pages mention a reduced KV cache and the window as its reason
  * ("What each piece does, and why"); a pool lets a server hold only the
- * pages a window still needs. */
+ * pages a window still needs.  A window-sized ring per sequence (position
+ * j kept in slot j mod R) is the same map with a cyclic table: R a multiple
+ * of page_size and at least window + q_len - 1, the ring's R / page_size
+ * pages listed over and over (block k -> ring page k mod (R / page_size)).
+ * Keys outside a row's window are never weighted, so ring slots that newer
+ * positions overwrote do not matter. */
 typedef struct {
     const int32_t *block_table;  /* device int32 [batch, max_blocks], 4-byte aligned: block k of
                                     sequence b (positions k*page_size ..) is page block_table[b][k] */

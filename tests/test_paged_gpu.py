@@ -106,3 +106,43 @@ def test_paged_rejects_bad_tables():
         swa.swa_verify_attn_paged(case.q, kp.view(-1, 2, 12, 256)[:100], vp.view(-1, 2, 12, 256)[:100],
                                   table, case.seq_lens, case.q_pos, case.window, case.scale)
     assert e.value.status == swa.SWA_ERR_INVALID_ARG
+
+
+def ring_pool(case, ring, page_size):
+    """A window-sized ring per sequence, written as a block table: logical
+    row j lives in slot j mod ring, logical page k in ring page k mod
+    (ring / page_size). The ring holds each sequence's most recent `ring`
+    rows; older rows were overwritten, so a read outside the window span
+    picks up the wrong row and fails the parity check."""
+    B, Hkv, L, D = case.k_cache.shape
+    assert ring % page_size == 0 and L % page_size == 0
+    rp = ring // page_size
+    kp = torch.empty((B * rp, Hkv, page_size, D), dtype=torch.bfloat16, device=case.q.device)
+    vp = torch.empty_like(kp)
+    for b, sl in enumerate(case.seq_lens_host):
+        for j in range(max(0, sl - ring), sl):
+            s = j % ring
+            kp[b * rp + s // page_size, :, s % page_size] = case.k_cache[b, :, j]
+            vp[b * rp + s // page_size, :, s % page_size] = case.v_cache[b, :, j]
+    k = torch.arange(L // page_size, dtype=torch.int32) % rp
+    table = (torch.arange(B, dtype=torch.int32)[:, None] * rp + k[None, :]).to(case.q.device)
+    return kp, vp, table
+
+
+@pytest.mark.parametrize("q_len", [8, 64])
+@pytest.mark.parametrize("page_size", [8, 64, 256])
+def test_window_ring_as_block_table(q_len, page_size, kernel):
+    """A cache of 256 slots (>= W + q_len - 1 = 251) serves positions far
+    past its length; spans that wrap the ring cross from its last slot to
+    its first."""
+    from sliding_window_speculative_gb300 import swa_verify_attn_paged
+    window = 188
+    lens = [4096, 4000 + q_len, 1000, 256 + 3, window + q_len - 5, q_len]
+    case = inputs.make_case("ring", len(lens), 8, 2, 256, q_len, window, lens, 4096, seed=23,
+                            outliers=True, device="cuda")
+    kp, vp, table = ring_pool(case, 256, page_size)
+    out, lse = swa_verify_attn_paged(case.q, kp, vp, table, case.seq_lens, case.q_pos,
+                                     case.window, case.scale)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle_reference(case)
+    compare(out, lse, ref_o, ref_l, f"ring 256, page {page_size}, q{q_len}, {kernel}")
