@@ -167,9 +167,10 @@ class Replicas:
     """Copies of a workload's tensors at distinct addresses, so consecutive
     calls read cold data."""
 
-    def __init__(self, case, n):
+    def __init__(self, case, n, append=None):
         self.n = n
         self.case = case
+        self.append = append  # None, "fused" (swa_append_verify_attn) or "torch" (copies + verify)
         B = case.q.shape[0]
         self.q = case.q.unsqueeze(0).repeat(n, 1, 1, 1, 1) if n > 1 else case.q.unsqueeze(0)
         if n > 1:
@@ -184,11 +185,33 @@ class Replicas:
         self.out = torch.empty_like(self.q)
         self.lse = torch.empty((n, B, case.q.shape[1], case.q.shape[2]), dtype=torch.float32,
                                device=case.q.device)
+        if append is not None:
+            # the verify block's rows as the projection would hand them over,
+            # [B, q_len, Hkv, D]; appending them rewrites the same values
+            q_len = case.q.shape[1]
+            Hkv, L, D = case.k_cache.shape[1:]
+            kn = torch.zeros((B, q_len, Hkv, D), dtype=torch.bfloat16, device=case.q.device)
+            vn = torch.zeros_like(kn)
+            for b, qp in enumerate(case.q_pos_host):
+                kn[b] = case.k_cache[b, :, qp:qp + q_len].transpose(0, 1)
+                vn[b] = case.v_cache[b, :, qp:qp + q_len].transpose(0, 1)
+            self.kn = kn.unsqueeze(0).repeat(n, 1, 1, 1, 1)
+            self.vn = vn.unsqueeze(0).repeat(n, 1, 1, 1, 1)
 
     def call(self, i, num_splits=0):
-        from sliding_window_speculative_gb300 import swa_verify_attn
+        from sliding_window_speculative_gb300 import swa_append_verify_attn, swa_verify_attn
         r = i % self.n
         c = self.case
+        if self.append == "fused":
+            swa_append_verify_attn(self.q[r], self.kn[r], self.vn[r], self.k[r], self.v[r],
+                                   c.seq_lens, c.q_pos, c.window, c.scale, out=self.out[r],
+                                   lse=self.lse[r], num_splits=num_splits)
+            return
+        if self.append == "torch":
+            q_len = c.q.shape[1]
+            for b, qp in enumerate(c.q_pos_host):
+                self.k[r][b, :, qp:qp + q_len].copy_(self.kn[r][b].transpose(0, 1))
+                self.v[r][b, :, qp:qp + q_len].copy_(self.vn[r][b].transpose(0, 1))
         swa_verify_attn(self.q[r], self.k[r], self.v[r], c.seq_lens, c.q_pos, c.window, c.scale,
                         out=self.out[r], lse=self.lse[r], num_splits=num_splits)
 
@@ -203,12 +226,12 @@ def replica_count(case, bytes_per_call):
     return n, l2
 
 
-def time_device(case, steps, warmup, num_splits=0, graph_len=1000, dist=None):
+def time_device(case, steps, warmup, num_splits=0, graph_len=1000, dist=None, append=None):
     """Device time of `steps` calls (graph replays), L2 defeated by replicas.
     Returns dict with total seconds and per-call microseconds."""
     kv, total = workload_bytes(case)
     nrep, l2 = replica_count(case, total)
-    rep = Replicas(case, nrep)
+    rep = Replicas(case, nrep, append)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -369,6 +392,26 @@ def time_paged(name, page_size, steps=50, warmup=5, seed=0):
     torch.cuda.empty_cache()
     return {"workload": name, "page_size": page_size, "us_per_call": round(us, 3),
             "achieved_gbs": round(total / (us * 1e-6) / 1e9, 2)}
+
+
+def time_append(name, steps=2000, warmup=5, seed=0):
+    """Fused KV append + verify (swa_append_verify_attn) against the plain
+    verify call on workload `name`; for one sequence also the unfused way
+    (two strided copies into the cache, then the verify call)."""
+    case = make_workload(name, torch.device("cuda"), seed=seed)
+    kv, total = workload_bytes(case)
+    B, q_len, Hq, D = case.q.shape
+    new_bytes = 2 * 2 * B * q_len * case.k_cache.shape[1] * D * 2  # K+V rows read and written
+    plain = time_device(case, steps, warmup)["us_per_call"]
+    fused = time_device(case, steps, warmup, append="fused")["us_per_call"]
+    res = {"workload": name, "verify_us": round(plain, 3), "fused_append_verify_us": round(fused, 3),
+           "fused_achieved_gbs": round((total + new_bytes) / (fused * 1e-6) / 1e9, 2)}
+    if B == 1:
+        unf = time_device(case, steps, warmup, append="torch")["us_per_call"]
+        res["torch_copies_then_verify_us"] = round(unf, 3)
+    del case
+    torch.cuda.empty_cache()
+    return res
 
 
 def time_accept(B, q_len, V, steps=2000, warmup=5, seed=0, graph_len=1000):
@@ -641,6 +684,9 @@ def main():
         line["accept"] = [time_accept(1, 8, 262144), time_accept(64, 8, 262144, steps=500)]
         # the bandwidth-stress batch (inputs larger than L2) on a paged cache
         line["paged"] = [time_paged("stress_w188_q8", 16), time_paged("stress_w188_q8", 64)]
+        # the cache write of the verify block fused into the attention call
+        line["append"] = [time_append("single_stream"), time_append("batched"),
+                          time_append("stress_w188_q8", steps=200)]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb = oracle_sample(case, args.cpu_budget)
         line["cpu_baseline"] = {"value": round(cb["kv_gbs"], 6), "unit": UNIT,

@@ -135,6 +135,31 @@ swa_status swa_verify_attn_paged(const void *q, const void *k_pages, const void 
                                  const int32_t *q_pos, int32_t window, float scale, void *out,
                                  float *lse, const swa_dims *dims, swa_stream_t stream);
 
+/* Fused KV append + verify: the step before the verify (writing the draft
+ * block's freshly projected K/V rows into the cache) done inside the
+ * attention kernels, so one launch both stores the rows and attends over
+ * them.  The pages name no such kernel; it serves the launch trimming they
+ * credit to the single-graph step (ONEGRAPH, "What each piece does, and
+ * why"): one launch fewer per verify step.
+ *   k_new, v_new  bf16 [B, q_len, Hkv, D], device, 16-byte aligned: row i of
+ *                 sequence b is key position q_pos[b] + i
+ *   k_cache, v_cache  writable caches: contiguous [B, Hkv, max_len, D]
+ *                 (paged == NULL) or page pools [num_pages, Hkv, page_size, D]
+ *                 described by *paged (as for swa_verify_attn_paged)
+ * Afterwards every cache row at position q_pos[b] + i < min(seq_lens[b],
+ * max_len) holds row i of k_new / v_new (bit copies); no other cache byte
+ * changes.  out / lse are those of swa_verify_attn on the updated cache.
+ * The same device preconditions hold (q_pos + q_len <= seq_len <= max_len;
+ * with a paged cache the blocks holding the new positions are valid pages);
+ * rows outside [0, min(seq_len, max_len)) are never written.  k_new / v_new
+ * must not overlap the caches, q or out.  Errors as for swa_verify_attn,
+ * plus SWA_ERR_INVALID_ARG for a NULL or misaligned k_new / v_new. */
+swa_status swa_append_verify_attn(const void *q, const void *k_new, const void *v_new,
+                                  void *k_cache, void *v_cache, const swa_paged *paged,
+                                  const int32_t *seq_lens, const int32_t *q_pos, int32_t window,
+                                  float scale, void *out, float *lse, const swa_dims *dims,
+                                  swa_stream_t stream);
+
 /* Upper bound, in bytes, of the split-partial workspace any call with these
  * dims and window may need on any device (pure host arithmetic; 0 if the
  * arguments are invalid).  Layout: fp32 acc [B, Hkv, splits, R, D] followed

@@ -41,6 +41,8 @@ def _bind(path):
     lib.oracle_lse_merge.restype = ctypes.c_int
     lib.oracle_greedy_accept.argtypes = [dp, ip, ip, i64, i64, i64, ip, ip]
     lib.oracle_greedy_accept.restype = ctypes.c_int
+    lib.oracle_append_rows.argtypes = [dp, dp, ip, ip, i64, i64, i64, i64, i64]
+    lib.oracle_append_rows.restype = ctypes.c_int
     return lib
 
 
@@ -167,3 +169,24 @@ def greedy_accept(logits, draft, keep=None):
                                       _ip(draft), B, q_len, V, _ip(argmax), _ip(accepted))
     _check(rc, "greedy_accept")
     return argmax, accepted
+
+
+def append_rows(cache, rows, q_pos, seq_lens):
+    """The cache after a verify block's new rows are written.
+
+    cache [B, Hkv, L, D], rows [B, q_len, Hkv, D] (widened to float64),
+    q_pos / seq_lens [B].  Returns a new float64 cache in which position
+    q_pos[b] + i of every KV head holds rows[b, i] wherever
+    0 <= q_pos[b] + i < min(seq_lens[b], L); the input is not modified.
+    """
+    out = np.array(cache, dtype=np.float64, order="C", copy=True)
+    rows = _f64(rows)
+    B, Hkv, L, D = out.shape
+    if rows.ndim != 4 or rows.shape[0] != B or rows.shape[2:] != (Hkv, D):
+        raise ValueError("rows must be [B, q_len, Hkv, D] matching the cache")
+    q_len = rows.shape[1]
+    q_pos, seq_lens = _i64(q_pos), _i64(seq_lens)
+    rc = _load().oracle_append_rows(_dp(out), _dp(rows), _ip(q_pos), _ip(seq_lens), B, q_len,
+                                    Hkv, L, D)
+    _check(rc, "append_rows")
+    return out

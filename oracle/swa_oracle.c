@@ -284,3 +284,30 @@ int oracle_greedy_accept(const double *logits, const int64_t *keep, const int64_
     }
     return 0;
 }
+
+/* Cache write of a verify block's new rows (the step before the attention,
+ * done in the same call by the fused append): row i of sequence b's block
+ * holds the key / value of position q_pos[b] + i, so for every KV head h
+ *   cache[b][h][q_pos[b] + i][:] = rows[b][i][h][:]
+ * for each i with 0 <= q_pos[b] + i < min(seq_len[b], L); no other cache
+ * entry changes.  In place on `cache`.
+ * Layouts: cache [B, Hkv, L, D]; rows [B, q_len, Hkv, D]. */
+int oracle_append_rows(double *cache, const double *rows, const int64_t *q_pos,
+                       const int64_t *seq_lens, int64_t B, int64_t q_len, int64_t Hkv,
+                       int64_t L, int64_t D)
+{
+    if (B < 0 || q_len < 1 || Hkv < 1 || L < 1 || D < 1) return 1;
+    for (int64_t b = 0; b < B; ++b) {
+        const int64_t end = seq_lens[b] < L ? seq_lens[b] : L;
+        for (int64_t i = 0; i < q_len; ++i) {
+            const int64_t pos = q_pos[b] + i;
+            if (pos < 0 || pos >= end) continue;
+            for (int64_t h = 0; h < Hkv; ++h) {
+                const double *src = rows + ((b * q_len + i) * Hkv + h) * D;
+                double *dst = cache + ((b * Hkv + h) * L + pos) * D;
+                for (int64_t d = 0; d < D; ++d) dst[d] = src[d];
+            }
+        }
+    }
+    return 0;
+}

@@ -77,6 +77,10 @@ def load_library(path=LIB_PATH):
     lib.swa_verify_attn_paged.argtypes = [vp, vp, vp, ctypes.POINTER(SwaPaged), vp, vp, i32,
                                           ctypes.c_float, vp, vp, ctypes.POINTER(SwaDims), vp]
     lib.swa_verify_attn_paged.restype = ctypes.c_int
+    lib.swa_append_verify_attn.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(SwaPaged), vp, vp,
+                                           i32, ctypes.c_float, vp, vp, ctypes.POINTER(SwaDims),
+                                           vp]
+    lib.swa_append_verify_attn.restype = ctypes.c_int
     lib.swa_greedy_accept.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp]
     lib.swa_greedy_accept.restype = ctypes.c_int
     _lib = lib
@@ -130,6 +134,56 @@ def swa_verify_attn_paged(q, k_pages, v_pages, block_table, seq_lens, q_pos, win
     handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     _check(lib.swa_verify_attn_paged(pq, pk, pv, ctypes.byref(paged), ps, pp, int(window),
                                      float(scale), po, pl, ctypes.byref(dims), handle))
+    return out, lse
+
+
+def swa_append_verify_attn(q, k_new, v_new, k_cache, v_cache, seq_lens, q_pos, window, scale,
+                           block_table=None, out=None, lse=None, num_splits=0, stream=None):
+    """Fused KV append + windowed verify attention (C entry point
+    swa_append_verify_attn): writes k_new / v_new bf16 [B, q_len, Hkv, D]
+    into the cache at positions q_pos + i, then attends over the updated
+    cache.  Without block_table the caches are [B, Hkv, max_len, D]; with it
+    they are page pools [num_pages, Hkv, page_size, D] as in
+    swa_verify_attn_paged.  The caches are modified in place.
+    """
+    lib = load_library()
+    B, q_len, Hq, D = q.shape
+    pq = _dev_tensor(q, "q", torch.bfloat16, 4)
+    pkn = _dev_tensor(k_new, "k_new", torch.bfloat16, 4)
+    pvn = _dev_tensor(v_new, "v_new", torch.bfloat16, 4)
+    pk = _dev_tensor(k_cache, "k_cache", torch.bfloat16, 4)
+    pv = _dev_tensor(v_cache, "v_cache", torch.bfloat16, 4)
+    Hkv = k_cache.shape[1]
+    if v_cache.shape != k_cache.shape or k_cache.shape[3] != D:
+        raise ValueError("k_cache / v_cache shapes do not match each other or q")
+    if k_new.shape != (B, q_len, Hkv, D) or v_new.shape != k_new.shape:
+        raise ValueError("k_new / v_new must be [B, q_len, Hkv, D] = %s" % ((B, q_len, Hkv, D),))
+    ps = _dev_tensor(seq_lens, "seq_lens", torch.int32, 1)
+    pp = _dev_tensor(q_pos, "q_pos", torch.int32, 1)
+    if out is None:
+        out = torch.empty_like(q)
+    po = _dev_tensor(out, "out", torch.bfloat16, 4)
+    if lse is None:
+        lse = torch.empty((B, q_len, Hq), dtype=torch.float32, device=q.device)
+    pl = _dev_tensor(lse, "lse", torch.float32, 3)
+    paged = None
+    if block_table is not None:
+        pt = _dev_tensor(block_table, "block_table", torch.int32, 2)
+        if block_table.shape[0] != B:
+            raise ValueError("block_table needs one row per sequence")
+        num_pages, page_size = k_cache.shape[0], k_cache.shape[2]
+        paged = SwaPaged(pt, block_table.shape[1], page_size, num_pages)
+        max_len = block_table.shape[1] * page_size
+    else:
+        max_len = k_cache.shape[2]
+    dims = make_dims(B, q_len, Hq, Hkv, D, max_len, num_splits)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    _check(lib.swa_append_verify_attn(pq, pkn, pvn, pk, pv,
+                                      ctypes.byref(paged) if paged is not None else None, ps, pp,
+                                      int(window), float(scale), po, pl, ctypes.byref(dims),
+                                      handle))
     return out, lse
 
 

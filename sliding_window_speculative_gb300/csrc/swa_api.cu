@@ -358,16 +358,43 @@ int device_sms(int dev) {
     return cache[dev];
 }
 
+// Host checks of a paged cache description against dims.
+swa_status check_paged(const swa_paged *paged, const swa_dims *dims) {
+    if (paged == nullptr || paged->block_table == nullptr)
+        return fail(SWA_ERR_INVALID_ARG, "paged cache description or its block table is NULL");
+    if (reinterpret_cast<uintptr_t>(paged->block_table) & 3u)
+        return fail(SWA_ERR_INVALID_ARG, "block_table must be 4-byte aligned");
+    if (paged->page_size < 8 || paged->page_size % 8 != 0)
+        return fail(SWA_ERR_INVALID_ARG, "page_size %d is not a positive multiple of 8",
+                    paged->page_size);
+    if (paged->max_blocks < 1 || paged->num_pages < 1)
+        return fail(SWA_ERR_INVALID_ARG, "max_blocks %d and num_pages %d must be >= 1",
+                    paged->max_blocks, paged->num_pages);
+    if (dims != nullptr && (long long)dims->max_len != (long long)paged->max_blocks * paged->page_size)
+        return fail(SWA_ERR_INVALID_ARG, "dims->max_len %d != max_blocks * page_size = %lld",
+                    dims->max_len, (long long)paged->max_blocks * paged->page_size);
+    if (dims != nullptr &&
+        (long long)paged->num_pages * dims->num_kv_heads * paged->page_size >= (1LL << 31))
+        return fail(SWA_ERR_UNSUPPORTED, "the page pool holds 2^31 or more rows");
+    return SWA_OK;
+}
+
 // The windowed verify attention of swa_verify_attn, on a contiguous cache
-// (paged == NULL) or a paged one.
+// (paged == NULL) or a paged one; with k_new / v_new non-NULL the kernels
+// first write the new rows into the cache (swa_append_verify_attn).
 swa_status verify_impl(const void *q, const void *k_cache, const void *v_cache,
                        const int32_t *seq_lens, const int32_t *q_pos, int32_t window, float scale,
                        void *out, float *lse, const swa_dims *dims, swa_stream_t stream,
-                       const swa_paged *paged) {
+                       const swa_paged *paged, const void *k_new = nullptr,
+                       const void *v_new = nullptr) {
     swa_status st = validate_dims(dims, window);
     if (st != SWA_OK) return st;
     if (!q || !k_cache || !v_cache || !seq_lens || !q_pos || !out)
         return fail(SWA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if ((k_new == nullptr) != (v_new == nullptr))
+        return fail(SWA_ERR_INVALID_ARG, "k_new and v_new must both be given");
+    if ((k_new && !aligned16(k_new)) || (v_new && !aligned16(v_new)))
+        return fail(SWA_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return fail(SWA_ERR_INVALID_ARG, "q, the K and V caches and out must be 16-byte aligned");
     if ((reinterpret_cast<uintptr_t>(seq_lens) & 3u) || (reinterpret_cast<uintptr_t>(q_pos) & 3u) ||
@@ -406,6 +433,8 @@ swa_status verify_impl(const void *q, const void *k_cache, const void *v_cache,
     P.rows_per_tile = pl.rows_per_tile;
     P.qk_scale = scale * swa::kLog2e;
     P.fault = fault;
+    P.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    P.v_new = static_cast<const __nv_bfloat16 *>(v_new);
     long long cache_rows = (long long)P.B * P.Hkv * P.L;
     if (paged != nullptr) {
         P.block_table = paged->block_table;
@@ -444,24 +473,25 @@ swa_status swa_verify_attn_paged(const void *q, const void *k_pages, const void 
                                  const swa_paged *paged, const int32_t *seq_lens,
                                  const int32_t *q_pos, int32_t window, float scale, void *out,
                                  float *lse, const swa_dims *dims, swa_stream_t stream) {
-    if (paged == nullptr || paged->block_table == nullptr)
-        return fail(SWA_ERR_INVALID_ARG, "paged cache description or its block table is NULL");
-    if (reinterpret_cast<uintptr_t>(paged->block_table) & 3u)
-        return fail(SWA_ERR_INVALID_ARG, "block_table must be 4-byte aligned");
-    if (paged->page_size < 8 || paged->page_size % 8 != 0)
-        return fail(SWA_ERR_INVALID_ARG, "page_size %d is not a positive multiple of 8",
-                    paged->page_size);
-    if (paged->max_blocks < 1 || paged->num_pages < 1)
-        return fail(SWA_ERR_INVALID_ARG, "max_blocks %d and num_pages %d must be >= 1",
-                    paged->max_blocks, paged->num_pages);
-    if (dims != nullptr && (long long)dims->max_len != (long long)paged->max_blocks * paged->page_size)
-        return fail(SWA_ERR_INVALID_ARG, "dims->max_len %d != max_blocks * page_size = %lld",
-                    dims->max_len, (long long)paged->max_blocks * paged->page_size);
-    if (dims != nullptr &&
-        (long long)paged->num_pages * dims->num_kv_heads * paged->page_size >= (1LL << 31))
-        return fail(SWA_ERR_UNSUPPORTED, "the page pool holds 2^31 or more rows");
+    const swa_status st = check_paged(paged, dims);
+    if (st != SWA_OK) return st;
     return verify_impl(q, k_pages, v_pages, seq_lens, q_pos, window, scale, out, lse, dims, stream,
                        paged);
+}
+
+swa_status swa_append_verify_attn(const void *q, const void *k_new, const void *v_new,
+                                  void *k_cache, void *v_cache, const swa_paged *paged,
+                                  const int32_t *seq_lens, const int32_t *q_pos, int32_t window,
+                                  float scale, void *out, float *lse, const swa_dims *dims,
+                                  swa_stream_t stream) {
+    if (k_new == nullptr || v_new == nullptr)
+        return fail(SWA_ERR_INVALID_ARG, "k_new and v_new must not be NULL");
+    if (paged != nullptr) {
+        const swa_status st = check_paged(paged, dims);
+        if (st != SWA_OK) return st;
+    }
+    return verify_impl(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out, lse, dims, stream,
+                       paged, k_new, v_new);
 }
 
 size_t swa_workspace_bytes(const swa_dims *dims, int32_t window) {

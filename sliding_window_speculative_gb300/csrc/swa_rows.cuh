@@ -24,13 +24,15 @@
 // ring slots, atoms of [slab][8 rows][128 B]); K is the B operand of the
 // score MMA (K-major), V the B operand of the PV MMAs (MN-major, N = D).
 //
-// Warp roles (320 threads):
+// Warp roles (320 threads, 352 under a fused append):
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM owner and MMA issuer (one lane)
 //   warps 2..9  softmax / epilogue; warp w owns TMEM lanes 32 (w % 4)..,
 //               i.e. packed rows 32 (w % 4).., and key half (w - 2) / 4 of
 //               every tile (head-dim half of the output); quadrants without
 //               rows idle.
+//   warp 10     fused append only (the kernel's AP variant): mixed atoms of a
+//               paged cache, and the new rows' cache stores
 //
 // TMEM: S/P buffers at columns 0 and 128, O at 256 (two O buffers at head
 // dim 128).  Every wait is bounded; a wait that gives up sets the fault
@@ -41,7 +43,7 @@
 
 namespace swa {
 
-constexpr int kRowsThreads = 320;
+constexpr int kRowsThreads = 320;  // and one append warp more under a fused append
 
 template <int D, int QR, int NT, int QB>
 struct RowsCfg {
@@ -65,11 +67,11 @@ struct RowsCfg {
     static constexpr int BAR_OFF = STG_OFF + (STAGE ? STG_NEED : 0);
     static constexpr int OB = D == 128 ? 2 : 1;      // O buffers in TMEM
     // ring full/empty [NT], q full/empty [QB], s full [2], s free [2],
-    // p full [2], pv done [2], o free [OB], drain
+    // p full [2], pv done [2], o free [OB], drain, mixed atom of a fused append [NT]
     static constexpr int B_FULL = 0, B_EMPTY = NT, B_QFULL = 2 * NT, B_QEMPTY = B_QFULL + QB,
                          B_SFULL = B_QEMPTY + QB, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2,
                          B_PVDONE = B_PFULL + 2, B_OFREE = B_PVDONE + 2, B_DRAIN = B_OFREE + OB,
-                         NBARS = B_DRAIN + 1;
+                         B_MIX = B_DRAIN + 1, NBARS = B_MIX + NT;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base
     static constexpr int END = MISC_OFF + 16;
     static constexpr int SMEM_BYTES = END + 1024;  // slack for 1024-byte alignment
@@ -84,10 +86,11 @@ struct RowsCfg {
     static_assert(STG_OFF % 16 == 0 && BAR_OFF % 8 == 0 && META_OFF % 8 == 0, "alignment");
 };
 
-template <int D, int QR, int NT, int QB>
-__global__ void __launch_bounds__(kRowsThreads, 1)
+template <int D, int QR, int NT, int QB, bool AP>
+__global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
     swa_rows_kernel(const __grid_constant__ TcParams T, const __grid_constant__ TcMaps M) {
     using C = RowsCfg<D, QR, NT, QB>;
+    constexpr int NTHR = AP ? kRowsThreads + 32 : kRowsThreads;
     using namespace tc;
     constexpr int SLABS = C::SLABS;
     constexpr int OB = C::OB;
@@ -111,18 +114,22 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
     const uint32_t n_act = 32u * (uint32_t)act_q;
 
     // ---------------------------------------------------------------- setup
-    if (warp == 0 && lane < 11) {
+    if (warp == 0 && lane < (AP ? 13 : 11)) {
         const CUtensorMap *mp = lane < 4    ? &M.k_atoms[lane]
                                 : lane < 8  ? &M.v_atoms[lane - 4]
                                 : lane == 8 ? &M.k_atom
                                 : lane == 9 ? &M.v_atom
-                                            : &M.q;
+                                : lane == 10 ? &M.q
+                                : lane == 11 ? &M.kn_atom
+                                             : &M.vn_atom;
         prefetch_tmap(mp);
     }
     if (tid == 0) {
         for (int i = 0; i < NT; ++i) {
-            mbar_init(&bars[C::B_FULL + i], 1);
+            // under a fused append a fill takes a second arrival
+            mbar_init(&bars[C::B_FULL + i], AP ? 2 : 1);
             mbar_init(&bars[C::B_EMPTY + i], 1);
+            mbar_init(&bars[C::B_MIX + i], 1);
         }
         for (int i = 0; i < QB; ++i) {
             mbar_init(&bars[C::B_QFULL + i], 1);
@@ -138,16 +145,16 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
         mbar_init(&bars[C::B_DRAIN], 1);
         fence_barrier_init();
     }
-    for (int i = tid; i < kFillTab; i += kRowsThreads) ftab[i] = 0xffffffffu;
+    for (int i = tid; i < kFillTab; i += NTHR) ftab[i] = 0xffffffffu;
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
     grid_dep_wait();
     grid_dep_trigger();
-    for (int j = tid; j < kTcMetaItems; j += kRowsThreads) {
+    for (int j = tid; j < kTcMetaItems; j += NTHR) {
         const long long item = (long long)blockIdx.x + (long long)j * gridDim.x;
-        if (item < T.items) meta[j] = tc_decode_global(T, (int)item);
+        if (item < T.items) meta[j] = tc_decode_global<AP>(T, (int)item);
     }
     fence_before_sync();
     __syncthreads();
@@ -156,84 +163,8 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
 
     if (warp == 0) {
         // ======================================================= producer
-        if (lane == 0) {
-            const uint64_t policy = l2_policy_evict_first();
-            uint32_t f = 0, k = 0;  // fills (two per tile: K then V), items with keys
-            uint32_t uses[NT];      // fills handed to each slot so far
-#pragma unroll
-            for (int s2 = 0; s2 < NT; ++s2) uses[s2] = 0;
-            bool ok = true;
-            int j = 0;
-            for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
-                const TcItem it = tc_decode(T, item, j, meta);
-                if (it.n_tiles == 0) continue;
-                const uint32_t qb = k % QB, quse = k / QB;
-                // Q of the item (its rows x 64 dims per slab), issued after the
-                // item's first K tile
-                auto load_q = [&]() -> bool {
-                    if (!mbar_wait_bounded(&bars[C::B_QEMPTY + qb], (quse & 1) ^ 1, P.fault,
-                                           kFaultCopyTimeout))
-                        return false;
-                    mbar_arrive_expect_tx(&bars[C::B_QFULL + qb], SLABS * T.rows_per_tile * 128);
-                    for (int s = 0; s < SLABS; ++s)
-                        tma_load_3d(qs + qb * C::Q_BUF + s * C::Q_SLAB, &M.q, 64 * s,
-                                    it.h * P.G, it.b * P.q_len + it.i0, &bars[C::B_QFULL + qb]);
-                    return true;
-                };
-                ++k;
-                for (int t = 0; t < it.n_tiles && ok; ++t) {
-                    const int p = it.t0 + kTcTileKeys * t;
-                    const int n_valid = min(kTcTileKeys, it.cr.c_hi - p);
-                    for (int kv = 0; kv < 2 && ok; ++kv) {
-                        if (t == 0 && kv == 1) {
-                            ok = load_q();
-                            if (!ok) break;
-                        }
-                        // the first free slot: never used, or its last fill consumed
-                        int slot = -1;
-                        uint32_t par = 0;
-                        const long long w0 = clock64();
-                        for (int spin = 0;; ++spin) {
-#pragma unroll
-                            for (int s2 = 0; s2 < NT; ++s2) {
-                                if (slot < 0 && (uses[s2] == 0 ||
-                                                 mbar_test(&bars[C::B_EMPTY + s2], (uses[s2] - 1) & 1))) {
-                                    slot = s2;
-                                    par = uses[s2] & 1;
-                                    ++uses[s2];
-                                }
-                            }
-                            if (slot >= 0) break;
-                            if (clock64() - w0 > kWaitLimitCycles) {
-                                atomicOr(P.fault, kFaultCopyTimeout);
-                                ok = false;
-                                break;
-                            }
-                            if (spin > 8) __nanosleep(32);
-                        }
-                        if (!ok) break;
-                        ftab[f % kFillTab] = (f << 8) | (par << 4) | (uint32_t)slot;
-                        uint64_t *bar = &bars[C::B_FULL + slot];
-                        mbar_arrive_expect_tx(bar, (uint32_t)((n_valid + 7) >> 3) * C::ATOM_BYTES);
-                        tile_copies<C::ATOM_BYTES>(P, M, kv, it.b, it.h, p, n_valid,
-                                                   ring + slot * C::TILE_BYTES, bar, policy);
-                        ++f;
-                    }
-                }
-            }
-            // every copy this CTA issued has landed before it exits
-#pragma unroll
-            for (int s2 = 0; s2 < NT; ++s2)
-                if (uses[s2] > 0)
-                    mbar_wait_bounded(&bars[C::B_FULL + s2], (uses[s2] - 1) & 1, P.fault,
-                                      kFaultCopyTimeout);
-            const uint32_t nq = k < (uint32_t)QB ? k : (uint32_t)QB;
-            for (uint32_t q = 0; q < nq; ++q) {
-                const uint32_t kq = k - 1 - q;
-                mbar_wait_bounded(&bars[C::B_QFULL + kq % QB], (kq / QB) & 1, P.fault,
-                                  kFaultCopyTimeout);
-            }
-        }
+        if (lane == 0)
+            tile_producer<C, NT, QB, AP>(T, M, meta, ftab, ring, qs, bars);
     } else if (warp == 1) {
         // ============================================================ MMA
         // Two cursors over the tile sequence: S = Q K^T of the next tile and
@@ -265,7 +196,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
             };
             auto seek = [&](Cursor &c) {
                 for (; c.item < T.items; c.item += gridDim.x, ++c.j) {
-                    const TcItem it = tc_decode(T, c.item, c.j, meta);
+                    const TcItem it = tc_decode<AP>(T, c.item, c.j, meta);
                     if (it.n_tiles > 0) {
                         c.n_tiles = it.n_tiles;
                         c.last_keys = it.cr.c_hi - it.t0 - kTcTileKeys * (it.n_tiles - 1);
@@ -418,7 +349,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
             }
             __syncwarp();
         }
-    } else {
+    } else if (warp < 10) {
         // ===================================================== softmax
         const int quad = warp & 3;        // TMEM lane quadrant = packed rows 32 quad ..
         const int half = (warp - 2) >> 2;  // key half of each tile, head-dim half of O
@@ -438,7 +369,7 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
             bool ok = true;
             int j = 0;
             for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
-                const TcItem it = tc_decode(T, item, j, meta);
+                const TcItem it = tc_decode<AP>(T, item, j, meta);
                 const bool live = r < it.rows;
                 const int rg = it.row0 + r;  // packed row of the (sequence, KV head)
                 const int i = rg / P.G, gg = rg - i * P.G;
@@ -687,6 +618,9 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
             }
             (void)ok;
         }
+    } else if constexpr (AP) {
+        // ================================================= append worker
+        append_worker<C, D>(T, meta, ftab, ring, bars);
     }
 
     // ---------------------------------------------------------- teardown
@@ -694,6 +628,9 @@ __global__ void __launch_bounds__(kRowsThreads, 1)
     __syncthreads();
     fence_after_sync();
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+    if constexpr (AP) {
+        if (T.items > 2 * (int)gridDim.x) append_flush<D>(T, meta, ring, NT * C::TILE_BYTES, NTHR);
+    }
 }
 
 }  // namespace swa

@@ -40,6 +40,11 @@ struct AttnParams {
     // and key position j of sequence b lives in page block_table[b][j / page_size]
     const int32_t *block_table;  // [B, max_blocks]
     int page_size, max_blocks;
+    // fused append (k_new non-null): the q_len new rows [B, q_len, Hkv, D] of
+    // every KV head, key positions q_pos + i, are attended from here and
+    // stored to the cache; k / v then point at writable caches
+    const __nv_bfloat16 *k_new;
+    const __nv_bfloat16 *v_new;
     int B, q_len, Hq, Hkv, G, L, window, R;
     int splits, chunk, row_tiles, rows_per_tile;
     float qk_scale;   // scale * log2(e)
@@ -85,6 +90,19 @@ __device__ __forceinline__ long long cache_row(const AttnParams &P, int b, int h
     if (P.block_table == nullptr) return ((long long)b * P.Hkv + h) * P.L + j;
     const int page = P.block_table[(long long)b * P.max_blocks + j / P.page_size];
     return ((long long)page * P.Hkv + h) * P.page_size + (j % P.page_size);
+}
+
+// Key positions [lo, hi) of a chunk that come from the fused append's new
+// rows (positions q_pos ..) rather than the cache; empty without an append.
+// The kernels load those rows into shared memory straight from k_new / v_new
+// and store them to the cache from there: no kernel reads a new row back
+// from the cache, so the stores need no ordering against the tile loads
+// (several CTAs, the row tiles of one chunk, store the same bytes).
+__device__ __forceinline__ void append_range(const AttnParams &P, const ChunkRange &cr, int &lo,
+                                             int &hi) {
+    lo = cr.c_lo > cr.qp ? cr.c_lo : cr.qp;
+    hi = P.k_new != nullptr ? cr.c_hi : lo;
+    if (hi < lo) hi = lo;
 }
 
 template <int D>
@@ -170,12 +188,8 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
     const int n_tiles = n_keys > 0 ? (n_keys + kSimtTileKeys - 1) / kSimtTileKeys : 0;
 
 
-    if (tid == 0) {
-        for (int s = 0; s < C::STAGES; ++s) mbar_init(&full[s], 1);
-        fence_barrier_init();
-    }
-    __syncthreads();
-
+    int ap_lo, ap_hi;
+    append_range(P, cr, ap_lo, ap_hi);
     auto issue = [&](int t) {
         const int s = t % C::STAGES;
         const int j0 = cr.c_lo + t * kSimtTileKeys;
@@ -184,20 +198,34 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
         uint8_t *dst = ring + s * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&full[s], 2 * bytes);
         // one copy per run of rows contiguous in the cache (a page's rows, or
-        // the whole tile of a contiguous cache)
+        // the whole tile of a contiguous cache); a new row of a fused append
+        // is one copy from k_new / v_new
         for (int j = j0; j < j0 + n;) {
-            int run = j0 + n - j;
+            const uint32_t off = (uint32_t)(j - j0) * D * 2;
+            if (j >= ap_lo && j < ap_hi) {
+                const size_t src = (((size_t)b * P.q_len + (j - cr.qp)) * P.Hkv + h) * D;
+                bulk_copy_g2s(dst + off, P.k_new + src, D * 2, &full[s]);
+                bulk_copy_g2s(dst + C::TILE_BYTES + off, P.v_new + src, D * 2, &full[s]);
+                ++j;
+                continue;
+            }
+            int run = (ap_lo < ap_hi && j < ap_lo && ap_lo < j0 + n ? ap_lo : j0 + n) - j;
             if (P.block_table != nullptr) {
                 const int left = P.page_size - j % P.page_size;
                 run = run < left ? run : left;
             }
             const size_t row = (size_t)cache_row(P, b, h, j);
-            const uint32_t rb = (uint32_t)run * D * 2, off = (uint32_t)(j - j0) * D * 2;
+            const uint32_t rb = (uint32_t)run * D * 2;
             bulk_copy_g2s(dst + off, P.k + row * D, rb, &full[s]);
             bulk_copy_g2s(dst + C::TILE_BYTES + off, P.v + row * D, rb, &full[s]);
             j += run;
         }
     };
+    if (tid == 0) {
+        for (int s = 0; s < C::STAGES; ++s) mbar_init(&full[s], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
     if (tid == 0) {
         for (int t = 0; t < C::STAGES - 1 && t < n_tiles; ++t) issue(t);
     }
@@ -252,6 +280,19 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
         const __nv_bfloat16 *Vs = Ks + kSimtTileKeys * D;
         const int j0 = cr.c_lo + t * kSimtTileKeys;
         const int n = min(kSimtTileKeys, cr.c_hi - j0);
+        if (rt == 0) {
+            // the fused append's new rows of this tile, from the stage to the
+            // cache (row tile 0 only: the others would store the same bytes)
+            const int r0 = max(ap_lo, j0) - j0, r1 = min(ap_hi, j0 + n) - j0;
+            constexpr int PR = D / 8;
+            for (int e = tid; e < 2 * (r1 - r0) * PR; e += kSimtThreads) {
+                const int kv = e >= (r1 - r0) * PR, rest = e - kv * (r1 - r0) * PR;
+                const int r = r0 + rest / PR, c = rest % PR;
+                const uint4 w = *reinterpret_cast<const uint4 *>((kv ? Vs : Ks) + (size_t)r * D + c * 8);
+                __nv_bfloat16 *cache = const_cast<__nv_bfloat16 *>(kv ? P.v : P.k);
+                *reinterpret_cast<uint4 *>(cache + cache_row(P, b, h, j0 + r) * D + c * 8) = w;
+            }
+        }
         const int kb0 = kg * C::KB;
 
         // scores of this warp's key block: one finished (key, row) per lane per group

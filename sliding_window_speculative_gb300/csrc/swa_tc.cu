@@ -44,11 +44,11 @@ bool load_encode() {
     return g_encode != nullptr;
 }
 
-template <int D, int N>
-cudaError_t launch(const TcLaunch &L, const TcMaps &maps, cudaStream_t stream) {
+template <int D, int N, bool AP>
+cudaError_t launch_ap(const TcLaunch &L, const TcMaps &maps, cudaStream_t stream) {
     using Cf = Conf<D, N>;
     using C = typename Cf::C;
-    auto kern = swa_tc_kernel<D, N, Cf::NT, Cf::QB, Cf::PB, Cf::OB>;
+    auto kern = swa_tc_kernel<D, N, Cf::NT, Cf::QB, Cf::PB, Cf::OB, AP>;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -58,7 +58,15 @@ cudaError_t launch(const TcLaunch &L, const TcMaps &maps, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    return launch_kernel(kern, dim3(L.grid), dim3(kTcThreads), C::SMEM_BYTES, stream, L.T, maps);
+    return launch_kernel(kern, dim3(L.grid), dim3(AP ? kTcThreads + 32 : kTcThreads),
+                         C::SMEM_BYTES, stream, L.T, maps);
+}
+
+// The plain kernel, or (fused append) its variant with the append warp.
+template <int D, int N>
+cudaError_t launch(const TcLaunch &L, const TcMaps &maps, cudaStream_t stream) {
+    return L.T.a.k_new != nullptr ? launch_ap<D, N, true>(L, maps, stream)
+                                  : launch_ap<D, N, false>(L, maps, stream);
 }
 
 // Rows-major kernel: per (head_dim, Q rows) the ring tiles and Q buffers
@@ -70,11 +78,11 @@ struct RowsConf {
     using C = RowsCfg<D, QR, NT, QB>;
 };
 
-template <int D, int QR>
-cudaError_t launch_rows(const TcLaunch &L, const TcMaps &maps, cudaStream_t stream) {
+template <int D, int QR, bool AP>
+cudaError_t launch_rows_ap(const TcLaunch &L, const TcMaps &maps, cudaStream_t stream) {
     using Cf = RowsConf<D, QR>;
     using C = typename Cf::C;
-    auto kern = swa_rows_kernel<D, QR, Cf::NT, Cf::QB>;
+    auto kern = swa_rows_kernel<D, QR, Cf::NT, Cf::QB, AP>;
     static bool attr_done[64] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -84,7 +92,14 @@ cudaError_t launch_rows(const TcLaunch &L, const TcMaps &maps, cudaStream_t stre
         if (e != cudaSuccess) return e;
         attr_done[dev] = true;
     }
-    return launch_kernel(kern, dim3(L.grid), dim3(kRowsThreads), C::SMEM_BYTES, stream, L.T, maps);
+    return launch_kernel(kern, dim3(L.grid), dim3(AP ? kRowsThreads + 32 : kRowsThreads),
+                         C::SMEM_BYTES, stream, L.T, maps);
+}
+
+template <int D, int QR>
+cudaError_t launch_rows(const TcLaunch &L, const TcMaps &maps, cudaStream_t stream) {
+    return L.T.a.k_new != nullptr ? launch_rows_ap<D, QR, true>(L, maps, stream)
+                                  : launch_rows_ap<D, QR, false>(L, maps, stream);
 }
 
 template <int D>
@@ -148,7 +163,7 @@ cudaError_t tc_launch(const TcLaunch &L, cudaStream_t stream, char *err, size_t 
     // 128 and 8*D*2 bytes) with boxes of 16, 8, 4 and 2 atoms, and a 3D
     // one-atom map (x, y, z) whose rows are bounds-checked one by one.
     // Both land as [atom][slab][8 rows][128 bytes], 128-byte swizzled.
-    TcMaps maps;
+    TcMaps maps{};
     const cuuint64_t rows = (cuuint64_t)L.cache_rows;
     const cuuint32_t slabs = (cuuint32_t)(D / 64);
     for (int kv = 0; kv < 2; ++kv) {
@@ -186,6 +201,27 @@ cudaError_t tc_launch(const TcLaunch &L, cudaStream_t stream, char *err, size_t 
         if (r != CUDA_SUCCESS) {
             snprintf(err, errlen, "cuTensorMapEncodeTiled(q) failed: %d", (int)r);
             return cudaErrorInvalidValue;
+        }
+    }
+    if (P.k_new != nullptr) {
+        for (int kv = 0; kv < 2; ++kv) {
+            cuuint64_t dims[5] = {64, (cuuint64_t)P.q_len, slabs, (cuuint64_t)P.Hkv,
+                                  (cuuint64_t)P.B};
+            cuuint64_t strides[4] = {(cuuint64_t)P.Hkv * D * 2, 128, (cuuint64_t)D * 2,
+                                     (cuuint64_t)P.q_len * P.Hkv * D * 2};
+            cuuint32_t box[5] = {64, 8, slabs, 1, 1};
+            cuuint32_t es[5] = {1, 1, 1, 1, 1};
+            CUresult r = g_encode(kv ? &maps.vn_atom : &maps.kn_atom,
+                                  CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
+                                  const_cast<__nv_bfloat16 *>(kv ? P.v_new : P.k_new), dims,
+                                  strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) {
+                snprintf(err, errlen, "cuTensorMapEncodeTiled(%s new rows) failed: %d",
+                         kv ? "V" : "K", (int)r);
+                return cudaErrorInvalidValue;
+            }
         }
     }
     if (L.rows_major) {

@@ -31,13 +31,15 @@
 // tile's PV, and the epilogue of one item runs while the next item's loads
 // and scores proceed.
 //
-// Warp roles (320 threads):
+// Warp roles (320 threads, 352 under a fused append):
 //   warp 0      TMA producer (one lane)
 //   warp 1      TMEM owner and MMA issuer (one lane)
 //   warps 2..9  softmax / correction / epilogue in two warpgroups that split
 //               the packed rows in halves; within a group a thread owns one
 //               TMEM lane: one key of the S^T tile and one head-dim row of
 //               the O^T accumulator (warps w and w + 4 read the same lanes).
+//   warp 10     fused append only (the kernel's AP variant): mixed atoms of a
+//               paged cache, and the new rows' cache stores
 //
 // Softmax runs in the log2 domain with a lazily raised reference maximum:
 // each row keeps m_ref (in registers, identical in every thread of the
@@ -58,7 +60,7 @@
 
 namespace swa {
 
-constexpr int kTcThreads = 320;
+constexpr int kTcThreads = 320;  // and one append warp more under a fused append
 constexpr int kTcTileKeys = 128;
 constexpr int kTcTailBox = 32;    // keys per box of a partial tile
 constexpr int kTcMetaItems = 7;   // items per CTA decoded once into shared memory
@@ -75,8 +77,9 @@ constexpr float kNoRef = -1.0e30f;
 struct TcItem {
     int b, h, split, rt;
     ChunkRange cr;
-    int t0;    // key position of tile 0: the chunk start, or (paged cache) that
-               // rounded down to 8 so every 8-key atom lies inside one page
+    int t0;    // key position of tile 0: the chunk start, or that rounded down to
+               // a multiple of 8 (paged cache: every atom inside one page) or to
+               // q_pos mod 8 (fused append: new rows start on an atom)
     int n_tiles;
     int row0;  // first packed row of the item
     int rows;  // packed rows of the item
@@ -103,11 +106,11 @@ struct TcCfg {
     static constexpr int FTAB_OFF = META_OFF + kTcMetaItems * (int)sizeof(TcItem);  // uint32 [kFillTab]
     static constexpr int BAR_OFF = FTAB_OFF + kFillTab * 4;
     // ring full/empty [NT], q full/empty [QB], s full/free [2], p full [PB],
-    // pv done [PB], o free [2] (OB used), drain
+    // pv done [PB], o free [2] (OB used), drain, mixed atom of a fused append [NT]
     static constexpr int B_FULL = 0, B_EMPTY = NT, B_QFULL = 2 * NT, B_QEMPTY = B_QFULL + QB,
                          B_SFULL = B_QEMPTY + QB, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2,
                          B_PVDONE = B_PFULL + PB, B_OFREE = B_PVDONE + PB, B_DRAIN = B_OFREE + 2,
-                         NBARS = B_DRAIN + 1;
+                         B_MIX = B_DRAIN + 1, NBARS = B_MIX + NT;
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;  // tmem base
     static constexpr int END = MISC_OFF + 16;
     static constexpr int SMEM_BYTES = END + 1024;  // slack for 1024-byte alignment
@@ -131,6 +134,7 @@ struct TcCfg {
 
 
 // Work item `item` (its sequence's seq_len / q_pos read from global memory).
+template <bool AP>
 __device__ __forceinline__ TcItem tc_decode_global(const TcParams &T, int item) {
     const AttnParams &P = T.a;
     TcItem it;
@@ -142,7 +146,13 @@ __device__ __forceinline__ TcItem tc_decode_global(const TcParams &T, int item) 
     it.h = rest % P.Hkv;
     it.b = rest / P.Hkv;
     it.cr = chunk_range(P, it.b, it.split);
-    it.t0 = P.block_table != nullptr ? (it.cr.c_lo & ~7) : it.cr.c_lo;
+    // a contiguous cache under a fused append: rounded down to q_pos mod 8,
+    // so the new block starts on an atom of every tile (not below position 0:
+    // a box must not start at a negative row, whose bounds check would blank
+    // the rows its later atoms hold)
+    it.t0 = P.block_table != nullptr ? (it.cr.c_lo & ~7)
+            : AP                     ? max(it.cr.c_lo - ((it.cr.c_lo - it.cr.qp) & 7), 0)
+                                     : it.cr.c_lo;
     const int nk = it.cr.c_hi - it.t0;
     it.n_tiles = it.cr.c_hi > it.cr.c_lo ? (nk + kTcTileKeys - 1) / kTcTileKeys : 0;
     it.row0 = it.rt * T.rows_per_tile;
@@ -153,10 +163,11 @@ __device__ __forceinline__ TcItem tc_decode_global(const TcParams &T, int item) 
 
 // Work item `item`, the j-th of this CTA: the first kTcMetaItems were
 // decoded once at set-up into shared memory.
+template <bool AP>
 __device__ __forceinline__ TcItem tc_decode(const TcParams &T, int item, int j,
                                             const TcItem *meta) {
     if (j < kTcMetaItems) return meta[j];
-    return tc_decode_global(T, item);
+    return tc_decode_global<AP>(T, item);
 }
 
 // Barrier of one softmax warpgroup (128 threads), ids 1 / 3.
@@ -302,10 +313,348 @@ __device__ __forceinline__ void tile_copies(const AttnParams &P, const TcMaps &M
     }
 }
 
-template <int D, int N, int NT, int QB, int PB, int OB>
-__global__ void __launch_bounds__(kTcThreads, 1)
+// How a K/V tile (key positions [p, p + n_valid), ceil(n_valid / 8) atoms)
+// is sourced under a fused append (new rows at positions qp ..): atoms
+// [0, a_m) hold cache rows only; atom a_m is mixed (cache rows, then new
+// rows) when the new block starts inside it, which happens only on a paged
+// cache; atoms [a_n, natoms) hold positions >= qp only and come from
+// k_new / v_new.  A tile whose valid keys end before qp, and every tile
+// without an append, has a_m = a_n = natoms.
+__device__ __forceinline__ void append_split(const AttnParams &P, int qp, int p, int n_valid,
+                                             int &a_m, int &a_n) {
+    a_m = a_n = (n_valid + 7) >> 3;
+    if (P.k_new == nullptr || p + n_valid <= qp) return;
+    a_m = qp > p ? (qp - p) >> 3 : 0;
+    a_n = qp > p && ((qp - p) & 7) ? a_m + 1 : a_m;
+}
+
+// The TMA producer (lane 0 of warp 0) of both tensor-core kernels: for
+// every item of the CTA, its K and V tiles into the first free ring slots
+// (the fill table records where each landed) and its Q rows, issued after
+// the item's first K tile so a single Q buffer does not hold back the K
+// stream.  With a fused append, the atoms of a tile from the first new row
+// on (a mixed atom from the cache, new-row atoms from k_new / v_new) land on
+// B_MIX, for the append worker to complete the fill.  Waits for every copy
+// it issued before returning.
+template <class C, int NT, int QB, bool AP>
+__device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M,
+                                              const TcItem *meta, volatile uint32_t *ftab,
+                                              uint8_t *ring, uint8_t *qs, uint64_t *bars) {
+    using namespace tc;
+    const AttnParams &P = T.a;
+    const uint64_t policy = l2_policy_evict_first();
+    uint32_t f = 0, k = 0;  // fills (two per tile: K then V), items with keys
+    uint32_t mix_used = 0, mix_n = 0;  // slots that took a mixed atom; use count parity
+    uint32_t uses[NT];              // fills handed to each slot so far
+#pragma unroll
+    for (int s2 = 0; s2 < NT; ++s2) uses[s2] = 0;
+    bool ok = true;
+    int j = 0;
+    for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
+        const TcItem it = tc_decode<AP>(T, item, j, meta);
+        if (it.n_tiles == 0) continue;
+        const uint32_t qb = k % QB, quse = k / QB;
+        auto load_q = [&]() -> bool {
+            if (!mbar_wait_bounded(&bars[C::B_QEMPTY + qb], (quse & 1) ^ 1, P.fault,
+                                   kFaultCopyTimeout))
+                return false;
+            mbar_arrive_expect_tx(&bars[C::B_QFULL + qb], C::SLABS * T.rows_per_tile * 128);
+            for (int s = 0; s < C::SLABS; ++s)
+                tma_load_3d(qs + qb * C::Q_BUF + s * C::Q_SLAB, &M.q, 64 * s, it.h * P.G,
+                            it.b * P.q_len + it.i0, &bars[C::B_QFULL + qb]);
+            return true;
+        };
+        ++k;
+        for (int t = 0; t < it.n_tiles && ok; ++t) {
+            const int p = it.t0 + kTcTileKeys * t;
+            const int n_valid = min(kTcTileKeys, it.cr.c_hi - p);
+            const int natoms = (n_valid + 7) >> 3;
+            int a_m = natoms, a_n = natoms;
+            if constexpr (AP) append_split(P, it.cr.qp, p, n_valid, a_m, a_n);
+            const bool worker_full = AP && a_n > a_m;  // the append worker completes a mixed atom
+            for (int kv = 0; kv < 2 && ok; ++kv) {
+                if (t == 0 && kv == 1) {
+                    ok = load_q();
+                    if (!ok) break;
+                }
+                // the first free slot: never used, or its last fill consumed
+                int slot = -1;
+                uint32_t par = 0;
+                const long long w0 = clock64();
+                for (int spin = 0;; ++spin) {
+#pragma unroll
+                    for (int s2 = 0; s2 < NT; ++s2) {
+                        if (slot < 0 &&
+                            (uses[s2] == 0 ||
+                             mbar_test(&bars[C::B_EMPTY + s2], (uses[s2] - 1) & 1))) {
+                            slot = s2;
+                            par = uses[s2] & 1;
+                            ++uses[s2];
+                        }
+                    }
+                    if (slot >= 0) break;
+                    if (clock64() - w0 > kWaitLimitCycles) {
+                        atomicOr(P.fault, kFaultCopyTimeout);
+                        ok = false;
+                        break;
+                    }
+                    if (spin > 8) __nanosleep(32);
+                }
+                if (!ok) break;
+                ftab[f % kFillTab] = (f << 8) | (par << 4) | (uint32_t)slot;
+                // a fill completes (FULL) on this lane's arrival with the bytes;
+                // under a fused append it takes a second arrival: this lane's,
+                // or the append worker's after it completed a mixed atom
+                uint64_t *bar = &bars[C::B_FULL + slot];
+                uint8_t *dst = ring + slot * C::TILE_BYTES;
+                mbar_arrive_expect_tx(bar, (uint32_t)(a_m + natoms - a_n) * C::ATOM_BYTES);
+                if (a_m > 0)
+                    tile_copies<C::ATOM_BYTES>(P, M, kv, it.b, it.h, p,
+                                               a_m < natoms ? 8 * a_m : n_valid, dst, bar,
+                                               policy);
+                for (int a = a_n; a < natoms; ++a)
+                    tma_load_5d(dst + a * C::ATOM_BYTES, kv ? &M.vn_atom : &M.kn_atom, 0,
+                                p + 8 * a - it.cr.qp, 0, it.h, it.b, bar);
+                if (worker_full) {
+                    // the mixed atom from the cache, on its own barrier
+                    uint64_t *mb = &bars[C::B_MIX + slot];
+                    mix_used |= 1u << slot;
+                    mix_n ^= 1u << slot;
+                    mbar_arrive_expect_tx(mb, C::ATOM_BYTES);
+                    tma_load_3d_hint(dst + a_m * C::ATOM_BYTES, kv ? &M.v_atom : &M.k_atom, 0,
+                                     (int)cache_row(P, it.b, it.h, p + 8 * a_m), 0, mb, policy);
+                } else if (AP) {
+                    mbar_arrive(bar);
+                }
+                ++f;
+            }
+        }
+    }
+    // every copy this CTA issued has landed before it exits
+#pragma unroll
+    for (int s2 = 0; s2 < NT; ++s2) {
+        if (uses[s2] > 0)
+            mbar_wait_bounded(&bars[C::B_FULL + s2], (uses[s2] - 1) & 1, P.fault,
+                              kFaultCopyTimeout);
+        if ((mix_used >> s2) & 1u)
+            mbar_wait_bounded(&bars[C::B_MIX + s2], ((mix_n >> s2) & 1u) ^ 1u, P.fault,
+                              kFaultCopyTimeout);
+    }
+    const uint32_t nq = k < (uint32_t)QB ? k : (uint32_t)QB;
+    for (uint32_t q = 0; q < nq; ++q) {
+        const uint32_t kq = k - 1 - q;
+        mbar_wait_bounded(&bars[C::B_QFULL + kq % QB], (kq / QB) & 1, P.fault,
+                          kFaultCopyTimeout);
+    }
+}
+
+// The append warp (warp 10) under a fused append.  Over the tiles whose new
+// block starts inside an atom (paged cache): the mixed atom landed
+//   from the cache on B_MIX of the ring slot the fill table names; the warp
+//   writes the new rows over its stale ones from registers loaded from
+//   k_new / v_new ahead of time, fences the writes against the tensor
+//   core's reads and gives FULL its second arrival.
+// With at most two items per CTA it also stores each chunk's new rows to the
+// cache (row tile 0 of the chunk), overlapped with the attention; with more
+// the CTA stores them together at the end (append_flush).
+// It runs in a warp of its own: lanes of the TMA warp blocked on their
+// loads would hold back the other, diverged path of that warp.
+template <class C, int D>
+__device__ __forceinline__ void append_worker(const TcParams &T, const TcItem *meta,
+                                              const volatile uint32_t *ftab, uint8_t *ring,
+                                              uint64_t *bars) {
+    const AttnParams &P = T.a;
+    constexpr int PR = D / 8;                   // 16-byte pieces per row
+    constexpr int MP = (7 * PR + 31) / 32;      // pieces per lane of a mixed atom's new rows
+    constexpr int U = 16;                       // pieces per lane in flight while storing
+    const int t = (int)(threadIdx.x & 31);
+    uint32_t f = 0, mixpar = 0;                 // fills seen; use parity of B_MIX per slot
+    int j = 0;
+    for (int item = blockIdx.x; item < T.items; item += gridDim.x, ++j) {
+        const TcItem it = tc_decode<true>(T, item, j, meta);
+        if (it.n_tiles == 0) continue;
+        int ap_lo, ap_hi;
+        append_range(P, it.cr, ap_lo, ap_hi);
+        const long long row_b = (long long)it.b * P.q_len;  // k_new row of draft row 0
+        for (int tt = 0; tt < it.n_tiles; ++tt, f += 2) {
+            const int p = it.t0 + kTcTileKeys * tt;
+            const int n_valid = min(kTcTileKeys, it.cr.c_hi - p);
+            int a_m, a_n;
+            append_split(P, it.cr.qp, p, n_valid, a_m, a_n);
+            if (a_n == a_m) continue;
+            // the mixed atom's new rows (rows [m_lo, 8) of atom a_m), loaded early
+            const int p_m = p + 8 * a_m;
+            const int m_lo = it.cr.qp - p_m;
+            const int np = (8 - m_lo) * PR;
+            uint4 w[2][MP];
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+                for (int u = 0; u < MP; ++u) {
+                    const int e = t + 32 * u;
+                    const int i = e / PR;  // draft row of the piece
+                    w[kv][u] = make_uint4(0, 0, 0, 0);
+                    if (e < np && i < P.q_len)
+                        w[kv][u] = __ldg(reinterpret_cast<const uint4 *>(
+                            (kv ? P.v_new : P.k_new) + ((row_b + i) * P.Hkv + it.h) * D +
+                            (e % PR) * 8));
+                }
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv) {
+                // lane 0 waits for the fill's table entry and hands it on
+                const uint32_t fill = f + kv;
+                uint32_t e = 0;
+                bool found = true;
+                if (t == 0) {
+                    e = ftab[fill % kFillTab];
+                    const long long w0 = clock64();
+                    while ((e >> 8) != (fill & 0xffffffu)) {
+                        if (clock64() - w0 > kWaitLimitCycles) {
+                            atomicOr(P.fault, kFaultCopyTimeout);
+                            found = false;
+                            break;
+                        }
+                        __nanosleep(32);
+                        e = ftab[fill % kFillTab];
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, (int)found, 0)) return;
+                const int slot = (int)(__shfl_sync(0xffffffffu, e, 0) & 15u);
+                const bool landed = mbar_wait_bounded(&bars[C::B_MIX + slot],
+                                                      (mixpar >> slot) & 1u, P.fault,
+                                                      kFaultCopyTimeout);
+                if (!__all_sync(0xffffffffu, landed)) return;
+                mixpar ^= 1u << slot;
+                uint8_t *atom = ring + slot * C::TILE_BYTES + a_m * C::ATOM_BYTES;
+#pragma unroll
+                for (int u = 0; u < MP; ++u) {
+                    const int e2 = t + 32 * u;
+                    if (e2 < np) {
+                        const int r = m_lo + e2 / PR, c = e2 % PR;
+                        *reinterpret_cast<uint4 *>(atom + (c >> 3) * 1024 + r * 128 +
+                                                   (((c & 7) ^ r) << 4)) = w[kv][u];
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (t == 0) mbar_arrive(&bars[C::B_FULL + slot]);
+            }
+        }
+        // with at most two items per CTA (latency-bound calls) the chunk's new
+        // rows go to the cache here, overlapped with the attention; otherwise
+        // the whole CTA stores them at the end (append_flush)
+        if (T.items > 2 * (int)gridDim.x || it.rt != 0 || ap_lo >= ap_hi) continue;
+        const int half = (ap_hi - ap_lo) * PR, n = 2 * half;  // K then V
+        for (int b0 = 0; b0 < n; b0 += 32 * U) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int e = b0 + t + 32 * u;
+                if (e < n) {
+                    const int kv = e >= half, rest = e - kv * half;
+                    const int i = ap_lo + rest / PR - it.cr.qp;
+                    v[u] = __ldg(reinterpret_cast<const uint4 *>(
+                        (kv ? P.v_new : P.k_new) + ((row_b + i) * P.Hkv + it.h) * D +
+                        (rest % PR) * 8));
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int e = b0 + t + 32 * u;
+                if (e < n) {
+                    const int kv = e >= half, rest = e - kv * half;
+                    __nv_bfloat16 *cache = const_cast<__nv_bfloat16 *>(kv ? P.v : P.k);
+                    *reinterpret_cast<uint4 *>(
+                        cache + cache_row(P, it.b, it.h, ap_lo + rest / PR) * D +
+                        (rest % PR) * 8) = v[u];
+                }
+            }
+        }
+    }
+}
+
+// The fused append's cache stores, by every thread of the CTA once its
+// attention work is done (after the CTA-wide barrier: the ring is free then).
+// Row tile 0 of every chunk the CTA verified (the other row tiles would
+// store the same bytes) owns the chunk's new rows [ap_lo, ap_hi); their
+// 16-byte pieces, K then V per chunk, form one sequence that the threads
+// stride through with U loads in flight each, so a CTA's stores take about
+// one memory round trip however many chunks it had.  A table of the chunks
+// (sequence, head, rows, first piece) is built in `scratch` first.  No kernel
+// reads a new row back from the cache: the stores only have to land before
+// the kernel ends.
+struct AppendChunk {
+    int b, h, lo, qp, n, first;
+};
+
+template <int D>
+__device__ __forceinline__ void append_flush(const TcParams &T, const TcItem *meta,
+                                             uint8_t *scratch, int scratch_bytes, int nthreads) {
+    const AttnParams &P = T.a;
+    constexpr int PR = D / 8;  // 16-byte pieces per row
+    constexpr int U = 8;
+    const int tid = threadIdx.x;
+    AppendChunk *tab = reinterpret_cast<AppendChunk *>(scratch);
+    const int n_items = (T.items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int cap = scratch_bytes / (int)sizeof(AppendChunk) - 1;
+    for (int k0 = 0; k0 < n_items; k0 += cap) {
+        const int nk = min(cap, n_items - k0);
+        for (int k = tid; k < nk; k += nthreads) {
+            const int j = k0 + k;
+            const TcItem it = tc_decode<true>(T, (int)blockIdx.x + j * (int)gridDim.x, j, meta);
+            int lo, hi;
+            append_range(P, it.cr, lo, hi);
+            const bool own = it.n_tiles > 0 && it.rt == 0 && lo < hi;
+            tab[k] = AppendChunk{it.b, it.h, lo, it.cr.qp, own ? 2 * (hi - lo) * PR : 0, 0};
+        }
+        __syncthreads();
+        if (tid == 0) {
+            int off = 0;
+            for (int k = 0; k < nk; ++k) {
+                tab[k].first = off;
+                off += tab[k].n;
+            }
+            tab[nk].first = off;  // total
+        }
+        __syncthreads();
+        const int total = tab[nk].first;
+        int k = 0;  // chunk of the current piece (pieces are visited in increasing order)
+        for (int g0 = 0; g0 < total; g0 += nthreads * U) {
+            uint4 v[U];
+            long long dst[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int g = g0 + tid + nthreads * u;
+                dst[u] = -1;
+                if (g < total) {
+                    while (tab[k + 1].first <= g) ++k;
+                    const AppendChunk c = tab[k];
+                    const int half = c.n / 2, e = g - c.first;
+                    const int kv = e >= half, rest = e - kv * half;
+                    const int pos = c.lo + rest / PR, pc = rest % PR;
+                    v[u] = __ldg(reinterpret_cast<const uint4 *>(
+                        (kv ? P.v_new : P.k_new) +
+                        (((long long)c.b * P.q_len + (pos - c.qp)) * P.Hkv + c.h) * D + pc * 8));
+                    dst[u] = ((cache_row(P, c.b, c.h, pos) * D + pc * 8) << 1) | kv;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (dst[u] >= 0) {
+                    __nv_bfloat16 *cache = const_cast<__nv_bfloat16 *>((dst[u] & 1) ? P.v : P.k);
+                    *reinterpret_cast<uint4 *>(cache + (dst[u] >> 1)) = v[u];
+                }
+            }
+        }
+        __syncthreads();  // the table is rebuilt for the next group of items
+    }
+}
+
+template <int D, int N, int NT, int QB, int PB, int OB, bool AP>
+__global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
     swa_tc_kernel(const __grid_constant__ TcParams T, const __grid_constant__ TcMaps M) {
     using C = TcCfg<D, N, NT, QB, PB, OB>;
+    constexpr int NTHR = AP ? kTcThreads + 32 : kTcThreads;
     using namespace tc;
     constexpr int SLABS = C::SLABS;
     constexpr int MH = D / 128;
@@ -334,18 +683,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // Nothing before grid_dep_wait() reads memory the previous kernel in the
     // stream may write: the tensor maps are kernel parameters, so their
     // descriptors are fetched while that kernel finishes.
-    if (warp == 0 && lane < 11) {
+    if (warp == 0 && lane < (AP ? 13 : 11)) {
         const CUtensorMap *mp = lane < 4    ? &M.k_atoms[lane]
                                 : lane < 8  ? &M.v_atoms[lane - 4]
                                 : lane == 8 ? &M.k_atom
                                 : lane == 9 ? &M.v_atom
-                                            : &M.q;
+                                : lane == 10 ? &M.q
+                                : lane == 11 ? &M.kn_atom
+                                             : &M.vn_atom;
         prefetch_tmap(mp);
     }
     if (tid == 0) {
         for (int i = 0; i < NT; ++i) {
-            mbar_init(&bars[C::B_FULL + i], 1);
+            // under a fused append a fill takes a second arrival
+            mbar_init(&bars[C::B_FULL + i], AP ? 2 : 1);
             mbar_init(&bars[C::B_EMPTY + i], 1);
+            mbar_init(&bars[C::B_MIX + i], 1);
         }
         for (int i = 0; i < QB; ++i) {
             mbar_init(&bars[C::B_QFULL + i], 1);
@@ -365,7 +718,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     // Q rows past an item's rows stay zero for the whole kernel (TMA writes
     // only the first rows_per_tile rows of each slab).
-    for (int i = tid; i < QB * C::Q_BUF / 16; i += kTcThreads)
+    for (int i = tid; i < QB * C::Q_BUF / 16; i += NTHR)
         reinterpret_cast<uint4 *>(qs)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 1) {
@@ -375,10 +728,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     grid_dep_wait();
     grid_dep_trigger();
     // metadata of this CTA's first items
-    for (int i = tid; i < kFillTab; i += kTcThreads) ftab[i] = 0xffffffffu;
-    for (int j = tid; j < kTcMetaItems; j += kTcThreads) {
+    for (int i = tid; i < kFillTab; i += NTHR) ftab[i] = 0xffffffffu;
+    for (int j = tid; j < kTcMetaItems; j += NTHR) {
         const long long item = (long long)blockIdx.x + (long long)j * gridDim.x;
-        if (item < T.items) meta[j] = tc_decode_global(T, (int)item);
+        if (item < T.items) meta[j] = tc_decode_global<AP>(T, (int)item);
     }
     fence_before_sync();
     __syncthreads();
@@ -387,84 +740,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp == 0) {
         // ======================================================= producer
-        if (lane == 0) {
-            const uint64_t policy = l2_policy_evict_first();
-            uint32_t f = 0, k = 0;  // fills (two per tile: K then V), items with keys
-            uint32_t uses[NT];      // fills handed to each slot so far
-#pragma unroll
-            for (int s2 = 0; s2 < NT; ++s2) uses[s2] = 0;
-            bool ok = true;
-            int j = 0;
-            for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
-                const TcItem it = tc_decode(T, item, j, meta);
-                if (it.n_tiles == 0) continue;
-                const uint32_t qb = k % QB, quse = k / QB;
-                // Q of the item, issued after its first K tile so that a single
-                // Q buffer does not hold back the K stream
-                auto load_q = [&]() -> bool {
-                    if (!mbar_wait_bounded(&bars[C::B_QEMPTY + qb], (quse & 1) ^ 1, P.fault,
-                                           kFaultCopyTimeout))
-                        return false;
-                    mbar_arrive_expect_tx(&bars[C::B_QFULL + qb], SLABS * T.rows_per_tile * 128);
-                    for (int s = 0; s < SLABS; ++s)
-                        tma_load_3d(qs + qb * C::Q_BUF + s * C::Q_SLAB, &M.q, 64 * s,
-                                    it.h * P.G, it.b * P.q_len + it.i0, &bars[C::B_QFULL + qb]);
-                    return true;
-                };
-                ++k;
-                for (int t = 0; t < it.n_tiles && ok; ++t) {
-                    const int p = it.t0 + kTcTileKeys * t;
-                    const int n_valid = min(kTcTileKeys, it.cr.c_hi - p);
-                    for (int kv = 0; kv < 2 && ok; ++kv) {
-                        if (t == 0 && kv == 1) {
-                            ok = load_q();
-                            if (!ok) break;
-                        }
-                        // the first free slot: never used, or its last fill consumed
-                        int slot = -1;
-                        uint32_t par = 0;
-                        const long long w0 = clock64();
-                        for (int spin = 0;; ++spin) {
-#pragma unroll
-                            for (int s2 = 0; s2 < NT; ++s2) {
-                                if (slot < 0 && (uses[s2] == 0 ||
-                                                 mbar_test(&bars[C::B_EMPTY + s2], (uses[s2] - 1) & 1))) {
-                                    slot = s2;
-                                    par = uses[s2] & 1;
-                                    ++uses[s2];
-                                }
-                            }
-                            if (slot >= 0) break;
-                            if (clock64() - w0 > kWaitLimitCycles) {
-                                atomicOr(P.fault, kFaultCopyTimeout);
-                                ok = false;
-                                break;
-                            }
-                            if (spin > 8) __nanosleep(32);
-                        }
-                        if (!ok) break;
-                        ftab[f % kFillTab] = (f << 8) | (par << 4) | (uint32_t)slot;
-                        uint64_t *bar = &bars[C::B_FULL + slot];
-                        mbar_arrive_expect_tx(bar, (uint32_t)((n_valid + 7) >> 3) * C::ATOM_BYTES);
-                        tile_copies<C::ATOM_BYTES>(P, M, kv, it.b, it.h, p, n_valid,
-                                                   ring + slot * C::TILE_BYTES, bar, policy);
-                        ++f;
-                    }
-                }
-            }
-            // every copy this CTA issued has landed before it exits
-#pragma unroll
-            for (int s2 = 0; s2 < NT; ++s2)
-                if (uses[s2] > 0)
-                    mbar_wait_bounded(&bars[C::B_FULL + s2], (uses[s2] - 1) & 1, P.fault,
-                                      kFaultCopyTimeout);
-            const uint32_t nq = k < (uint32_t)QB ? k : (uint32_t)QB;
-            for (uint32_t q = 0; q < nq; ++q) {
-                const uint32_t kq = k - 1 - q;
-                mbar_wait_bounded(&bars[C::B_QFULL + kq % QB], (kq / QB) & 1, P.fault,
-                                  kFaultCopyTimeout);
-            }
-        }
+        if (lane == 0)
+            tile_producer<C, NT, QB, AP>(T, M, meta, ftab, ring, qs, bars);
     } else if (warp == 1) {
         // ============================================================ MMA
         // An event loop over two cursors on the same tile sequence: S = K Q^T
@@ -501,7 +778,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // first tile of the next non-empty item at or after (item, j)
             auto seek = [&](Cursor &c) {
                 for (; c.item < T.items; c.item += gridDim.x, ++c.j) {
-                    const TcItem it = tc_decode(T, c.item, c.j, meta);
+                    const TcItem it = tc_decode<AP>(T, c.item, c.j, meta);
                     if (it.n_tiles > 0) {
                         c.n_tiles = it.n_tiles;
                         c.last_keys = it.cr.c_hi - it.t0 - kTcTileKeys * (it.n_tiles - 1);
@@ -675,7 +952,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             __syncwarp();
         }
-    } else {
+    } else if (warp < 10) {
         // ===================================================== softmax
         constexpr int HN = N / 2;                 // rows per softmax warpgroup
         constexpr int CWH = HN >= 32 ? 32 : HN;  // TMEM columns per S load
@@ -696,7 +973,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool ok = true;
         int j = 0;
         for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
-            const TcItem it = tc_decode(T, item, j, meta);
+            const TcItem it = tc_decode<AP>(T, item, j, meta);
             const size_t bh = (size_t)it.b * P.Hkv + it.h;
             const int my_rows = min(HN, it.rows - r0);  // rows of this group in the item
             if (it.n_tiles == 0) {
@@ -993,6 +1270,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             ++k;
         }
+    } else if constexpr (AP) {
+        // ================================================= append worker
+        append_worker<C, D>(T, meta, ftab, ring, bars);
     }
 
     // ---------------------------------------------------------- teardown
@@ -1000,6 +1280,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __syncthreads();
     fence_after_sync();
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+    if constexpr (AP) {
+        if (T.items > 2 * (int)gridDim.x) append_flush<D>(T, meta, ring, NT * C::TILE_BYTES, NTHR);
+    }
 }
 
 }  // namespace swa

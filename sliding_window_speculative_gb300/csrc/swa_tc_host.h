@@ -30,6 +30,11 @@ struct TcMaps {
     CUtensorMap v_atoms[4];
     CUtensorMap v_atom;
     CUtensorMap q;           // 3D box (64 dims x G heads x draft rows)
+    // fused append only: the new rows k_new / v_new [B, q_len, Hkv, D] as 5D
+    // (x = 64 dims, y = draft row, z = slab, w = KV head, v = sequence), a
+    // box of one atom (8 draft rows; rows past q_len are zero-filled)
+    CUtensorMap kn_atom;
+    CUtensorMap vn_atom;
 };
 
 struct TcConfInfo {

@@ -226,6 +226,16 @@ __device__ __forceinline__ void tma_load_4d_hint(void *smem_dst, const CUtensorM
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_5d(void *smem_dst, const CUtensorMap *map, int x, int y,
+                                            int z, int w, int v, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+          "r"(z), "r"(w), "r"(v), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

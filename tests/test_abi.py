@@ -192,3 +192,22 @@ def test_greedy_accept_rejects_bad_arguments(lib):
         st = lib.swa_greedy_accept(*args, None)
         assert st == swa.SWA_ERR_INVALID_ARG, args
         assert swa.swa_last_error()
+
+
+def test_append_verify_rejects_bad_arguments(lib):
+    # validated on the host before any CUDA call
+    d = swa.make_dims(*GOOD)
+
+    def call(kn=16, vn=32, paged=None, q=48):
+        return lib.swa_append_verify_attn(q, kn, vn, 64, 80, paged, 96, 112, 188, 0.0625, 128,
+                                          None, ctypes.byref(d), None)
+
+    assert call(kn=None) == swa.SWA_ERR_INVALID_ARG
+    assert call(vn=None) == swa.SWA_ERR_INVALID_ARG
+    assert call(kn=24) == swa.SWA_ERR_INVALID_ARG        # 8-byte aligned only
+    assert call(q=None) == swa.SWA_ERR_INVALID_ARG
+    bad_page = swa.SwaPaged(160, 4096 // 12, 12, 100)    # pages of 12 rows
+    assert call(paged=ctypes.byref(bad_page)) == swa.SWA_ERR_INVALID_ARG
+    short = swa.SwaPaged(160, 10, 16, 100)               # max_len != max_blocks * page_size
+    assert call(paged=ctypes.byref(short)) == swa.SWA_ERR_INVALID_ARG
+    assert swa.swa_last_error()

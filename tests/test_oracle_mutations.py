@@ -33,6 +33,14 @@ MUTATIONS = {
     # the acceptance compares a draft with the next row's token
     "accept_wrong_row": ("while (n < q_len - 1 && argmax[b * q_len + n] == draft[b * (q_len - 1) + n]) ++n;",
                          "while (n < q_len - 1 && argmax[b * q_len + n + 1] == draft[b * (q_len - 1) + n]) ++n;"),
+    # the append writes up to the cache end instead of stopping at seq_len
+    "append_no_seq_len_clip": ("const int64_t end = seq_lens[b] < L ? seq_lens[b] : L;",
+                               "const int64_t end = L;"),
+    # the new rows read as [B, Hkv, q_len, D] instead of [B, q_len, Hkv, D]
+    "append_rows_layout": ("const double *src = rows + ((b * q_len + i) * Hkv + h) * D;",
+                           "const double *src = rows + ((b * Hkv + h) * q_len + i) * D;"),
+    # row i lands one position late
+    "append_row_offset": ("const int64_t pos = q_pos[b] + i;", "const int64_t pos = q_pos[b] + i + 1;"),
 }
 
 PIN_CHECKS = [
@@ -44,6 +52,7 @@ PIN_CHECKS = [
     lambda: pins.test_zero_keys_closed_form(),
     lambda: [pins.test_accept_hand_worked_examples(c) for c in pins._load_accept_golden()],
     lambda: pins.test_accept_matches_numpy_argmax_and_prefix_count(),
+    lambda: [pins.test_append_hand_worked_examples(c) for c in pins._load_append_golden()],
 ]
 
 

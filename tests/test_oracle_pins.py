@@ -338,3 +338,53 @@ def test_accept_keep_set_is_a_relabelling():
     am1, acc1 = oracle.greedy_accept(logits, keep[am0[:, :-1]], keep)
     assert np.array_equal(am1, keep[am0])
     assert np.all(acc1 == 7)                 # drafts taken from the argmax: all accepted
+
+
+# ------------------------------------------------------------ fused KV append
+
+def _load_append_golden():
+    path = os.path.join(os.path.dirname(__file__), "golden", "append_cases.json")
+    with open(path) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _load_append_golden(), ids=lambda c: c["name"])
+def test_append_hand_worked_examples(case):
+    got = oracle.append_rows(np.array(case["cache"], dtype=np.float64),
+                             np.array(case["rows"], dtype=np.float64), case["q_pos"],
+                             case["seq_lens"])
+    assert np.array_equal(got, np.array(case["expected"], dtype=np.float64)), case["derivation"]
+
+
+def test_append_restores_a_cleared_block():
+    # A seeded case's cache already holds its block's rows; blanking them and
+    # appending the rows read back out gives the cache back exactly, so
+    # attention over the appended cache is the attention of the case itself.
+    case = inputs.make_case("append", 3, 8, 2, 64, 8, 16, [40, 8, 25], 48, seed=5)
+    k, v = f64(case.k_cache), f64(case.v_cache)
+    B, Hkv, L, D = k.shape
+    rows_k = np.zeros((B, 8, Hkv, D))
+    rows_v = np.zeros((B, 8, Hkv, D))
+    k0, v0 = k.copy(), v.copy()
+    for b, qp in enumerate(case.q_pos_host):
+        rows_k[b] = k[b, :, qp:qp + 8].transpose(1, 0, 2)
+        rows_v[b] = v[b, :, qp:qp + 8].transpose(1, 0, 2)
+        k0[b, :, qp:qp + 8] = 7.0
+        v0[b, :, qp:qp + 8] = -7.0
+    k1 = oracle.append_rows(k0, rows_k, case.q_pos_host, case.seq_lens_host)
+    v1 = oracle.append_rows(v0, rows_v, case.q_pos_host, case.seq_lens_host)
+    assert np.array_equal(k1, k) and np.array_equal(v1, v)
+    assert np.all(k0[0, :, case.q_pos_host[0]] == 7.0)   # the input is not modified
+
+
+def test_append_writes_nothing_outside_the_block():
+    rng = np.random.default_rng(9)
+    cache = rng.standard_normal((2, 3, 20, 4))
+    rows = rng.standard_normal((2, 5, 3, 4))
+    got = oracle.append_rows(cache, rows, [4, 15], [9, 20])
+    mask = np.zeros(cache.shape, dtype=bool)
+    mask[0, :, 4:9] = True
+    mask[1, :, 15:20] = True
+    assert np.array_equal(got[~mask], cache[~mask])
+    assert np.array_equal(got[0, :, 4:9], rows[0].transpose(1, 0, 2))
+    assert np.array_equal(got[1, :, 15:20], rows[1].transpose(1, 0, 2))
