@@ -59,6 +59,12 @@ def make_workload(name, device, seed=0):
         return inputs.window_vs_full(int(name.rsplit("w", 1)[1]), device=device, seed=seed)
     if name.startswith("tiny_q"):
         return inputs.tiny(int(name[6:]), device=device, seed=seed)
+    if name.startswith("prefill_q"):
+        # prefill_q{Q}[_b{B}]: sliding-window prefill chunks of Q tokens
+        parts = name.split("_")
+        Q = int(parts[1][1:])
+        B = int(parts[2][1:]) if len(parts) > 2 else 1
+        return inputs.prefill(Q, batch=B, device=device, seed=seed)
     if name.startswith("stress_w"):
         # stress_w{W}_q{Q}[_l{L}]: the bandwidth-stress batch; _l shortens the
         # cache (and the context range) for profiler captures.
@@ -684,6 +690,20 @@ def main():
         line["accept"] = [time_accept(1, 8, 262144), time_accept(64, 8, 262144, steps=500)]
         # the bandwidth-stress batch (inputs larger than L2) on a paged cache
         line["paged"] = [time_paged("stress_w188_q8", 16), time_paged("stress_w188_q8", 64)]
+        # sliding-window prefill chunks of 512 tokens (one sequence, and 64)
+        pre = {}
+        for name in ("prefill_q512", "prefill_q512_b64"):
+            c2 = make_workload(name, dev)
+            k2, t2 = workload_bytes(c2)
+            r2 = time_device(c2, 200, 5)
+            ach = t2 / (r2["us_per_call"] * 1e-6) / 1e9
+            pre[name] = {"us_per_call": round(r2["us_per_call"], 3),
+                         "achieved_gbs": round(ach, 2), "frac": round(ach / peak, 4),
+                         "tokens_per_s": round(c2.q.shape[0] * c2.q.shape[1] /
+                                               (r2["us_per_call"] * 1e-6))}
+            del c2
+            torch.cuda.empty_cache()
+        line["prefill"] = pre
         # the cache write of the verify block fused into the attention call
         line["append"] = [time_append("single_stream"), time_append("batched"),
                           time_append("stress_w188_q8", steps=200)]

@@ -11,7 +11,8 @@
  *   recent W tokens, section "What each piece does, and why"),
  *   SPECULATIVE_CONFIG num_speculative_tokens=7 (q_len = 1 + 7 = 8),
  *   SPLITKV_VERIFY=1 and SPLITKV_VERIFY_MAX_Q=64 (split-KV verify kernel,
- *   at most 64 query rows per call).
+ *   at most 64 query rows per verify call); MAX_NUM_BATCHED_TOKENS=512 (the
+ *   same windowed attention over prefill chunks of up to 512 tokens).
  *
  * Definition (per sequence b, query head h, draft row i, p = q_pos[b] + i,
  * KV head g = floor(h / (Hq / Hkv))):
@@ -50,7 +51,9 @@ typedef enum {
  * dimensions.  All tensors are contiguous row-major. */
 typedef struct {
     int32_t batch;         /* B, number of sequences, 1..65535                  */
-    int32_t q_len;         /* query rows per sequence, 1..64 (SPLITKV_VERIFY_MAX_Q) */
+    int32_t q_len;         /* query rows per sequence, 1..512: verify blocks of up to
+                              64 rows (SPLITKV_VERIFY_MAX_Q) and sliding-window
+                              prefill chunks of up to 512 (MAX_NUM_BATCHED_TOKENS) */
     int32_t num_q_heads;   /* Hq                                                */
     int32_t num_kv_heads;  /* Hkv, Hq % Hkv == 0; G = Hq / Hkv query heads per KV head */
     int32_t head_dim;      /* D, one of 64, 128, 256                            */

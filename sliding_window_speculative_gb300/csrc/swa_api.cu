@@ -24,7 +24,9 @@ namespace {
 constexpr int kMaxSplits = 64;
 constexpr int kTcKeysPerTile = 128;  // keys per tensor-core tile (MMA M)
 static_assert(kMaxSplits <= swa::kMergeMaxSplits, "the merge kernel weighs at most 64 splits");
-constexpr int kMaxQLen = 64;      // SPLITKV_VERIFY_MAX_Q
+constexpr int kMaxQLen = 64;      // SPLITKV_VERIFY_MAX_Q: draft rows of a greedy verification
+constexpr int kMaxBlockLen = 512; // MAX_NUM_BATCHED_TOKENS: rows of an attention call
+                                  // (verify blocks up to 64, prefill chunks up to 512)
 constexpr int kMaxDevices = 64;
 
 thread_local char t_last_error[512] = "";
@@ -47,8 +49,8 @@ swa_status validate_dims(const swa_dims *d, int32_t window) {
     if (d == nullptr) return fail(SWA_ERR_INVALID_ARG, "dims is NULL");
     if (d->batch < 1 || d->batch > 65535)
         return fail(SWA_ERR_INVALID_ARG, "batch %d outside [1, 65535]", d->batch);
-    if (d->q_len < 1 || d->q_len > kMaxQLen)
-        return fail(SWA_ERR_INVALID_ARG, "q_len %d outside [1, %d]", d->q_len, kMaxQLen);
+    if (d->q_len < 1 || d->q_len > kMaxBlockLen)
+        return fail(SWA_ERR_INVALID_ARG, "q_len %d outside [1, %d]", d->q_len, kMaxBlockLen);
     if (d->num_q_heads < 1 || d->num_kv_heads < 1)
         return fail(SWA_ERR_INVALID_ARG, "head counts must be >= 1 (Hq %d, Hkv %d)",
                     d->num_q_heads, d->num_kv_heads);
@@ -97,7 +99,9 @@ int forced_kernel() {
 }
 
 // Split heuristic.  Host-only: seq_lens live on the device, so the
-// worst-case span W + q_len - 1 (bounded by the cache length) is used.
+// worst-case span W + q_len - 1 (bounded by the cache length) is used; a
+// work item reads only the windows of its own draft rows, W + rows - 1 keys
+// (the kernels narrow each item's chunk), and that decides the splits.
 //  - Rows-major tensor-core kernel for more than 32 packed rows, up to 128
 //    rows per item; same chunking as below.
 //  - Tensor-core path (head_dim 128/256; >= 16 packed rows, or a batch whose
@@ -157,22 +161,35 @@ Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
     if (use_rows || use_tc) {
         const int ctas_per_sm = 1;  // both tensor-core kernels: one persistent CTA per SM
         const long long units = (long long)d->batch * d->num_kv_heads * p.row_tiles;
+        long long item_span = (long long)window + p.q_rows_per_tile - 1;
+        if (item_span > span) item_span = span;
+        long long chunk;
         if (d->num_splits > 0) {
             splits = d->num_splits;
-        } else if (units * 2 >= num_sms || span <= 3 * kTcKeysPerTile) {
-            // a split costs a partial round trip, a dependent merge launch
-            // and the merge (~2.5 us measured on GB300), which a span of up to
-            // three 128-key tiles (~1.2 us each) does not win back
-            splits = 1;
+            chunk = (span + splits - 1) / splits;
         } else {
-            long long s = (num_sms + units - 1) / units;
-            const long long by_len = (span + kTcKeysPerTile - 1) / kTcKeysPerTile;
-            splits = (int)(s < by_len ? s : by_len);
+            int per_item;  // chunks across one item's keys
+            if (units * 2 >= num_sms || item_span <= 3 * kTcKeysPerTile) {
+                // a split costs a partial round trip, a dependent merge launch
+                // and the merge (~2.5 us measured on GB300), which a span of up
+                // to three 128-key tiles (~1.2 us each) does not win back
+                per_item = 1;
+            } else {
+                const long long s = (num_sms + units - 1) / units;
+                const long long by_len = (item_span + kTcKeysPerTile - 1) / kTcKeysPerTile;
+                per_item = (int)(s < by_len ? s : by_len);
+            }
+            chunk = (item_span + per_item - 1) / per_item;
+            if (per_item == 1) chunk = span;  // one chunk: the whole span
+            chunk = (chunk + 15) / 16 * 16;
+            if ((span + chunk - 1) / chunk > kMaxSplits) chunk = (span + kMaxSplits - 1) / kMaxSplits;
+            splits = ceil_div(span, chunk);
         }
         if (splits < 1) splits = 1;
-        if (splits > kMaxSplits) splits = kMaxSplits;
-        long long chunk = (span + splits - 1) / splits;
-        if (d->num_splits == 0) chunk = (chunk + 15) / 16 * 16;
+        if (splits > kMaxSplits) {
+            splits = kMaxSplits;
+            chunk = (span + splits - 1) / splits;
+        }
         if (chunk < 1) chunk = 1;
         splits = ceil_div(span, chunk);
         p.splits = splits;
@@ -189,19 +206,24 @@ Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
         p.rows_per_tile = p.rpw * p.nrg;
         p.row_tiles = ceil_div(R, p.rows_per_tile);
         const long long units = (long long)d->batch * d->num_kv_heads * p.row_tiles;
+        // keys one CTA reads: the windows of its draft rows
+        long long item_span = (long long)window + (p.rows_per_tile + G - 1) / G;
+        if (item_span > span) item_span = span;
+        long long chunk;
         if (d->num_splits > 0) {
             splits = d->num_splits;
+            if (splits > kMaxSplits) splits = kMaxSplits;
+            chunk = (span + splits - 1) / splits;
         } else {
             const long long target = 2LL * num_sms;
             long long s = (target + units - 1) / units;
-            const long long by_len = (span + swa::kSimtTileKeys - 1) / swa::kSimtTileKeys;
+            const long long by_len = (item_span + swa::kSimtTileKeys - 1) / swa::kSimtTileKeys;
             if (s > by_len) s = by_len;
-            splits = (int)s;
+            if (s < 1) s = 1;
+            chunk = (item_span + s - 1) / s;
+            chunk = (chunk + 15) / 16 * 16;
+            if ((span + chunk - 1) / chunk > kMaxSplits) chunk = (span + kMaxSplits - 1) / kMaxSplits;
         }
-        if (splits < 1) splits = 1;
-        if (splits > kMaxSplits) splits = kMaxSplits;
-        long long chunk = (span + splits - 1) / splits;
-        if (d->num_splits == 0) chunk = (chunk + 15) / 16 * 16;
         if (chunk < 1) chunk = 1;
         splits = ceil_div(span, chunk);
         p.splits = splits;

@@ -50,12 +50,13 @@ struct AttnParams {
     float qk_scale;   // scale * log2(e)
 };
 
-// Key range [c_lo, c_hi) of chunk `split` of sequence b's window span,
-// clamped to the sequence's own slab [0, L).
+// Chunk `split` [lo, hi) of sequence b's window span (clamped to the
+// sequence's own slab [0, L)), and the keys [c_lo, c_hi) a work item reads:
+// the chunk, narrowed to the windows of the item's draft rows.
 struct ChunkRange {
-    int lo, hi;   // whole span, hi exclusive
-    int c_lo, c_hi;
-    int qp;       // q_pos of the sequence
+    int lo, hi;     // the chunk
+    int c_lo, c_hi; // keys read
+    int qp;         // q_pos of the sequence
 };
 
 __device__ __forceinline__ ChunkRange chunk_range_of(const AttnParams &P, long long qp,
@@ -72,16 +73,25 @@ __device__ __forceinline__ ChunkRange chunk_range_of(const AttnParams &P, long l
     long long chi = clo + P.chunk;
     if (clo > hi) clo = hi;
     if (chi > hi) chi = hi;
-    c.lo = (int)lo;
-    c.hi = (int)hi;
-    c.c_lo = (int)clo;
-    c.c_hi = (int)chi;
+    c.lo = c.c_lo = (int)clo;
+    c.hi = c.c_hi = (int)chi;
     c.qp = (int)(qp < -(1LL << 30) ? -(1LL << 30) : (qp > (1LL << 30) ? (1LL << 30) : qp));
     return c;
 }
 
-__device__ __forceinline__ ChunkRange chunk_range(const AttnParams &P, int b, int split) {
-    return chunk_range_of(P, P.q_pos[b], P.seq_lens[b], split);
+// The chunk of a work item holding draft rows [i_first, i_last]: the keys
+// it reads narrowed to the union of those rows' windows,
+// [q_pos + i_first - W + 1, q_pos + i_last] (a row tile of a long block,
+// e.g. a 512-token prefill chunk, sees W + its rows - 1 keys, not the whole
+// span).
+__device__ __forceinline__ ChunkRange chunk_range(const AttnParams &P, int b, int split,
+                                                  int i_first, int i_last) {
+    ChunkRange c = chunk_range_of(P, P.q_pos[b], P.seq_lens[b], split);
+    const long long lo = (long long)c.qp + i_first - P.window + 1;
+    const long long hi = (long long)c.qp + i_last + 1;
+    if (lo > c.c_lo) c.c_lo = (int)(lo < c.c_hi ? lo : c.c_hi);
+    if (hi < c.c_hi) c.c_hi = (int)(hi > c.c_lo ? hi : c.c_lo);
+    return c;
 }
 
 // Cache row (in rows of D elements) of key position j of (sequence b, KV
@@ -92,17 +102,18 @@ __device__ __forceinline__ long long cache_row(const AttnParams &P, int b, int h
     return ((long long)page * P.Hkv + h) * P.page_size + (j % P.page_size);
 }
 
-// Key positions [lo, hi) of a chunk that come from the fused append's new
-// rows (positions q_pos ..) rather than the cache; empty without an append.
-// The kernels load those rows into shared memory straight from k_new / v_new
-// and store them to the cache from there: no kernel reads a new row back
-// from the cache, so the stores need no ordering against the tile loads
-// (several CTAs, the row tiles of one chunk, store the same bytes).
-__device__ __forceinline__ void append_range(const AttnParams &P, const ChunkRange &cr, int &lo,
-                                             int &hi) {
-    lo = cr.c_lo > cr.qp ? cr.c_lo : cr.qp;
-    hi = P.k_new != nullptr ? cr.c_hi : lo;
-    if (hi < lo) hi = lo;
+// The new rows of a fused append that a work item (draft rows
+// [i_first, i_last], its chunk cr) stores to the cache: positions
+// q_pos + i of its own draft rows inside its chunk, so every new row has
+// exactly one owner; empty without an append.  The kernels read new rows
+// straight from k_new / v_new and no kernel reads one back from the cache,
+// so the stores need no ordering against the tile loads.
+__device__ __forceinline__ void append_range(const AttnParams &P, const ChunkRange &cr,
+                                             int i_first, int i_last, int &lo, int &hi) {
+    const long long a = (long long)cr.qp + i_first, e = (long long)cr.qp + i_last + 1;
+    lo = (int)(a > cr.lo ? (a < cr.hi ? a : cr.hi) : cr.lo);
+    hi = (int)(e < cr.hi ? (e > lo ? e : lo) : cr.hi);
+    if (P.k_new == nullptr || hi < lo) hi = lo;
 }
 
 template <int D>
@@ -183,13 +194,20 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
 
     grid_dep_wait();
     grid_dep_trigger();
-    const ChunkRange cr = chunk_range(P, b, split);
+    // draft rows of this CTA's packed rows [rt * RPT, min(R, rt * RPT + RPT))
+    const int i_first = rt * C::RPT / P.G;
+    const int i_last = (min(P.R, rt * C::RPT + C::RPT) - 1) / P.G;
+    const ChunkRange cr = chunk_range(P, b, split, i_first, i_last);
     const int n_keys = cr.c_hi - cr.c_lo;
     const int n_tiles = n_keys > 0 ? (n_keys + kSimtTileKeys - 1) / kSimtTileKeys : 0;
 
 
+    // keys read from k_new / v_new (every position >= q_pos under an append)
+    // and the new rows this CTA stores to the cache
+    const int nw_lo = cr.c_lo > cr.qp ? cr.c_lo : cr.qp;
+    const int nw_hi = P.k_new != nullptr && cr.c_hi > nw_lo ? cr.c_hi : nw_lo;
     int ap_lo, ap_hi;
-    append_range(P, cr, ap_lo, ap_hi);
+    append_range(P, cr, i_first, i_last, ap_lo, ap_hi);
     auto issue = [&](int t) {
         const int s = t % C::STAGES;
         const int j0 = cr.c_lo + t * kSimtTileKeys;
@@ -202,14 +220,14 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
         // is one copy from k_new / v_new
         for (int j = j0; j < j0 + n;) {
             const uint32_t off = (uint32_t)(j - j0) * D * 2;
-            if (j >= ap_lo && j < ap_hi) {
+            if (j >= nw_lo && j < nw_hi) {
                 const size_t src = (((size_t)b * P.q_len + (j - cr.qp)) * P.Hkv + h) * D;
                 bulk_copy_g2s(dst + off, P.k_new + src, D * 2, &full[s]);
                 bulk_copy_g2s(dst + C::TILE_BYTES + off, P.v_new + src, D * 2, &full[s]);
                 ++j;
                 continue;
             }
-            int run = (ap_lo < ap_hi && j < ap_lo && ap_lo < j0 + n ? ap_lo : j0 + n) - j;
+            int run = (nw_lo < nw_hi && j < nw_lo && nw_lo < j0 + n ? nw_lo : j0 + n) - j;
             if (P.block_table != nullptr) {
                 const int left = P.page_size - j % P.page_size;
                 run = run < left ? run : left;
@@ -280,9 +298,9 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
         const __nv_bfloat16 *Vs = Ks + kSimtTileKeys * D;
         const int j0 = cr.c_lo + t * kSimtTileKeys;
         const int n = min(kSimtTileKeys, cr.c_hi - j0);
-        if (rt == 0) {
-            // the fused append's new rows of this tile, from the stage to the
-            // cache (row tile 0 only: the others would store the same bytes)
+        {
+            // the fused append's new rows of this tile that this CTA owns, from
+            // the stage to the cache
             const int r0 = max(ap_lo, j0) - j0, r1 = min(ap_hi, j0 + n) - j0;
             constexpr int PR = D / 8;
             for (int e = tid; e < 2 * (r1 - r0) * PR; e += kSimtThreads) {

@@ -145,7 +145,10 @@ __device__ __forceinline__ TcItem tc_decode_global(const TcParams &T, int item) 
     rest /= P.splits;
     it.h = rest % P.Hkv;
     it.b = rest / P.Hkv;
-    it.cr = chunk_range(P, it.b, it.split);
+    it.row0 = it.rt * T.rows_per_tile;
+    it.rows = min(P.R - it.row0, T.rows_per_tile);
+    it.i0 = it.rt * T.q_rows_per_tile;
+    it.cr = chunk_range(P, it.b, it.split, it.i0, (it.row0 + it.rows - 1) / P.G);
     // a contiguous cache under a fused append: rounded down to q_pos mod 8,
     // so the new block starts on an atom of every tile (not below position 0:
     // a box must not start at a negative row, whose bounds check would blank
@@ -155,9 +158,6 @@ __device__ __forceinline__ TcItem tc_decode_global(const TcParams &T, int item) 
                                      : it.cr.c_lo;
     const int nk = it.cr.c_hi - it.t0;
     it.n_tiles = it.cr.c_hi > it.cr.c_lo ? (nk + kTcTileKeys - 1) / kTcTileKeys : 0;
-    it.row0 = it.rt * T.rows_per_tile;
-    it.rows = min(P.R - it.row0, T.rows_per_tile);
-    it.i0 = it.rt * T.q_rows_per_tile;
     return it;
 }
 
@@ -454,9 +454,10 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
 //   writes the new rows over its stale ones from registers loaded from
 //   k_new / v_new ahead of time, fences the writes against the tensor
 //   core's reads and gives FULL its second arrival.
-// With at most two items per CTA it also stores each chunk's new rows to the
-// cache (row tile 0 of the chunk), overlapped with the attention; with more
-// the CTA stores them together at the end (append_flush).
+// With at most two items per CTA it also stores the new rows the item owns
+// (its own draft rows' positions inside its chunk) to the cache, overlapped
+// with the attention; with more the CTA stores them together at the end
+// (append_flush).
 // It runs in a warp of its own: lanes of the TMA warp blocked on their
 // loads would hold back the other, diverged path of that warp.
 template <class C, int D>
@@ -474,7 +475,7 @@ __device__ __forceinline__ void append_worker(const TcParams &T, const TcItem *m
         const TcItem it = tc_decode<true>(T, item, j, meta);
         if (it.n_tiles == 0) continue;
         int ap_lo, ap_hi;
-        append_range(P, it.cr, ap_lo, ap_hi);
+        append_range(P, it.cr, it.i0, (it.row0 + it.rows - 1) / P.G, ap_lo, ap_hi);
         const long long row_b = (long long)it.b * P.q_len;  // k_new row of draft row 0
         for (int tt = 0; tt < it.n_tiles; ++tt, f += 2) {
             const int p = it.t0 + kTcTileKeys * tt;
@@ -540,10 +541,10 @@ __device__ __forceinline__ void append_worker(const TcParams &T, const TcItem *m
                 if (t == 0) mbar_arrive(&bars[C::B_FULL + slot]);
             }
         }
-        // with at most two items per CTA (latency-bound calls) the chunk's new
+        // with at most two items per CTA (latency-bound calls) the item's new
         // rows go to the cache here, overlapped with the attention; otherwise
         // the whole CTA stores them at the end (append_flush)
-        if (T.items > 2 * (int)gridDim.x || it.rt != 0 || ap_lo >= ap_hi) continue;
+        if (T.items > 2 * (int)gridDim.x || ap_lo >= ap_hi) continue;
         const int half = (ap_hi - ap_lo) * PR, n = 2 * half;  // K then V
         for (int b0 = 0; b0 < n; b0 += 32 * U) {
             uint4 v[U];
@@ -575,9 +576,9 @@ __device__ __forceinline__ void append_worker(const TcParams &T, const TcItem *m
 
 // The fused append's cache stores, by every thread of the CTA once its
 // attention work is done (after the CTA-wide barrier: the ring is free then).
-// Row tile 0 of every chunk the CTA verified (the other row tiles would
-// store the same bytes) owns the chunk's new rows [ap_lo, ap_hi); their
-// 16-byte pieces, K then V per chunk, form one sequence that the threads
+// Each item owns the new rows at its own draft rows' positions inside its
+// chunk (append_range); their 16-byte pieces, K then V per item, form one
+// sequence that the threads
 // stride through with U loads in flight each, so a CTA's stores take about
 // one memory round trip however many chunks it had.  A table of the chunks
 // (sequence, head, rows, first piece) is built in `scratch` first.  No kernel
@@ -603,8 +604,8 @@ __device__ __forceinline__ void append_flush(const TcParams &T, const TcItem *me
             const int j = k0 + k;
             const TcItem it = tc_decode<true>(T, (int)blockIdx.x + j * (int)gridDim.x, j, meta);
             int lo, hi;
-            append_range(P, it.cr, lo, hi);
-            const bool own = it.n_tiles > 0 && it.rt == 0 && lo < hi;
+            append_range(P, it.cr, it.i0, (it.row0 + it.rows - 1) / P.G, lo, hi);
+            const bool own = lo < hi;
             tab[k] = AppendChunk{it.b, it.h, lo, it.cr.qp, own ? 2 * (hi - lo) * PR : 0, 0};
         }
         __syncthreads();

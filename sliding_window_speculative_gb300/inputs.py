@@ -180,6 +180,16 @@ def batched(device="cpu", gen_device=None, **kw):
                      gen_device=gen_device or device, fill="window", **kw)
 
 
+def prefill(q_len, window=188, batch=1, device="cuda", max_len=4096, gen_device=None, **kw):
+    """Sliding-window prefill chunks: `batch` sequences whose last q_len
+    positions form the chunk (contexts U[q_len, max_len], q_pos = seq_len -
+    q_len), single_stream's heads and head_dim."""
+    lens = context_lengths(batch, q_len, max_len)
+    return make_case(f"prefill_q{q_len}", batch, 8, 2, 256, q_len, window, lens, max_len,
+                     outliers=True, device=device, gen_device=gen_device or device,
+                     fill="window", **kw)
+
+
 def stress(window, q_len, device="cuda", batch=512, max_len=32768, gen_device=None, **kw):
     lens = context_lengths(batch, 1024, max_len)
     return make_case(f"stress_w{window}_q{q_len}", batch, 8, 2, 256, q_len, window, lens,

@@ -60,7 +60,7 @@ GOOD = (2, 8, 8, 2, 256, 4096, 0)
 @pytest.mark.parametrize("dims,window,code", [
     ((0, 8, 8, 2, 256, 4096, 0), 188, swa.SWA_ERR_INVALID_ARG),     # batch 0
     ((2, 0, 8, 2, 256, 4096, 0), 188, swa.SWA_ERR_INVALID_ARG),     # q_len 0
-    ((2, 65, 8, 2, 256, 4096, 0), 188, swa.SWA_ERR_INVALID_ARG),    # q_len > 64
+    ((2, 513, 8, 2, 256, 4096, 0), 188, swa.SWA_ERR_INVALID_ARG),   # q_len > 512
     ((2, 8, 8, 3, 256, 4096, 0), 188, swa.SWA_ERR_INVALID_ARG),     # Hq % Hkv
     ((2, 8, 8, 0, 256, 4096, 0), 188, swa.SWA_ERR_INVALID_ARG),     # Hkv 0
     ((2, 8, 8, 2, 96, 4096, 0), 188, swa.SWA_ERR_UNSUPPORTED),      # head_dim
@@ -96,6 +96,8 @@ def test_workspace_bytes(lib):
     (1, 8, 8, 2, 256, 4096, 188), (1, 1, 8, 2, 256, 4096, 188), (1, 1, 8, 2, 256, 4096, 4096),
     (64, 8, 8, 2, 256, 4096, 188), (512, 64, 8, 2, 256, 32768, 1024), (1, 1, 2, 1, 64, 40, 16),
     (3, 64, 16, 2, 256, 1024, 188), (7, 5, 6, 2, 128, 300, 5000),
+    (1, 512, 8, 2, 256, 4096, 188), (2, 300, 8, 2, 64, 1024, 37), (1, 512, 8, 2, 128, 8192, 4096),
+    (4, 200, 16, 2, 256, 2048, 600),
 ])
 @pytest.mark.parametrize("sms", [1, 148, 152])
 def test_plan_invariants(lib, B, q_len, Hq, Hkv, D, L, W, sms):
@@ -211,3 +213,13 @@ def test_append_verify_rejects_bad_arguments(lib):
     short = swa.SwaPaged(160, 10, 16, 100)               # max_len != max_blocks * page_size
     assert call(paged=ctypes.byref(short)) == swa.SWA_ERR_INVALID_ARG
     assert swa.swa_last_error()
+
+
+def test_plan_prefill_chunk_reads_row_windows(lib):
+    # a 512-row prefill chunk at W = 188: a row tile's rows see W + 31 keys,
+    # so no split although the whole span is 699 keys; at W = 4096 the row
+    # tiles' windows (4127 keys) are split to reach the SMs
+    p = swa.swa_plan(swa.make_dims(1, 512, 8, 2, 256, 4096), 188, 152)
+    assert p["kernel"] == 3 and p["row_tiles"] == 16 and p["num_splits"] == 1
+    p = swa.swa_plan(swa.make_dims(1, 512, 8, 2, 128, 8192), 4096, 152)
+    assert p["num_splits"] > 1 and p["chunk_keys"] < 4096 + 31
