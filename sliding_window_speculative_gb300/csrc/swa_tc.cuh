@@ -342,7 +342,11 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
                                               uint8_t *ring, uint8_t *qs, uint64_t *bars) {
     using namespace tc;
     const AttnParams &P = T.a;
-    const uint64_t policy = l2_policy_evict_first();
+    // K/V are read once per row tile: with one row tile nothing reads a line
+    // again (evict first); with several, the row tiles of a (sequence, KV
+    // head) run side by side on neighbouring CTAs and the later ones should
+    // find the lines in L2
+    const uint64_t policy = P.row_tiles > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
     uint32_t f = 0, k = 0;  // fills (two per tile: K then V), items with keys
     uint32_t mix_used = 0, mix_n = 0;  // slots that took a mixed atom; use count parity
     uint32_t uses[NT];              // fills handed to each slot so far
