@@ -25,7 +25,7 @@
 // score MMA (K-major), V the B operand of the PV MMAs (MN-major, N = D).
 //
 // Warp roles (320 threads, 352 under a fused append):
-//   warp 0      TMA producer (one lane)
+//   warp 0      TMA producer (lane 0 runs it; the warp issues a tile's copies)
 //   warp 1      TMEM owner and MMA issuer (one lane)
 //   warps 2..9  softmax / epilogue; warp w owns TMEM lanes 32 (w % 4)..,
 //               i.e. packed rows 32 (w % 4).., and key half (w - 2) / 4 of
@@ -163,8 +163,7 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
 
     if (warp == 0) {
         // ======================================================= producer
-        if (lane == 0)
-            tile_producer<C, NT, QB, AP>(T, M, meta, ftab, ring, qs, bars);
+        tile_producer<C, NT, QB, AP>(T, M, meta, ftab, ring, qs, bars);
     } else if (warp == 1) {
         // ============================================================ MMA
         // Two cursors over the tile sequence: S = Q K^T of the next tile and

@@ -32,7 +32,7 @@
 // and scores proceed.
 //
 // Warp roles (320 threads, 352 under a fused append):
-//   warp 0      TMA producer (one lane)
+//   warp 0      TMA producer (lane 0 runs it; the warp issues a tile's copies)
 //   warp 1      TMEM owner and MMA issuer (one lane)
 //   warps 2..9  softmax / correction / epilogue in two warpgroups that split
 //               the packed rows in halves; within a group a thread owns one
@@ -274,43 +274,39 @@ __device__ __forceinline__ void atom_run(const CUtensorMap *m4, const CUtensorMa
 
 // The copies of one K or V tile: key positions [p, p + n_valid) of
 // (sequence b, KV head h) into ceil(n_valid / 8) atoms of AB bytes at dst,
-// completing on `bar`.  Whole atoms go through the 4D boxes (16, 8, 4 or 2
-// atoms: the rows of a run are consecutive cache rows); a single or a
-// partial atom through the 3D one-atom box, whose rows past the cache the
-// TMA zero-fills.  A contiguous cache is one run; a paged cache breaks runs
-// at page ends (pages hold a multiple of 8 rows and its tiles start on an
-// 8-key boundary, so no atom straddles two pages), and the tile's page ids
-// are read from the block table together, before the first copy.
+// completing on `bar`, issued by the lanes of the producer warp.  Whole
+// atoms go through the 4D boxes (16, 8, 4 or 2 atoms: the rows of a run are
+// consecutive cache rows); a single or a partial atom through the 3D
+// one-atom box, whose rows past the cache the TMA zero-fills.  A contiguous
+// cache is one run (lane 0); a paged cache breaks runs at page ends (pages
+// hold a multiple of 8 rows and its tiles start on an 8-key boundary, so no
+// atom straddles two pages) and lane k reads the page id of run k and
+// issues its copies, so a tile over many small pages costs one round of
+// copies, not one per page.
 template <int AB>
 __device__ __forceinline__ void tile_copies(const AttnParams &P, const TcMaps &M, int kv, int b,
                                             int h, int p, int n_valid, uint8_t *dst, uint64_t *bar,
-                                            uint64_t policy) {
+                                            uint64_t policy, int lane) {
     const CUtensorMap *m4 = kv ? M.v_atoms : M.k_atoms;
     const CUtensorMap *m1 = kv ? &M.v_atom : &M.k_atom;
     const int full = n_valid >> 3, natoms = (n_valid + 7) >> 3;
     if (P.block_table == nullptr) {
-        atom_run<AB>(m4, m1, (int)cache_row(P, b, h, p), full, natoms > full, dst, bar, policy);
+        if (lane == 0)
+            atom_run<AB>(m4, m1, (int)cache_row(P, b, h, p), full, natoms > full, dst, bar,
+                         policy);
         return;
     }
-    constexpr int kMaxRuns = kTcTileKeys / 8 + 1;  // pages of >= 8 rows
-    const int ps = P.page_size, pa = ps >> 3;       // rows, atoms per page
+    const int ps = P.page_size, pa = ps >> 3;           // rows, atoms per page
     const int k0 = p / ps, first = (ps - p % ps) >> 3;  // first page, its atoms
-    const int32_t *trow = P.block_table + (long long)b * P.max_blocks + k0;
-    int pg[kMaxRuns];
-#pragma unroll
-    for (int k = 0; k < kMaxRuns; ++k)
-        if (k == 0 || first + (k - 1) * pa < natoms) pg[k] = __ldg(trow + k);
-#pragma unroll
-    for (int k = 0; k < kMaxRuns; ++k) {
-        const int a = k == 0 ? 0 : first + (k - 1) * pa;  // first atom of run k
-        if (a >= natoms) break;
-        int run = k == 0 ? first : pa;
-        run = run < natoms - a ? run : natoms - a;
-        int whole = full - a;
-        whole = whole < 0 ? 0 : (whole > run ? run : whole);
-        const int y = (pg[k] * P.Hkv + h) * ps + (k == 0 ? p % ps : 0);
-        atom_run<AB>(m4, m1, y, whole, run > whole, dst + a * AB, bar, policy);
-    }
+    const int a = lane == 0 ? 0 : first + (lane - 1) * pa;  // first atom of run `lane`
+    if (a >= natoms) return;
+    int run = lane == 0 ? first : pa;
+    run = run < natoms - a ? run : natoms - a;
+    int whole = full - a;
+    whole = whole < 0 ? 0 : (whole > run ? run : whole);
+    const int pg = __ldg(P.block_table + (long long)b * P.max_blocks + k0 + lane);
+    const int y = (pg * P.Hkv + h) * ps + (lane == 0 ? p % ps : 0);
+    atom_run<AB>(m4, m1, y, whole, run > whole, dst + a * AB, bar, policy);
 }
 
 // How a K/V tile (key positions [p, p + n_valid), ceil(n_valid / 8) atoms)
@@ -328,8 +324,10 @@ __device__ __forceinline__ void append_split(const AttnParams &P, int qp, int p,
     a_n = qp > p && ((qp - p) & 7) ? a_m + 1 : a_m;
 }
 
-// The TMA producer (lane 0 of warp 0) of both tensor-core kernels: for
-// every item of the CTA, its K and V tiles into the first free ring slots
+// The TMA producer (warp 0) of both tensor-core kernels: lane 0 runs the
+// control (slots, barriers, the fill table, Q and the fused append's extra
+// copies) and the warp issues each tile's copies.  For every item of the
+// CTA, its K and V tiles into the first free ring slots
 // (the fill table records where each landed) and its Q rows, issued after
 // the item's first K tile so a single Q buffer does not hold back the K
 // stream.  With a fused append, the atoms of a tile from the first new row
@@ -342,6 +340,7 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
                                               uint8_t *ring, uint8_t *qs, uint64_t *bars) {
     using namespace tc;
     const AttnParams &P = T.a;
+    const int lane = (int)(threadIdx.x & 31);
     // K/V are read once per row tile: with one row tile nothing reads a line
     // again (evict first); with several, the row tiles of a (sequence, KV
     // head) run side by side on neighbouring CTAs and the later ones should
@@ -378,62 +377,73 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
             const bool worker_full = AP && a_n > a_m;  // the append worker completes a mixed atom
             for (int kv = 0; kv < 2 && ok; ++kv) {
                 if (t == 0 && kv == 1) {
-                    ok = load_q();
+                    if (lane == 0) ok = load_q();
+                    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
                     if (!ok) break;
                 }
                 // the first free slot: never used, or its last fill consumed
                 int slot = -1;
                 uint32_t par = 0;
-                const long long w0 = clock64();
-                for (int spin = 0;; ++spin) {
+                if (lane == 0) {
+                    const long long w0 = clock64();
+                    for (int spin = 0;; ++spin) {
 #pragma unroll
-                    for (int s2 = 0; s2 < NT; ++s2) {
-                        if (slot < 0 &&
-                            (uses[s2] == 0 ||
-                             mbar_test(&bars[C::B_EMPTY + s2], (uses[s2] - 1) & 1))) {
-                            slot = s2;
-                            par = uses[s2] & 1;
-                            ++uses[s2];
+                        for (int s2 = 0; s2 < NT; ++s2) {
+                            if (slot < 0 &&
+                                (uses[s2] == 0 ||
+                                 mbar_test(&bars[C::B_EMPTY + s2], (uses[s2] - 1) & 1))) {
+                                slot = s2;
+                                par = uses[s2] & 1;
+                                ++uses[s2];
+                            }
                         }
+                        if (slot >= 0) break;
+                        if (clock64() - w0 > kWaitLimitCycles) {
+                            atomicOr(P.fault, kFaultCopyTimeout);
+                            break;
+                        }
+                        if (spin > 8) __nanosleep(32);
                     }
-                    if (slot >= 0) break;
-                    if (clock64() - w0 > kWaitLimitCycles) {
-                        atomicOr(P.fault, kFaultCopyTimeout);
-                        ok = false;
-                        break;
-                    }
-                    if (spin > 8) __nanosleep(32);
                 }
+                slot = __shfl_sync(0xffffffffu, slot, 0);
+                par = __shfl_sync(0xffffffffu, par, 0);
+                ok = slot >= 0;
                 if (!ok) break;
-                ftab[f % kFillTab] = (f << 8) | (par << 4) | (uint32_t)slot;
+                if (lane == 0) ftab[f % kFillTab] = (f << 8) | (par << 4) | (uint32_t)slot;
                 // a fill completes (FULL) on this lane's arrival with the bytes;
                 // under a fused append it takes a second arrival: this lane's,
                 // or the append worker's after it completed a mixed atom
                 uint64_t *bar = &bars[C::B_FULL + slot];
                 uint8_t *dst = ring + slot * C::TILE_BYTES;
-                mbar_arrive_expect_tx(bar, (uint32_t)(a_m + natoms - a_n) * C::ATOM_BYTES);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(bar, (uint32_t)(a_m + natoms - a_n) * C::ATOM_BYTES);
+                __syncwarp();  // the expected bytes are posted before any copy is issued
                 if (a_m > 0)
                     tile_copies<C::ATOM_BYTES>(P, M, kv, it.b, it.h, p,
                                                a_m < natoms ? 8 * a_m : n_valid, dst, bar,
-                                               policy);
-                for (int a = a_n; a < natoms; ++a)
-                    tma_load_5d(dst + a * C::ATOM_BYTES, kv ? &M.vn_atom : &M.kn_atom, 0,
-                                p + 8 * a - it.cr.qp, 0, it.h, it.b, bar);
-                if (worker_full) {
-                    // the mixed atom from the cache, on its own barrier
-                    uint64_t *mb = &bars[C::B_MIX + slot];
-                    mix_used |= 1u << slot;
-                    mix_n ^= 1u << slot;
-                    mbar_arrive_expect_tx(mb, C::ATOM_BYTES);
-                    tma_load_3d_hint(dst + a_m * C::ATOM_BYTES, kv ? &M.v_atom : &M.k_atom, 0,
-                                     (int)cache_row(P, it.b, it.h, p + 8 * a_m), 0, mb, policy);
-                } else if (AP) {
-                    mbar_arrive(bar);
+                                               policy, lane);
+                if (lane == 0) {
+                    for (int a = a_n; a < natoms; ++a)
+                        tma_load_5d(dst + a * C::ATOM_BYTES, kv ? &M.vn_atom : &M.kn_atom, 0,
+                                    p + 8 * a - it.cr.qp, 0, it.h, it.b, bar);
+                    if (worker_full) {
+                        // the mixed atom from the cache, on its own barrier
+                        uint64_t *mb = &bars[C::B_MIX + slot];
+                        mix_used |= 1u << slot;
+                        mix_n ^= 1u << slot;
+                        mbar_arrive_expect_tx(mb, C::ATOM_BYTES);
+                        tma_load_3d_hint(dst + a_m * C::ATOM_BYTES, kv ? &M.v_atom : &M.k_atom,
+                                         0, (int)cache_row(P, it.b, it.h, p + 8 * a_m), 0, mb,
+                                         policy);
+                    } else if (AP) {
+                        mbar_arrive(bar);
+                    }
                 }
                 ++f;
             }
         }
     }
+    if (lane != 0) return;
     // every copy this CTA issued has landed before it exits
 #pragma unroll
     for (int s2 = 0; s2 < NT; ++s2) {
@@ -745,8 +755,7 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
 
     if (warp == 0) {
         // ======================================================= producer
-        if (lane == 0)
-            tile_producer<C, NT, QB, AP>(T, M, meta, ftab, ring, qs, bars);
+        tile_producer<C, NT, QB, AP>(T, M, meta, ftab, ring, qs, bars);
     } else if (warp == 1) {
         // ============================================================ MMA
         // An event loop over two cursors on the same tile sequence: S = K Q^T
