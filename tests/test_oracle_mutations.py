@@ -47,6 +47,7 @@ PIN_CHECKS = [
     lambda: [pins.test_hand_worked_examples(c) for c in pins._load_golden()],
     lambda: pins.test_brute_force_tiny(8),
     lambda: pins.test_brute_force_gqa_batch_ragged(),
+    lambda: pins.test_brute_force_prefill_block(),
     lambda: pins.test_full_window_is_causal_attention(64, 2, 1, 40, 8),
     lambda: [pins.test_split_merge_identity(n) for n in (2, 3)],
     lambda: pins.test_zero_keys_closed_form(),

@@ -106,6 +106,26 @@ def test_brute_force_gqa_batch_ragged():
     np.testing.assert_allclose(lse, bl, rtol=0, atol=1e-12)
 
 
+def test_brute_force_prefill_block():
+    """A prefill-sized block (more rows than the window): rows near the
+    start see the whole prefix, later rows slide; G=2, ragged lengths."""
+    case = inputs.make_case("pf", 2, 4, 2, 8, 40, 9, [40, 47], 48, seed=12, outliers=True)
+    out, lse = oracle_case(case)
+    bo, bl = brute_force(f64(case.q), f64(case.k_cache), f64(case.v_cache),
+                         case.seq_lens_host, case.q_pos_host, case.window, case.scale)
+    np.testing.assert_allclose(out, bo, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, bl, rtol=0, atol=1e-12)
+
+
+def test_prefill_recipe():
+    """The prefill workload's block is the last q_len positions of each
+    sequence, contexts within [q_len, max_len]."""
+    case = inputs.prefill(64, batch=5, device="cpu", max_len=256)
+    assert case.q.shape == (5, 64, 8, 256)
+    for sl, qp in zip(case.seq_lens_host, case.q_pos_host):
+        assert 64 <= sl <= 256 and qp == sl - 64
+
+
 # ------------------------------------------- W >= context: full causal (SDPA)
 
 @pytest.mark.parametrize("D,Hq,Hkv,ctx,q_len", [(64, 2, 1, 40, 8), (256, 8, 2, 300, 8),
