@@ -1023,9 +1023,10 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
             const int qp_i0 = it.cr.qp + it.i0;  // position of the item's first draft row
             for (int t = 0; t < it.n_tiles; ++t, ++g) {
                 const uint32_t sb = g & 1, suse = g >> 1;
-                ok = !group_any(wg, !mbar_wait_bounded(&bars[C::B_SFULL + sb], suse & 1,
-                                                       P.fault, kFaultCopyTimeout));
-                if (!ok) break;
+                // (a failed wait is voted on together with the raise below: one
+                // group barrier per tile when nothing is raised)
+                const bool got = mbar_wait_bounded(&bars[C::B_SFULL + sb], suse & 1, P.fault,
+                                                   kFaultCopyTimeout);
                 fence_after_sync();
                 const int j0 = it.t0 + kTcTileKeys * t;
                 const int n_valid = min(kTcTileKeys, it.cr.c_hi - j0);
@@ -1067,7 +1068,11 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
                 bool flag = false;
 #pragma unroll
                 for (int r = 0; r < HN; ++r) flag |= v[r] > mref[r] + 8.f;
-                const bool raise = group_any(wg, flag);
+                const bool raise = group_any(wg, flag || !got);
+                if (raise) {
+                    ok = !group_any(wg, !got);
+                    if (!ok) break;
+                }
                 if (raise) {
                     // exact tile maximum per row; raise the references
                     float *rd = red + (g & 1) * 4 * N + r0;
@@ -1101,7 +1106,8 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
                     for (int r = 0; r < HN; ++r) {
                         const float mo = mref[r];
                         const float mn = fmaxf(mo, tm[r]);
-                        const float al = (mn == mo) ? 1.f : fast_exp2(mo - mn);
+                        // (on the item's first tile the row sums are still 0)
+                        const float al = (t == 0 || mn == mo) ? 1.f : fast_exp2(mo - mn);
                         if (gtid == r) my_alpha = al;
                         lrow[r] *= al;
                         mref[r] = mn;
