@@ -99,31 +99,6 @@ __device__ __forceinline__ void bulk_copy_g2s(void *smem_dst, const void *gmem_s
         : "memory");
 }
 
-// 16-byte asynchronous copy global -> shared (L2 only); src_bytes = 0
-// writes zeros instead of reading.  Completion: cp_async_wait_all.
-__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void *gmem_src,
-                                           uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_dst),
-                 "l"(gmem_src), "r"(src_bytes)
-                 : "memory");
-}
-
-// Wait until every cp_async16 of this thread has landed.
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.wait_all;" ::: "memory");
-}
-
-// Same, with an L2 eviction-priority hint (K/V tiles are read once).
-__device__ __forceinline__ void bulk_copy_g2s_hint(void *smem_dst, const void *gmem_src,
-                                                   uint32_t bytes, uint64_t *bar,
-                                                   uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-        "[%0], [%1], %2, [%3], %4;"
-        ::"r"(smem_u32(smem_dst)), "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
