@@ -151,7 +151,8 @@ Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
     } else if (use_tc) {
         p.kernel = 2;
         // rows per item: at most 64 (shared memory holds Q and P tiles beside
-        // the ring; the softmax keeps a row's reference maximum in registers)
+        // the ring; the softmax keeps a row's reference maximum in registers);
+        // fewer when SMs would stay idle (below, once the key split is known)
         const int max_rows = 64;
         p.rows_per_tile = R <= max_rows ? R : (max_rows / G) * G;
         p.q_rows_per_tile = p.rows_per_tile / G;
@@ -194,7 +195,30 @@ Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
         splits = ceil_div(span, chunk);
         p.splits = splits;
         p.chunk = (int)chunk;
-        p.items = (long long)splits * units;
+        if (use_tc && !use_rows && d->num_splits == 0) {
+            // Key-major kernel, key split fixed: cut the rows into smaller
+            // items while SMs would stay idle, so more SMs share each tile's
+            // softmax (the row tiles' extra K/V reads come from L2): 8 rows
+            // while all items fit in half the SMs, else 16 while they fit in
+            // the SMs.  Measured on GB300 (q8, 4:1 GQA, us): W188 one sequence
+            // 9.0 -> 7.5, 8 sequences 9.2 -> 8.0, 16: 9.3 -> 8.3, 32: 9.9 ->
+            // 9.2; W1024 one sequence 10.1 -> 9.0; W4096 one sequence 10.8 ->
+            // 10.6 (16 rows; 8 rows, with fewer key chunks, was 13.0).
+            const long long per_unit = (long long)d->batch * d->num_kv_heads * splits;
+            for (int r : {8, 16}) {
+                const int rows = r < G ? G : (r / G) * G;
+                if (rows >= p.rows_per_tile) break;
+                const long long rt = ceil_div(d->q_len, rows / G);
+                if (per_unit * rt * (r == 8 ? 2 : 1) <= num_sms) {
+                    p.rows_per_tile = rows;
+                    p.q_rows_per_tile = rows / G;
+                    p.row_tiles = (int)rt;
+                    p.tc_n = 16 * ((rows + 15) / 16);
+                    break;
+                }
+            }
+        }
+        p.items = (long long)splits * d->batch * d->num_kv_heads * p.row_tiles;
         const long long slots = (long long)num_sms * ctas_per_sm;
         p.grid = p.items < slots ? p.items : slots;
     } else {
