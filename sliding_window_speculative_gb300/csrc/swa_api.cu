@@ -112,7 +112,7 @@ int forced_kernel() {
 //  - CUDA-core path: enough CTAs to cover every SM about twice, chunks of at
 //    least one 32-key tile.
 // Chunks are multiples of 16 keys; at most kMaxSplits chunks.
-Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
+Plan make_plan_with(const swa_dims *d, int32_t window, int num_sms, int force) {
     Plan p{};
     const int G = d->num_q_heads / d->num_kv_heads;
     const int R = d->q_len * G;
@@ -122,7 +122,6 @@ Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
     if (span > d->max_len) span = d->max_len;
     if (span < 1) span = 1;
 
-    const int force = forced_kernel();
     const bool tc_shape = (D == 128 || D == 256) && G <= 64 &&
                           (long long)d->batch * d->num_kv_heads * d->max_len < (1LL << 31) &&
                           (long long)d->batch * d->q_len < (1LL << 31) &&
@@ -258,6 +257,21 @@ Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
     p.workspace = p.splits > 1 ? (long long)d->batch * d->num_kv_heads * p.splits * R *
                                      ((long long)D + 2) * 4
                                : 0;
+    return p;
+}
+
+// The plan of a call.  More than 32 packed rows go to the rows-major kernel
+// unless the call leaves so many SMs idle that the key-major kernel cuts its
+// rows into 8- or 16-row items: then the key-major plan is taken (measured on
+// GB300, W188: one sequence q16 11.5 -> 7.8 us, q64 12.5 -> 7.9 us; eight
+// sequences q16 11.7 -> 8.2 us).
+Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
+    const int force = forced_kernel();
+    Plan p = make_plan_with(d, window, num_sms, force);
+    if (force == 0 && p.kernel == 3) {
+        const Plan k = make_plan_with(d, window, num_sms, 2);
+        if (k.kernel == 2 && k.rows_per_tile <= 16) return k;
+    }
     return p;
 }
 

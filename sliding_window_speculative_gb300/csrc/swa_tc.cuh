@@ -341,6 +341,12 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
     using namespace tc;
     const AttnParams &P = T.a;
     const int lane = (int)(threadIdx.x & 31);
+    // The warp walks the loop together when a tile's copies are many (paged
+    // cache) or the CTA has one item (latency-bound calls: measured faster);
+    // a long run of items over a contiguous cache is faster with lane 0
+    // alone (no per-fill warp synchronisation).
+    const bool coop = P.block_table != nullptr || T.items <= (int)gridDim.x;
+    if (!coop && lane != 0) return;
     // K/V are read once per row tile: with one row tile nothing reads a line
     // again (evict first); with several, the row tiles of a (sequence, KV
     // head) run side by side on neighbouring CTAs and the later ones should
@@ -378,7 +384,7 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
             for (int kv = 0; kv < 2 && ok; ++kv) {
                 if (t == 0 && kv == 1) {
                     if (lane == 0) ok = load_q();
-                    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+                    if (coop) ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
                     if (!ok) break;
                 }
                 // the first free slot: never used, or its last fill consumed
@@ -405,8 +411,10 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
                         if (spin > 8) __nanosleep(32);
                     }
                 }
-                slot = __shfl_sync(0xffffffffu, slot, 0);
-                par = __shfl_sync(0xffffffffu, par, 0);
+                if (coop) {
+                    slot = __shfl_sync(0xffffffffu, slot, 0);
+                    par = __shfl_sync(0xffffffffu, par, 0);
+                }
                 ok = slot >= 0;
                 if (!ok) break;
                 if (lane == 0) ftab[f % kFillTab] = (f << 8) | (par << 4) | (uint32_t)slot;
@@ -417,7 +425,7 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
                 uint8_t *dst = ring + slot * C::TILE_BYTES;
                 if (lane == 0)
                     mbar_arrive_expect_tx(bar, (uint32_t)(a_m + natoms - a_n) * C::ATOM_BYTES);
-                __syncwarp();  // the expected bytes are posted before any copy is issued
+                if (coop) __syncwarp();  // the expected bytes are posted before any copy
                 if (a_m > 0)
                     tile_copies<C::ATOM_BYTES>(P, M, kv, it.b, it.h, p,
                                                a_m < natoms ? 8 * a_m : n_valid, dst, bar,

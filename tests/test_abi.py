@@ -114,7 +114,9 @@ def test_plan_invariants(lib, B, q_len, Hq, Hkv, D, L, W, sms):
         assert p["grid_ctas"] == units
     else:                                   # persistent grid over the work items
         assert p["kernel"] in (2, 3) and 1 <= p["grid_ctas"] <= min(units, sms)
-        assert p["kernel"] == (3 if R > 32 else 2)   # rows-major above 32 packed rows
+        # rows-major above 32 packed rows, unless few units take small
+        # key-major items
+        assert p["kernel"] == (3 if R > 32 else 2) or (p["kernel"] == 2 and p["rows_per_tile"] <= 16)
         assert p["rows_per_tile"] <= (128 if p["kernel"] == 3 else 64)
         assert p["rows_per_tile"] % (Hq // Hkv) == 0
     assert p["merge"] == (1 if p["num_splits"] > 1 else 0)
@@ -223,3 +225,17 @@ def test_plan_prefill_chunk_reads_row_windows(lib):
     assert p["kernel"] == 3 and p["row_tiles"] == 16 and p["num_splits"] == 1
     p = swa.swa_plan(swa.make_dims(1, 512, 8, 2, 128, 8192), 4096, 152)
     assert p["num_splits"] > 1 and p["chunk_keys"] < 4096 + 31
+
+
+def test_plan_few_units_prefer_small_key_major_items(lib):
+    # few (sequence, KV head) units: the key-major kernel with 8- or 16-row
+    # items, even above 32 packed rows; full batches keep the rows-major kernel
+    for B, q_len, rows in ((1, 8, 8), (1, 16, 8), (1, 64, 8), (8, 16, 16), (16, 8, 16)):
+        p = swa.swa_plan(swa.make_dims(B, q_len, 8, 2, 256, 4096), 188, 152)
+        assert p["kernel"] == 2 and p["rows_per_tile"] == rows, (B, q_len, p)
+        assert p["grid_ctas"] <= 152
+    for B, q_len in ((512, 16), (512, 64), (64, 16), (1, 512)):
+        p = swa.swa_plan(swa.make_dims(B, q_len, 8, 2, 256, 4096), 188, 152)
+        assert p["kernel"] == 3, (B, q_len, p)
+    p = swa.swa_plan(swa.make_dims(64, 8, 8, 2, 256, 4096), 188, 152)
+    assert p["kernel"] == 2 and p["rows_per_tile"] == 32
