@@ -321,10 +321,10 @@ swa_status ensure_workspace(int dev, size_t need, cudaStream_t stream, void **ou
     return SWA_OK;
 }
 
-template <int D, int RPW, int NRG>
-cudaError_t launch_simt(const swa::AttnParams &P, cudaStream_t stream) {
+template <int D, int RPW, int NRG, bool AP>
+cudaError_t launch_simt_ap(const swa::AttnParams &P, cudaStream_t stream) {
     using C = swa::SimtCfg<D, RPW, NRG>;
-    auto kern = swa::swa_simt_kernel<D, RPW, NRG>;
+    auto kern = swa::swa_simt_kernel<D, RPW, NRG, AP>;
     static bool attr_done[kMaxDevices] = {};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -336,6 +336,13 @@ cudaError_t launch_simt(const swa::AttnParams &P, cudaStream_t stream) {
     }
     dim3 grid(P.splits, P.Hkv * P.row_tiles, P.B);
     return swa::launch_kernel(kern, grid, dim3(swa::kSimtThreads), C::SMEM_BYTES, stream, P);
+}
+
+// The plain kernel, or (fused append) its variant.
+template <int D, int RPW, int NRG>
+cudaError_t launch_simt(const swa::AttnParams &P, cudaStream_t stream) {
+    return P.k_new != nullptr ? launch_simt_ap<D, RPW, NRG, true>(P, stream)
+                              : launch_simt_ap<D, RPW, NRG, false>(P, stream);
 }
 
 template <int D>

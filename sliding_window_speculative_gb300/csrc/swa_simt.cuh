@@ -172,7 +172,7 @@ struct SimtCfg {
     static_assert(KB % KPG == 0, "key block must hold whole butterfly groups");
 };
 
-template <int D, int RPW, int NRG>
+template <int D, int RPW, int NRG, bool AP>
 __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams P) {
     using C = SimtCfg<D, RPW, NRG>;
     constexpr int DPL = C::DPL;
@@ -203,11 +203,14 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
 
 
     // keys read from k_new / v_new (every position >= q_pos under an append)
-    // and the new rows this CTA stores to the cache
-    const int nw_lo = cr.c_lo > cr.qp ? cr.c_lo : cr.qp;
-    const int nw_hi = P.k_new != nullptr && cr.c_hi > nw_lo ? cr.c_hi : nw_lo;
-    int ap_lo, ap_hi;
-    append_range(P, cr, i_first, i_last, ap_lo, ap_hi);
+    // and the new rows this CTA stores to the cache; both empty in the plain
+    // variant (AP false)
+    int nw_lo = 0, nw_hi = 0, ap_lo = 0, ap_hi = 0;
+    if constexpr (AP) {
+        nw_lo = cr.c_lo > cr.qp ? cr.c_lo : cr.qp;
+        nw_hi = cr.c_hi > nw_lo ? cr.c_hi : nw_lo;
+        append_range(P, cr, i_first, i_last, ap_lo, ap_hi);
+    }
     auto issue = [&](int t) {
         const int s = t % C::STAGES;
         const int j0 = cr.c_lo + t * kSimtTileKeys;
@@ -220,14 +223,14 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
         // is one copy from k_new / v_new
         for (int j = j0; j < j0 + n;) {
             const uint32_t off = (uint32_t)(j - j0) * D * 2;
-            if (j >= nw_lo && j < nw_hi) {
+            if (AP && j >= nw_lo && j < nw_hi) {
                 const size_t src = (((size_t)b * P.q_len + (j - cr.qp)) * P.Hkv + h) * D;
                 bulk_copy_g2s(dst + off, P.k_new + src, D * 2, &full[s]);
                 bulk_copy_g2s(dst + C::TILE_BYTES + off, P.v_new + src, D * 2, &full[s]);
                 ++j;
                 continue;
             }
-            int run = (nw_lo < nw_hi && j < nw_lo && nw_lo < j0 + n ? nw_lo : j0 + n) - j;
+            int run = (AP && nw_lo < nw_hi && j < nw_lo && nw_lo < j0 + n ? nw_lo : j0 + n) - j;
             if (P.block_table != nullptr) {
                 const int left = P.page_size - j % P.page_size;
                 run = run < left ? run : left;
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
         const __nv_bfloat16 *Vs = Ks + kSimtTileKeys * D;
         const int j0 = cr.c_lo + t * kSimtTileKeys;
         const int n = min(kSimtTileKeys, cr.c_hi - j0);
-        {
+        if constexpr (AP) {
             // the fused append's new rows of this tile that this CTA owns, from
             // the stage to the cache
             const int r0 = max(ap_lo, j0) - j0, r1 = min(ap_hi, j0 + n) - j0;
