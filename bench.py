@@ -570,6 +570,9 @@ def launch_floor(steps, graph_len=1000):
     return start.elapsed_time(end) * 1e3 / (reps * n)
 
 
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal bandwidth
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -590,7 +593,8 @@ def main():
     ap.add_argument("--splits", type=int, default=0, help="force a split count (0 = heuristic)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--also", default="batched,stress_w188_q8",
+    ap.add_argument("--also",
+                    default="tiny_q8,window_vs_full_w188,window_vs_full_w4096,batched,stress_w188_q8",
                     help="extra workloads measured the same way (rank 0, device time)")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     args = ap.parse_args()
@@ -648,6 +652,8 @@ def main():
                      (" + swa_merge_kernel" if plan["merge"] else ""),
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                     "nominal_peak": NOMINAL_HBM_GBS,
+                     "frac_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "traffic": traffic,
                      "traffic_source": ("profiles/traffic.json (ncu dram__bytes_read.sum + "
                                         "dram__bytes_write.sum per launch)" if traffic else
@@ -680,6 +686,7 @@ def main():
                           "us_per_call": round(r2["us_per_call"], 3),
                           "kv_gbs": round(k2 / (r2["us_per_call"] * 1e-6) / 1e9, 2),
                           "achieved_gbs": round(ach, 2), "frac": round(ach / peak, 4),
+                          "frac_nominal": round(ach / NOMINAL_HBM_GBS, 4),
                           "steps": steps2, "replicas": r2["replicas"],
                           "splits": p2["num_splits"], "traffic": ncu_traffic(name)[0]}
             del c2
