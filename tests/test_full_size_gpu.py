@@ -6,7 +6,10 @@ checks a seeded subset of sequences of each launch.
 - the bandwidth-stress batch (512 sequences, cache 32768) on a paged cache
   of 16-row pages, the pool shuffled as in the bench;
 - the fused KV append on the bandwidth-stress batch: the sampled sequences'
-  new cache rows bit for bit, and their outputs.
+  new cache rows bit for bit, and their outputs;
+- the plain verify call on the bandwidth-stress batch at draft lengths 1 and
+  8 for every window: all 512 sequences, not a sample (the oracle needs a
+  few seconds per case: each sequence reads at most W + 7 keys).
 """
 import numpy as np
 import pytest
@@ -109,4 +112,15 @@ def test_append_stress_full_size_sampled():
         exp_v = oracle.append_rows(before_v, rows_v, [qp - lo], [sl - lo])
         assert np.array_equal(blk_k, exp_k) and np.array_equal(blk_v, exp_v), b
     del case, k_new, v_new
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("window", [188, 512, 1024])
+@pytest.mark.parametrize("q_len", [1, 8])
+def test_stress_every_sequence(window, q_len):
+    case = inputs.stress(window, q_len)
+    out, lse = run_gpu(case)
+    ref_o, ref_l = oracle_reference(case)
+    compare(out, lse, ref_o, ref_l, f"stress_w{window}_q{q_len}, all sequences")
+    del case, out, lse
     torch.cuda.empty_cache()
