@@ -718,6 +718,10 @@ def main():
         cb = oracle_sample(case, args.cpu_budget)
         line["cpu_baseline"] = {"value": round(cb["kv_gbs"], 6), "unit": UNIT,
                                 "cores": cb["cores"], "kind": "oracle", "sample": cb["sample"]}
+        # the same oracle on one host thread, over a shorter sample
+        c1 = oracle_sample(case, max(1.0, args.cpu_budget / 3), threads=1)
+        line["cpu_baseline"]["single_thread"] = {"value": round(c1["kv_gbs"], 6), "unit": UNIT,
+                                                 "cores": 1, "sample": c1["sample"]}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
