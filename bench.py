@@ -287,48 +287,60 @@ def time_device(case, steps, warmup, num_splits=0, graph_len=1000, dist=None, ap
             "l2_bytes": l2, "wall": (t0, t1), "kv_bytes": kv, "bytes": total}
 
 
+def _packed(parts, device=None, pin=False, align=256):
+    """One byte buffer holding tensors of the given (shape, dtype) at
+    `align`-byte offsets; returns (buffer, views)."""
+    offs, n = [], 0
+    for shape, dtype in parts:
+        offs.append(n)
+        nbytes = math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+        n = (n + nbytes + align - 1) // align * align
+    buf = torch.empty(n, dtype=torch.uint8, device=device)
+    if pin:
+        buf = buf.pin_memory()
+    views = []
+    for (shape, dtype), o in zip(parts, offs):
+        nbytes = math.prod(shape) * torch.empty((), dtype=dtype).element_size()
+        views.append(buf[o:o + nbytes].view(dtype).view(shape))
+    return buf, views
+
+
 def time_e2e(case, steps, warmup):
-    """Through the public call with host buffers: each step copies q,
-    seq_lens, q_pos and the q_len new K/V rows per (sequence, KV head) from
-    pinned host memory, calls swa_verify_attn, and copies out and lse back to
-    pinned host memory.  Timed with CUDA events around all steps."""
-    from sliding_window_speculative_gb300 import swa_verify_attn
+    """Through the public call with host buffers: each step copies the
+    step's inputs (q, the q_len new K/V rows of every sequence and KV head,
+    seq_lens, q_pos), packed in one pinned host buffer, to the device in one
+    copy; calls swa_append_verify_attn, which writes the new rows into the
+    cache and attends over it; and copies out and lse, packed in one device
+    buffer, back to pinned host memory in one copy.  Timed with CUDA events
+    around all steps."""
+    from sliding_window_speculative_gb300 import swa_append_verify_attn
     B, q_len, Hq, D = case.q.shape
     Hkv = case.k_cache.shape[1]
-    h_q = case.q.cpu().pin_memory()
-    h_sl = case.seq_lens.cpu().pin_memory()
-    h_qp = case.q_pos.cpu().pin_memory()
-    # new K/V rows: [B, Hkv, q_len, D] at positions q_pos .. q_pos + q_len
-    rows_k = torch.stack([case.k_cache[b, :, p:p + q_len] for b, p in
-                          enumerate(case.q_pos_host)]).cpu().pin_memory()
-    rows_v = torch.stack([case.v_cache[b, :, p:p + q_len] for b, p in
-                          enumerate(case.q_pos_host)]).cpu().pin_memory()
-    d_q = torch.empty_like(case.q)
-    d_sl = torch.empty_like(case.seq_lens)
-    d_qp = torch.empty_like(case.q_pos)
-    d_rows_k = torch.empty(rows_k.shape, dtype=rows_k.dtype, device=case.q.device)
-    d_rows_v = torch.empty_like(d_rows_k)
-    out = torch.empty_like(case.q)
-    lse = torch.empty((B, q_len, Hq), dtype=torch.float32, device=case.q.device)
-    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    dev = case.q.device
+    rows = (B, q_len, Hkv, D)
+    parts_in = [(tuple(case.q.shape), torch.bfloat16), (rows, torch.bfloat16),
+                (rows, torch.bfloat16), ((B,), torch.int32), ((B,), torch.int32)]
+    h_in, (h_q, h_kn, h_vn, h_sl, h_qp) = _packed(parts_in, pin=True)
+    d_in, (d_q, d_kn, d_vn, d_sl, d_qp) = _packed(parts_in, device=dev)
+    h_q.copy_(case.q.cpu())
+    h_sl.copy_(case.seq_lens.cpu())
+    h_qp.copy_(case.q_pos.cpu())
+    for b, p in enumerate(case.q_pos_host):
+        # the block's rows as the cache holds them: [q_len, Hkv, D]
+        h_kn[b].copy_(case.k_cache[b, :, p:p + q_len].transpose(0, 1).cpu())
+        h_vn[b].copy_(case.v_cache[b, :, p:p + q_len].transpose(0, 1).cpu())
+    parts_out = [(tuple(case.q.shape), torch.bfloat16), ((B, q_len, Hq), torch.float32)]
+    d_out, (out, lse) = _packed(parts_out, device=dev)
+    h_out, (h_o, h_l) = _packed(parts_out, pin=True)
     stream = torch.cuda.Stream()
-    h2d = (h_q.numel() * 2 + h_sl.numel() * 4 + h_qp.numel() * 4 + rows_k.numel() * 2 * 2)
-    d2h = out.numel() * 2 + lse.numel() * 4
+    h2d = h_in.numel()
+    d2h = h_out.numel()
 
     def step():
-        d_q.copy_(h_q, non_blocking=True)
-        d_sl.copy_(h_sl, non_blocking=True)
-        d_qp.copy_(h_qp, non_blocking=True)
-        d_rows_k.copy_(rows_k, non_blocking=True)
-        d_rows_v.copy_(rows_v, non_blocking=True)
-        for b, p in enumerate(case.q_pos_host):
-            case.k_cache[b, :, p:p + q_len].copy_(d_rows_k[b], non_blocking=True)
-            case.v_cache[b, :, p:p + q_len].copy_(d_rows_v[b], non_blocking=True)
-        swa_verify_attn(d_q, case.k_cache, case.v_cache, d_sl, d_qp, case.window, case.scale,
-                        out=out, lse=lse)
-        h_out.copy_(out, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
+        swa_append_verify_attn(d_q, d_kn, d_vn, case.k_cache, case.v_cache, d_sl, d_qp,
+                               case.window, case.scale, out=out, lse=lse, stream=stream)
+        h_out.copy_(d_out, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(max(warmup, 3)):
@@ -344,7 +356,8 @@ def time_e2e(case, steps, warmup):
         end.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(end)
-    return {"us_per_call": ms * 1e3 / steps, "h2d": h2d, "d2h": d2h, "steps": steps}
+    return {"us_per_call": ms * 1e3 / steps, "h2d": h2d, "d2h": d2h, "steps": steps,
+            "out": h_o, "lse": h_l}
 
 
 # ------------------------------------------------------------ CPU oracle
