@@ -596,6 +596,43 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def tensor_peak():
+    """Dense bf16 TFLOP/s for a kernel timed alone (burst), and its source."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def extra_entry(name, dev, peak, tpeak, sms, steps=None):
+    """One more workload measured like the main one (device time, graph
+    replay, L2 defeated): time per call, HBM and tensor-pipe fractions of
+    the peaks, and the plan the library picks for it."""
+    import sliding_window_speculative_gb300 as swa
+    case = make_workload(name, dev)
+    kv, total = workload_bytes(case)
+    steps = steps or max(50, min(2000, int(0.3e9 / max(total, 1))))
+    r = time_device(case, steps, 5)
+    plan = swa.swa_plan(swa.dims_of(case.q, case.k_cache), case.window, sms)
+    sec = r["us_per_call"] * 1e-6
+    ach = total / sec / 1e9
+    tf = workload_flops(case) / sec / 1e12
+    entry = {"kernel": KERNEL_NAMES.get(plan["kernel"], "?"),
+             "us_per_call": round(r["us_per_call"], 3),
+             "kv_gbs": round(kv / sec / 1e9, 2),
+             "achieved_gbs": round(ach, 2), "frac": round(ach / peak, 4),
+             "frac_nominal": round(ach / NOMINAL_HBM_GBS, 4),
+             "useful_tflops": round(tf, 3), "tensor_frac": round(tf / tpeak, 5),
+             "tokens_per_s": round(case.q.shape[0] * case.q.shape[1] / sec),
+             "steps": steps, "replicas": r["replicas"],
+             "splits": plan["num_splits"], "traffic": ncu_traffic(name)[0]}
+    del case
+    torch.cuda.empty_cache()
+    return entry
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -646,6 +683,7 @@ def main():
     us = seconds * 1e6 / args.steps
 
     peak, peak_src = peaks()
+    tpeak, _ = tensor_peak()
     launches_per_call = 1 + plan["merge"]
     achieved = total / (us * 1e-6) / 1e9
     traffic, traffic_kernel = ncu_traffic(args.workload)
@@ -686,44 +724,17 @@ def main():
                        "us_per_call": round(e["us_per_call"], 3),
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
     if rank == 0 and world == 1 and args.also:
-        also = {}
-        for name in [a for a in args.also.split(",") if a and a != args.workload]:
-            c2 = make_workload(name, dev)
-            k2, t2 = workload_bytes(c2)
-            steps2 = max(50, min(2000, int(0.3e9 / max(t2, 1))))
-            r2 = time_device(c2, steps2, 5)
-            p2 = swa.swa_plan(swa.dims_of(c2.q, c2.k_cache), c2.window,
-                              torch.cuda.get_device_properties(dev).multi_processor_count)
-            ach = t2 / (r2["us_per_call"] * 1e-6) / 1e9
-            also[name] = {"kernel": KERNEL_NAMES.get(p2["kernel"], "?"),
-                          "us_per_call": round(r2["us_per_call"], 3),
-                          "kv_gbs": round(k2 / (r2["us_per_call"] * 1e-6) / 1e9, 2),
-                          "achieved_gbs": round(ach, 2), "frac": round(ach / peak, 4),
-                          "frac_nominal": round(ach / NOMINAL_HBM_GBS, 4),
-                          "steps": steps2, "replicas": r2["replicas"],
-                          "splits": p2["num_splits"], "traffic": ncu_traffic(name)[0]}
-            del c2
-            torch.cuda.empty_cache()
-        line["also"] = also
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        line["also"] = {name: extra_entry(name, dev, peak, tpeak, sms)
+                        for name in args.also.split(",") if name and name != args.workload}
         # greedy verification of the draft block over a Gemma-size vocabulary
         # (one sequence, and a 64-sequence batch)
         line["accept"] = [time_accept(1, 8, 262144), time_accept(64, 8, 262144, steps=500)]
         # the bandwidth-stress batch (inputs larger than L2) on a paged cache
         line["paged"] = [time_paged("stress_w188_q8", 16), time_paged("stress_w188_q8", 64)]
         # sliding-window prefill chunks of 512 tokens (one sequence, and 64)
-        pre = {}
-        for name in ("prefill_q512", "prefill_q512_b64"):
-            c2 = make_workload(name, dev)
-            k2, t2 = workload_bytes(c2)
-            r2 = time_device(c2, 200, 5)
-            ach = t2 / (r2["us_per_call"] * 1e-6) / 1e9
-            pre[name] = {"us_per_call": round(r2["us_per_call"], 3),
-                         "achieved_gbs": round(ach, 2), "frac": round(ach / peak, 4),
-                         "tokens_per_s": round(c2.q.shape[0] * c2.q.shape[1] /
-                                               (r2["us_per_call"] * 1e-6))}
-            del c2
-            torch.cuda.empty_cache()
-        line["prefill"] = pre
+        line["prefill"] = {name: extra_entry(name, dev, peak, tpeak, sms, steps=200)
+                           for name in ("prefill_q512", "prefill_q512_b64")}
         # the cache write of the verify block fused into the attention call
         line["append"] = [time_append("single_stream"), time_append("batched"),
                           time_append("stress_w188_q8", steps=200)]
