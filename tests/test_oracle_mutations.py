@@ -41,6 +41,28 @@ MUTATIONS = {
                            "const double *src = rows + ((b * Hkv + h) * q_len + i) * D;"),
     # row i lands one position late
     "append_row_offset": ("const int64_t pos = q_pos[b] + i;", "const int64_t pos = q_pos[b] + i + 1;"),
+    # the window holds W-1 keys (the query's own key dropped at the far edge)
+    "window_short": ("int64_t a = p - window + 1;", "int64_t a = p - window + 2;"),
+    # rows past the cached context see the key at seq_len
+    "seq_len_clip_inclusive": ("*hi = p < seq_len - 1 ? p : seq_len - 1;",
+                               "*hi = p < seq_len ? p : seq_len;"),
+    # the score misses the scale
+    "scale_dropped": ("s[j - lo] = J->scale * dot;", "s[j - lo] = dot;"),
+    # softmax weights not divided by their sum
+    "weights_unnormalised": ("const double w = s[j - lo] / z; /* = exp(s_j - lse) */",
+                             "const double w = s[j - lo];"),
+    # lse reported in log2 units
+    "lse_log2": ("J->lse[row] = m + log(z);", "J->lse[row] = (m + log(z)) / log(2.0);"),
+    # a partial's key range includes its end key (chunks overlap by one)
+    "partial_range_inclusive": ("if (hi > J->c_hi[b] - 1) hi = J->c_hi[b] - 1;",
+                                "if (hi > J->c_hi[b]) hi = J->c_hi[b];"),
+    # the merge's denominator forgets the partials' rescaling
+    "merge_lambda_unscaled": ("Lam += l[k * rows + r] * w;", "Lam += l[k * rows + r];"),
+    # the accepted count includes the bonus token
+    "accept_counts_bonus": ("accepted[b] = n;", "accepted[b] = n + 1;"),
+    # the keep set's relabelling skipped
+    "accept_keep_ignored": ("argmax[b * q_len + i] = keep ? keep[jbest] : jbest;",
+                            "argmax[b * q_len + i] = jbest;"),
 }
 
 PIN_CHECKS = [
