@@ -583,6 +583,27 @@ def launch_floor(steps, graph_len=1000):
     return start.elapsed_time(end) * 1e3 / (reps * n)
 
 
+def launch_floor_stream(steps):
+    """Per-launch time of the same one-element kernel launched from the host
+    one call at a time (no graph): the floor of an eager caller."""
+    x = torch.zeros(1, device="cuda")
+    stream = torch.cuda.Stream()
+    n = max(1, min(steps, 2000))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            x.add_(1.0)
+    stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(n):
+            x.add_(1.0)
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) * 1e3 / n
+
+
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal bandwidth
 
 
@@ -688,6 +709,7 @@ def main():
     achieved = total / (us * 1e-6) / 1e9
     traffic, traffic_kernel = ncu_traffic(args.workload)
     floor_us = launch_floor(args.steps) if rank == 0 else None
+    floor_stream_us = launch_floor_stream(args.steps) if rank == 0 else None
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3,
@@ -711,10 +733,14 @@ def main():
                                         ("stale: kernel sources changed since the capture"
                                          if traffic_kernel == "stale" else None)),
                      "launch_floor_us": round(floor_us, 3) if floor_us else None,
+                     "launch_floor_stream_us": (round(floor_stream_us, 3)
+                                                if floor_stream_us else None),
                      "floor_frac": round(floor_us * launches_per_call / us, 4) if floor_us else None,
                      "note": "achieved = algorithmic bytes per call / device time per call "
                              "(one attention kernel per call when the plan does not split); "
-                             "floor_frac = launch floor x kernels per call / time per call"},
+                             "floor_frac = launch floor x kernels per call / time per call; "
+                             "launch floors: a one-element kernel replayed from a CUDA graph, "
+                             "and launched from the host one call at a time"},
         "clocks": clocks,
         "gpu_launches": launches_per_call * args.steps,
     }
