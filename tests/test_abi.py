@@ -217,6 +217,27 @@ def test_append_verify_rejects_bad_arguments(lib):
     assert swa.swa_last_error()
 
 
+def test_paged_verify_rejects_bad_tables(lib):
+    # every case fails on the host, before any CUDA call
+    d = swa.make_dims(*GOOD)                              # max_len 4096, Hkv 2
+
+    def call(paged, q=48):
+        return lib.swa_verify_attn_paged(q, 16, 32, ctypes.byref(paged) if paged else None,
+                                         96, 112, 188, 0.0625, 128, None, ctypes.byref(d), None)
+
+    assert call(None) == swa.SWA_ERR_INVALID_ARG                       # no description
+    assert call(swa.SwaPaged(None, 256, 16, 100)) == swa.SWA_ERR_INVALID_ARG   # no table
+    assert call(swa.SwaPaged(162, 256, 16, 100)) == swa.SWA_ERR_INVALID_ARG    # table misaligned
+    assert call(swa.SwaPaged(160, 1024, 4, 100)) == swa.SWA_ERR_INVALID_ARG    # pages of 4 rows
+    assert call(swa.SwaPaged(160, 0, 16, 100)) == swa.SWA_ERR_INVALID_ARG      # no blocks
+    assert call(swa.SwaPaged(160, 256, 16, 0)) == swa.SWA_ERR_INVALID_ARG      # empty pool
+    assert call(swa.SwaPaged(160, 128, 16, 100)) == swa.SWA_ERR_INVALID_ARG    # 2048 != max_len
+    # 2^20 pages x 2 KV heads x 1024 rows = 2^31 pool rows
+    assert call(swa.SwaPaged(160, 4, 1024, 1 << 20)) == swa.SWA_ERR_UNSUPPORTED
+    assert call(swa.SwaPaged(160, 256, 16, 100), q=None) == swa.SWA_ERR_INVALID_ARG
+    assert "page" in swa.swa_last_error() or "NULL" in swa.swa_last_error()
+
+
 def test_plan_prefill_chunk_reads_row_windows(lib):
     # a 512-row prefill chunk at W = 188: a row tile's rows see W + 31 keys,
     # so no split although the whole span is 699 keys; at W = 4096 the row
