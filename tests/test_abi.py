@@ -260,3 +260,27 @@ def test_plan_few_units_prefer_small_key_major_items(lib):
         assert p["kernel"] == 3, (B, q_len, p)
     p = swa.swa_plan(swa.make_dims(64, 8, 8, 2, 256, 4096), 188, 152)
     assert p["kernel"] == 2 and p["rows_per_tile"] == 32
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    from sliding_window_speculative_gb300 import _binding
+    monkeypatch.setattr(_binding, "_lib", None)
+    with pytest.raises(ImportError, match="no CPU fallback"):
+        _binding.load_library(str(tmp_path / "libswa.so"))
+
+
+def test_last_error_is_per_thread(lib):
+    import threading
+    got = {}
+    barrier = threading.Barrier(2)
+
+    def worker(name, dims, window):
+        assert _call_raw(lib, dims, window) == swa.SWA_ERR_INVALID_ARG
+        barrier.wait()          # both calls have failed before either reads
+        got[name] = swa.swa_last_error()
+
+    t1 = threading.Thread(target=worker, args=("batch", (0, 8, 8, 2, 256, 4096, 0), 188))
+    t2 = threading.Thread(target=worker, args=("window", GOOD, 0))
+    t1.start(); t2.start(); t1.join(); t2.join()
+    assert "batch" in got["batch"] and "window" in got["window"]
+    assert got["batch"] != got["window"]
