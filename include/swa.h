@@ -208,7 +208,6 @@ swa_status swa_read_device_errors(uint32_t *flags);
 /* Library version, e.g. "swa 0.1.0 sm_103a". */
 const char *swa_version(void);
 
-/* Bytes of the fixed device scratch used by swa_verify_attn_noalloc. */
 /* Greedy verification of a draft block: the argmax of every verify row's
  * logits (FUSED_SPARSE_ARGMAX, with the keep set of a pruned LM head) and
  * the number of drafted tokens accepted (SPECULATIVE_CONFIG's drafts), in
@@ -242,6 +241,7 @@ swa_status swa_greedy_accept(const void *logits, const int32_t *keep_ids, const 
                              int32_t *argmax_out, int32_t *accepted, int32_t batch,
                              int32_t q_len, int32_t vocab, swa_stream_t stream);
 
+/* Bytes of the fixed device scratch used by swa_verify_attn_noalloc. */
 #define SWA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 
 /* Allocation-free variant of swa_verify_attn (no counterpart on the pages:
