@@ -52,3 +52,51 @@ def test_plain_c_program_uses_the_library(tmp_path):
     run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert run.returncode == 0, (run.returncode, run.stdout, run.stderr)
     assert "kernel 2" in run.stdout
+
+
+LAYOUT = r"""
+#include <stddef.h>
+#include <stdio.h>
+#include "swa.h"
+#define F(T, f) printf(#T "." #f " %zu %zu\n", offsetof(T, f), sizeof(((T *)0)->f))
+int main(void) {
+    printf("swa_dims %zu\nswa_paged %zu\nswa_plan_info %zu\n", sizeof(swa_dims),
+           sizeof(swa_paged), sizeof(swa_plan_info));
+    F(swa_dims, batch); F(swa_dims, q_len); F(swa_dims, num_q_heads);
+    F(swa_dims, num_kv_heads); F(swa_dims, head_dim); F(swa_dims, max_len);
+    F(swa_dims, num_splits);
+    F(swa_paged, block_table); F(swa_paged, max_blocks); F(swa_paged, page_size);
+    F(swa_paged, num_pages);
+    F(swa_plan_info, kernel); F(swa_plan_info, num_splits); F(swa_plan_info, chunk_keys);
+    F(swa_plan_info, row_tiles); F(swa_plan_info, rows_per_tile); F(swa_plan_info, grid_ctas);
+    F(swa_plan_info, merge); F(swa_plan_info, workspace_bytes);
+    return 0;
+}
+"""
+
+
+def test_binding_structs_match_the_c_layout(tmp_path):
+    """The ctypes mirrors of the header's structs have the C compiler's
+    size, field offsets and field sizes."""
+    import ctypes
+
+    from sliding_window_speculative_gb300 import _binding
+    src = tmp_path / "layout.c"
+    src.write_text(LAYOUT)
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o",
+                    str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout
+    mirrors = {"swa_dims": _binding.SwaDims, "swa_paged": _binding.SwaPaged,
+               "swa_plan_info": _binding.SwaPlanInfo}
+    seen = 0
+    for line in out.splitlines():
+        parts = line.split()
+        if "." not in parts[0]:
+            assert ctypes.sizeof(mirrors[parts[0]]) == int(parts[1]), line
+        else:
+            struct, field = parts[0].split(".")
+            desc = getattr(mirrors[struct], field)
+            assert (desc.offset, desc.size) == (int(parts[1]), int(parts[2])), line
+        seen += 1
+    assert seen == 3 + 7 + 4 + 8
