@@ -100,3 +100,46 @@ def test_binding_structs_match_the_c_layout(tmp_path):
             assert (desc.offset, desc.size) == (int(parts[1]), int(parts[2])), line
         seen += 1
     assert seen == 3 + 7 + 4 + 8
+
+
+def _prototypes():
+    """(return type, name, [parameter types]) of every function include/swa.h
+    declares, comments removed."""
+    import re
+    text = open(os.path.join(ROOT, "include", "swa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"#[^\n]*\n", "\n", text)
+    protos = []
+    for ret, name, params in re.findall(r"([A-Za-z_][\w \*]*?)\s*\b(swa_\w+)\s*\(([^)]*)\)\s*;",
+                                        text):
+        ps = [p.strip() for p in params.split(",") if p.strip() and p.strip() != "void"]
+        types = [re.sub(r"\s*\b\w+$", "", p) if not p.endswith("*") else p for p in ps]
+        protos.append((ret.strip(), name, types))
+    return protos
+
+
+def test_binding_signatures_match_the_header():
+    """Every declared function's ctypes argtypes / restype agree with the
+    header's parameter types: pointers as pointers, int32_t as c_int32,
+    float as c_float, size_t as c_size_t."""
+    import ctypes
+
+    from sliding_window_speculative_gb300 import build, load_library
+    build.build()
+    lib = load_library()
+    protos = _prototypes()
+    assert len(protos) >= 12
+    for ret, name, types in protos:
+        fn = getattr(lib, name)
+        assert fn.argtypes is not None and len(fn.argtypes) == len(types), (name, types)
+        for c_t, py_t in zip(types, fn.argtypes):
+            if "*" in c_t or c_t == "swa_stream_t":
+                assert py_t in (ctypes.c_void_p, ctypes.c_char_p) or \
+                    issubclass(py_t, ctypes._Pointer), (name, c_t, py_t)
+            else:
+                want = {"int32_t": ctypes.c_int32, "float": ctypes.c_float,
+                        "size_t": ctypes.c_size_t}[c_t]
+                assert py_t is want, (name, c_t, py_t)
+        want_ret = {"swa_status": ctypes.c_int, "size_t": ctypes.c_size_t,
+                    "const char *": ctypes.c_char_p}[ret]
+        assert fn.restype is want_ret, (name, ret, fn.restype)
