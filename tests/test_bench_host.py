@@ -37,3 +37,31 @@ def test_extra_entry_from_a_fixed_time(monkeypatch):
     assert e["useful_tflops"] == pytest.approx(flops / 10e-6 / 1e12, abs=1e-3)
     assert e["tokens_per_s"] == 800_000
     assert e["kernel"] == "swa_tc_kernel" and e["splits"] == 1
+
+
+def test_ncu_traffic_only_for_the_captured_sources(monkeypatch):
+    import json
+    import os
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        d = json.load(f)
+    monkeypatch.setattr(bench, "source_digest", lambda: d["source_sha"])
+    n, kernel = bench.ncu_traffic("single_stream")
+    assert n == d["workloads"]["single_stream"]["dram_bytes_per_launch"]
+    assert kernel == "swa_tc_kernel"
+    assert bench.ncu_traffic("no_such_workload") == (None, None)
+    # once the kernel sources change, the capture no longer applies
+    monkeypatch.setattr(bench, "source_digest", lambda: "0" * 16)
+    assert bench.ncu_traffic("single_stream") == (None, "stale")
+
+
+def test_source_digest_covers_the_kernel_sources(tmp_path, monkeypatch):
+    import os
+    import shutil
+    pkg = tmp_path / "sliding_window_speculative_gb300"
+    shutil.copytree(os.path.join(bench.ROOT, "sliding_window_speculative_gb300", "csrc"),
+                    pkg / "csrc")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    before = bench.source_digest()
+    with open(pkg / "csrc" / "swa_tc.cuh", "a") as f:
+        f.write("\n")
+    assert bench.source_digest() != before
