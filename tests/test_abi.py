@@ -98,6 +98,10 @@ def test_workspace_bytes(lib):
     (3, 64, 16, 2, 256, 1024, 188), (7, 5, 6, 2, 128, 300, 5000),
     (1, 512, 8, 2, 256, 4096, 188), (2, 300, 8, 2, 64, 1024, 37), (1, 512, 8, 2, 128, 8192, 4096),
     (4, 200, 16, 2, 256, 2048, 600),
+    # large query groups and odd head ratios, the largest batch
+    (1, 8, 64, 1, 128, 1024, 188), (3, 1, 32, 1, 256, 512, 188), (2, 64, 64, 1, 256, 2048, 188),
+    (5, 3, 48, 4, 128, 777, 100), (65535, 1, 8, 2, 256, 16, 8), (2, 17, 24, 8, 64, 300, 50),
+    (4, 64, 128, 2, 128, 1024, 1024),
 ])
 @pytest.mark.parametrize("sms", [1, 148, 152])
 def test_plan_invariants(lib, B, q_len, Hq, Hkv, D, L, W, sms):
