@@ -23,6 +23,19 @@ Algorithmic bytes per call = sum over sequences of
 + 4 * q_len * Hq          (lse)
 with S_b = min(q_pos + q_len, seq_len) - max(0, q_pos - W + 1).
 
+Beside the timed value, rank 0 of a one-GPU run reports:
+  e2e        the same metric per step of a caller with host buffers: one
+             packed input copy from pinned memory, the fused append + verify
+             call, one packed output copy back (copies inside the timed region);
+  roofline   the dominant kernel's achieved GB/s against the measured copy
+             bandwidth and the nominal 7.9 TB/s, its ncu DRAM traffic per
+             launch while the kernel sources match the capture, and the launch
+             floors;
+  also, prefill, paged, append, accept
+             the other workloads and entry points, measured the same way;
+  cpu_baseline
+             the fp64 oracle on the host cores (all threads, and one thread).
+
 --impl reference times the fp64 CPU oracle (the only reference this path
 has) on the host cores, same workload, metric and unit.
 """
