@@ -6,12 +6,18 @@ generators (``inputs``).  The library is loaded on first use and a missing
 build raises: there is no CPU path.
 """
 from ._binding import (SWA_ERR_CUDA, SWA_ERR_INVALID_ARG, SWA_ERR_UNSUPPORTED,  # noqa: F401
-                       SWA_ERR_WORKSPACE, SWA_OK, SwaDims, SwaError, dims_of, load_library,
-                       make_dims, swa_last_error, swa_plan, swa_read_device_errors,
-                       swa_greedy_accept, swa_release_workspace, swa_set_workspace,
-                       swa_verify_attn, swa_verify_attn_paged, SwaPaged, swa_append_verify_attn,
-                       swa_verify_attn_noalloc, swa_version, swa_workspace_bytes)
+                       SWA_ERR_WORKSPACE, SWA_OK, SwaDims, SwaError, SwaPaged, dims_of,
+                       load_library, make_dims, swa_append_verify_attn, swa_greedy_accept,
+                       swa_last_error, swa_plan, swa_read_device_errors, swa_release_workspace,
+                       swa_set_workspace, swa_verify_attn, swa_verify_attn_noalloc,
+                       swa_verify_attn_paged, swa_version, swa_workspace_bytes)
 
-__all__ = ["swa_verify_attn", "swa_workspace_bytes", "swa_set_workspace",
-           "swa_release_workspace", "swa_plan", "swa_last_error", "swa_read_device_errors",
-           "swa_version", "swa_verify_attn_noalloc", "swa_greedy_accept", "swa_verify_attn_paged", "SwaPaged", "swa_append_verify_attn", "SwaDims", "SwaError", "make_dims", "dims_of", "load_library"]
+__all__ = [
+    # the C entry points of include/swa.h, same names
+    "swa_verify_attn", "swa_verify_attn_noalloc", "swa_verify_attn_paged",
+    "swa_append_verify_attn", "swa_greedy_accept", "swa_workspace_bytes", "swa_set_workspace",
+    "swa_release_workspace", "swa_plan", "swa_last_error", "swa_read_device_errors",
+    "swa_version",
+    # structs and helpers
+    "SwaDims", "SwaPaged", "SwaError", "make_dims", "dims_of", "load_library",
+]
