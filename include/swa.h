@@ -96,8 +96,13 @@ typedef struct {
  * give each its own device.
  *
  * Errors: SWA_ERR_INVALID_ARG / SWA_ERR_UNSUPPORTED are returned before any
- * CUDA call and leave the outputs untouched.  SWA_ERR_CUDA reports a failed
- * launch or allocation.  swa_last_error() gives the message. */
+ * CUDA call and leave the outputs untouched.  SWA_ERR_INVALID_ARG: a NULL or
+ * misaligned pointer, a non-finite scale, or dims outside the ranges above
+ * (also num_kv_heads > 65535).  SWA_ERR_UNSUPPORTED: head_dim not in {64,
+ * 128, 256}; more than 4096 packed rows q_len * (Hq / Hkv) per KV head; or
+ * num_kv_heads * ceil(q_len * (Hq / Hkv) / 32) > 65535.  SWA_ERR_CUDA
+ * reports a failed launch or allocation.  swa_last_error() gives the
+ * message. */
 swa_status swa_verify_attn(const void *q, const void *k_cache, const void *v_cache,
                            const int32_t *seq_lens, const int32_t *q_pos, int32_t window,
                            float scale, void *out, float *lse, const swa_dims *dims,
