@@ -9,7 +9,8 @@ checks a seeded subset of sequences of each launch.
   new cache rows bit for bit, and their outputs;
 - the plain verify call on the bandwidth-stress batch at draft lengths 1 and
   8 for every window: all 512 sequences, not a sample (the oracle needs a
-  few seconds per case: each sequence reads at most W + 7 keys).
+  few seconds per case: each sequence reads at most W + 7 keys); at draft
+  length 64 a seeded subset of 64 sequences.
 """
 import numpy as np
 import pytest
@@ -122,5 +123,16 @@ def test_stress_every_sequence(window, q_len):
     out, lse = run_gpu(case)
     ref_o, ref_l = oracle_reference(case)
     compare(out, lse, ref_o, ref_l, f"stress_w{window}_q{q_len}, all sequences")
+    del case, out, lse
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("window", [188, 512, 1024])
+def test_stress_q64_sixty_four_sequences(window):
+    case = inputs.stress(window, 64)
+    out, lse = run_gpu(case)
+    seqs = _sample(case, 62, 54 + window)
+    ref_o, ref_l = oracle_reference(case, seqs)
+    compare(out[seqs], lse[seqs], ref_o, ref_l, f"stress_w{window}_q64, {len(seqs)} sequences")
     del case, out, lse
     torch.cuda.empty_cache()
