@@ -30,9 +30,12 @@ struct AcceptParams {
 };
 
 // Total order on float bits for an unsigned maximum (-inf lowest of the
-// values that can win; NaN never reaches here).
+// values that can win; NaN never reaches here).  -0.0 and +0.0 compare equal
+// as floats (the per-thread scan treats them as one value), so both map to
+// the key of +0.0: otherwise a later +0.0 column would beat an earlier -0.0
+// column across threads or CTAs and break "the first of equal maxima".
 __device__ __forceinline__ uint32_t accept_key(float x) {
-    const uint32_t u = __float_as_uint(x);
+    const uint32_t u = x == 0.f ? 0u : __float_as_uint(x);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 

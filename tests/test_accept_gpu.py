@@ -108,3 +108,68 @@ def test_accept_scratch_grows_and_graph_replays():
         torch.cuda.synchronize()
         assert np.array_equal(am.cpu().numpy(), ref_am)
         assert np.array_equal(acc.cpu().numpy(), ref_acc)
+
+
+def _signed_zero_logits(B, q_len, V, zeros, seed):
+    """bf16 logits of negative values in [-4, -1] with the row maximum held
+    as signed zeros at the given (column, sign) places of every row."""
+    g = torch.Generator().manual_seed(seed)
+    x = -1.0 - 3.0 * torch.rand((B, q_len, V), generator=g)
+    for col, sign in zeros:
+        x[:, :, col] = -0.0 if sign < 0 else 0.0
+    return x.to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("B,q_len,V,zeros,keep", [
+    # -0.0 first, +0.0 later, in different threads of one CTA (8 logits per
+    # 16-byte load: columns 0 and 8 belong to neighbouring threads)
+    (1, 2, 4000, [(0, -1), (8, +1)], False),
+    # the same across warps of one CTA
+    (2, 3, 4000, [(3, -1), (1029, +1), (2047, -1)], False),
+    # across CTAs of a 262,144-column row (chunks of 4096 logits)
+    (1, 8, 262144, [(5, -1), (200000, +1)], False),
+    (1, 8, 262144, [(70000, -1), (70008, +1), (262143, +1)], False),
+    # +0.0 first, -0.0 later: still the first column
+    (1, 4, 262144, [(9, +1), (100000, -1)], False),
+    # through a keep set
+    (3, 5, 262144, [(4100, -1), (4108, +1), (150000, +1)], True),
+])
+def test_accept_signed_zero_ties(B, q_len, V, zeros, keep):
+    """-0.0 and +0.0 are equal maxima: the first column wins, wherever the
+    two sit (threads, warps, CTAs), bit-exactly as the oracle says."""
+    logits = _signed_zero_logits(B, q_len, V, zeros, seed=V + len(zeros))
+    assert torch.signbit(logits[0, 0, zeros[0][0]]).item() == (zeros[0][1] < 0)
+    g = torch.Generator().manual_seed(7)
+    keep_ids = torch.randperm(2 * V, generator=g)[:V].to(torch.int32) if keep else None
+    ref_am, _ = oracle.greedy_accept(logits.double().numpy(), np.zeros((B, q_len - 1)),
+                                     None if keep_ids is None else keep_ids.numpy())
+    first = zeros[0][0]
+    want = keep_ids[first].item() if keep else first
+    assert (ref_am == want).all()
+    draft = torch.from_numpy(ref_am[:, :-1].copy()).to(torch.int32)
+    _, ref_acc = oracle.greedy_accept(logits.double().numpy(), draft.numpy(),
+                                      None if keep_ids is None else keep_ids.numpy())
+    for _ in range(2):
+        am, acc = _run(logits, keep_ids, draft)
+        assert np.array_equal(am, ref_am)
+        assert np.array_equal(acc, ref_acc)
+
+
+def test_accept_random_signed_zero_maxima():
+    """Rows whose maximum is zero at several random columns of random sign."""
+    B, q_len, V = 16, 8, 50000
+    g = torch.Generator().manual_seed(21)
+    x = -1.0 - torch.rand((B, q_len, V), generator=g)
+    cols = torch.randint(0, V, (B, q_len, 6), generator=g)
+    signs = torch.randint(0, 2, (B, q_len, 6), generator=g)
+    for b in range(B):
+        for i in range(q_len):
+            for c, s in zip(cols[b, i].tolist(), signs[b, i].tolist()):
+                x[b, i, c] = -0.0 if s else 0.0
+    logits = x.to(torch.bfloat16)
+    ref_am, _ = oracle.greedy_accept(logits.double().numpy(), np.zeros((B, q_len - 1)), None)
+    assert np.array_equal(ref_am, cols.min(dim=2).values.numpy())
+    draft = torch.from_numpy(ref_am[:, :-1].copy()).to(torch.int32)
+    am, acc = _run(logits, None, draft)
+    assert np.array_equal(am, ref_am)
+    assert (acc == q_len - 1).all()
