@@ -213,6 +213,32 @@ swa_status swa_read_device_errors(uint32_t *flags);
 /* Library version, e.g. "swa 0.1.0 sm_103a". */
 const char *swa_version(void);
 
+/* Test and sweep controls.  Not for serving: every call uses the defaults
+ * unless a test or a benchmark sweep changes them; a change applies to all
+ * later calls in the process (every thread and device).  The library reads
+ * no environment variable. */
+typedef struct {
+    int32_t force_kernel;      /* 0 (default): the plan's kernel; 1 CUDA-core, 2 key-major
+                                  tensor-core, 3 rows-major tensor-core (a shape the forced
+                                  kernel does not take runs the plan's kernel) */
+    int32_t pdl;               /* 1 (default): launches with programmatic dependent launch;
+                                  0: plain stream-ordered launches */
+    int64_t wait_limit_cycles; /* 0 (default): every bounded wait inside the kernels gives up
+                                  after 2e9 SM cycles (about 1 s); n > 0: after n cycles */
+    int32_t withhold_fill;     /* -1 (default); n >= 0: the first CTA's copy producer posts
+                                  its n-th K/V fill but never issues the copies, so every wait
+                                  on that fill runs out and the call reports bit 0 through
+                                  swa_read_device_errors (the test of the bounded waits) */
+    int32_t reserved;          /* must be 0 */
+} swa_debug_options;
+
+/* Set the controls above (NULL restores the defaults).  Returns
+ * SWA_ERR_INVALID_ARG for a field outside its range. */
+swa_status swa_set_debug_options(const swa_debug_options *opt);
+
+/* The controls in effect. */
+swa_status swa_get_debug_options(swa_debug_options *opt);
+
 /* Greedy verification of a draft block: the argmax of every verify row's
  * logits (FUSED_SPARSE_ARGMAX, with the keep set of a pruned LM head) and
  * the number of drafted tokens accepted (SPECULATIVE_CONFIG's drafts), in

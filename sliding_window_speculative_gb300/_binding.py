@@ -36,6 +36,17 @@ class SwaPlanInfo(ctypes.Structure):
                 ("merge", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64)]
 
 
+class SwaDebugOptions(ctypes.Structure):
+    """swa_debug_options of include/swa.h (test and sweep controls)."""
+    _fields_ = [("force_kernel", ctypes.c_int32), ("pdl", ctypes.c_int32),
+                ("wait_limit_cycles", ctypes.c_int64), ("withhold_fill", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+# force_kernel values of swa_debug_options
+KERNEL_IDS = {"plan": 0, "simt": 1, "tc": 2, "rows": 3}
+
+
 class SwaError(RuntimeError):
     def __init__(self, status, message):
         super().__init__(f"{_STATUS.get(status, status)}: {message}")
@@ -83,6 +94,10 @@ def load_library(path=LIB_PATH):
     lib.swa_append_verify_attn.restype = ctypes.c_int
     lib.swa_greedy_accept.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp]
     lib.swa_greedy_accept.restype = ctypes.c_int
+    lib.swa_set_debug_options.argtypes = [ctypes.POINTER(SwaDebugOptions)]
+    lib.swa_set_debug_options.restype = ctypes.c_int
+    lib.swa_get_debug_options.argtypes = [ctypes.POINTER(SwaDebugOptions)]
+    lib.swa_get_debug_options.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -345,3 +360,19 @@ def swa_read_device_errors():
 
 def swa_version():
     return load_library().swa_version().decode()
+
+
+def swa_set_debug_options(force_kernel=0, pdl=1, wait_limit_cycles=0, withhold_fill=-1):
+    """Test and sweep controls of the C entry point swa_set_debug_options
+    (not for serving).  force_kernel: 0 or "plan", 1 or "simt", 2 or "tc",
+    3 or "rows"; pdl 1/0; wait_limit_cycles 0 (default ~2e9) or the bounded
+    waits' limit; withhold_fill -1 or the fill the first CTA never copies."""
+    fk = KERNEL_IDS[force_kernel] if isinstance(force_kernel, str) else int(force_kernel)
+    opt = SwaDebugOptions(fk, int(pdl), int(wait_limit_cycles), int(withhold_fill), 0)
+    _check(load_library().swa_set_debug_options(ctypes.byref(opt)))
+
+
+def swa_get_debug_options():
+    opt = SwaDebugOptions()
+    _check(load_library().swa_get_debug_options(ctypes.byref(opt)))
+    return {f: getattr(opt, f) for f, _ in SwaDebugOptions._fields_}

@@ -3,12 +3,11 @@
 // Every entry point is declared (with its contract) in include/swa.h.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
-
-#include <cstdlib>
 
 #include "../../include/swa.h"
 #include "swa_simt.cuh"
@@ -88,15 +87,15 @@ struct Plan {
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
-// Kernel override for sweeps and tests: SWA_FORCE_KERNEL=simt or =tc.
-int forced_kernel() {
-    const char *v = getenv("SWA_FORCE_KERNEL");
-    if (v == nullptr) return 0;
-    if (strcmp(v, "simt") == 0) return 1;
-    if (strcmp(v, "tc") == 0) return 2;
-    if (strcmp(v, "rows") == 0) return 3;
-    return 0;
-}
+// Test and sweep controls (swa_set_debug_options); relaxed atomics, read on
+// every call.
+std::atomic<int> g_opt_force{0};
+std::atomic<int> g_opt_pdl{1};
+std::atomic<long long> g_opt_wait_limit{0};
+std::atomic<int> g_opt_withhold{-1};
+
+// Kernel override of a test or sweep: 0 none, 1 CUDA-core, 2 key-major, 3 rows-major.
+int forced_kernel() { return g_opt_force.load(std::memory_order_relaxed); }
 
 // Split heuristic.  Host-only: seq_lens live on the device, so the
 // worst-case span W + q_len - 1 (bounded by the cache length) is used; a
@@ -405,24 +404,29 @@ swa_status launch_plan(const Plan &pl, const swa_dims *dims, const swa::AttnPara
     return SWA_OK;
 }
 
+// Per-device caches, filled on first use by whichever host thread gets
+// there (a race between threads only resolves the same value twice).
+std::atomic<uint32_t *> g_fault_ptr[kMaxDevices];
+std::atomic<int> g_sms[kMaxDevices];
+
 uint32_t *fault_word_ptr(int dev) {
-    static uint32_t *cache[kMaxDevices] = {};
-    if (cache[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_fault_word) != cudaSuccess) return nullptr;
-        cache[dev] = static_cast<uint32_t *>(p);
+    uint32_t *p = g_fault_ptr[dev].load(std::memory_order_acquire);
+    if (p == nullptr) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_fault_word) != cudaSuccess) return nullptr;
+        p = static_cast<uint32_t *>(a);
+        g_fault_ptr[dev].store(p, std::memory_order_release);
     }
-    return cache[dev];
+    return p;
 }
 
 int device_sms(int dev) {
-    static int cache[kMaxDevices] = {};
-    if (cache[dev] == 0) {
-        int n = 0;
+    int n = g_sms[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
         if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 148;
-        cache[dev] = n;
+        g_sms[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 // Host checks of a paged cache description against dims.
@@ -446,14 +450,46 @@ swa_status check_paged(const swa_paged *paged, const swa_dims *dims) {
     return SWA_OK;
 }
 
+}  // namespace
+
+// ------------------------------------------------- allocation-free scratch
+//
+// Split partials of swa_verify_attn_noalloc live in this fixed array instead
+// of a cudaMalloc'd workspace.  In host code `g_noalloc_scratch` only names
+// the symbol; its device address comes from cudaGetSymbolAddress, resolved
+// once per device with that device current.
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SWA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mutex;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on device `dev` (which must be the
+// current device), resolved once per device.
+swa_status noalloc_scratch(int dev, void **ptr) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return SWA_OK;
+}
+
 // The windowed verify attention of swa_verify_attn, on a contiguous cache
 // (paged == NULL) or a paged one; with k_new / v_new non-NULL the kernels
-// first write the new rows into the cache (swa_append_verify_attn).
+// first write the new rows into the cache (swa_append_verify_attn).  With
+// `noalloc` the split partials go to the fixed scratch array above
+// (swa_verify_attn_noalloc) and nothing is ever allocated.
 swa_status verify_impl(const void *q, const void *k_cache, const void *v_cache,
                        const int32_t *seq_lens, const int32_t *q_pos, int32_t window, float scale,
                        void *out, float *lse, const swa_dims *dims, swa_stream_t stream,
                        const swa_paged *paged, const void *k_new = nullptr,
-                       const void *v_new = nullptr) {
+                       const void *v_new = nullptr, bool noalloc = false) {
     swa_status st = validate_dims(dims, window);
     if (st != SWA_OK) return st;
     if (!q || !k_cache || !v_cache || !seq_lens || !q_pos || !out)
@@ -502,6 +538,9 @@ swa_status verify_impl(const void *q, const void *k_cache, const void *v_cache,
     P.fault = fault;
     P.k_new = static_cast<const __nv_bfloat16 *>(k_new);
     P.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    const long long wl = g_opt_wait_limit.load(std::memory_order_relaxed);
+    P.wait_limit = wl > 0 ? wl : swa::kWaitLimitCycles;
+    P.withhold_fill = g_opt_withhold.load(std::memory_order_relaxed);
     long long cache_rows = (long long)P.B * P.Hkv * P.L;
     if (paged != nullptr) {
         P.block_table = paged->block_table;
@@ -513,7 +552,17 @@ swa_status verify_impl(const void *q, const void *k_cache, const void *v_cache,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (pl.splits > 1) {
         void *ws = nullptr;
-        st = ensure_workspace(dev, (size_t)pl.workspace, s, &ws);
+        if (noalloc) {
+            if (pl.workspace > (long long)SWA_NOALLOC_SCRATCH_BYTES)
+                return fail(SWA_ERR_WORKSPACE,
+                            "this call's %d-way split needs %lld bytes of scratch, above the fixed "
+                            "%zu-byte maximum of swa_verify_attn_noalloc; pass fewer splits "
+                            "(num_splits = 1 needs none)",
+                            pl.splits, pl.workspace, (size_t)SWA_NOALLOC_SCRATCH_BYTES);
+            st = noalloc_scratch(dev, &ws);
+        } else {
+            st = ensure_workspace(dev, (size_t)pl.workspace, s, &ws);
+        }
         if (st != SWA_OK) return st;
         P.part_acc = static_cast<float *>(ws);
         P.part_ml = P.part_acc + (size_t)P.B * P.Hkv * P.splits * P.R * dims->head_dim;
@@ -650,7 +699,38 @@ swa_status swa_read_device_errors(uint32_t *flags) {
 
 const char *swa_version(void) { return "swa 0.1.0 sm_103a"; }
 
+swa_status swa_set_debug_options(const swa_debug_options *opt) {
+    swa_debug_options d{0, 1, 0, -1, 0};
+    if (opt != nullptr) d = *opt;
+    if (d.force_kernel < 0 || d.force_kernel > 3)
+        return fail(SWA_ERR_INVALID_ARG, "force_kernel %d outside [0, 3]", d.force_kernel);
+    if (d.pdl != 0 && d.pdl != 1) return fail(SWA_ERR_INVALID_ARG, "pdl %d is not 0 or 1", d.pdl);
+    if (d.wait_limit_cycles < 0)
+        return fail(SWA_ERR_INVALID_ARG, "wait_limit_cycles %lld < 0",
+                    (long long)d.wait_limit_cycles);
+    if (d.withhold_fill < -1)
+        return fail(SWA_ERR_INVALID_ARG, "withhold_fill %d < -1", d.withhold_fill);
+    if (d.reserved != 0) return fail(SWA_ERR_INVALID_ARG, "reserved must be 0");
+    g_opt_force.store(d.force_kernel, std::memory_order_relaxed);
+    g_opt_pdl.store(d.pdl, std::memory_order_relaxed);
+    g_opt_wait_limit.store(d.wait_limit_cycles, std::memory_order_relaxed);
+    g_opt_withhold.store(d.withhold_fill, std::memory_order_relaxed);
+    return SWA_OK;
+}
+
+swa_status swa_get_debug_options(swa_debug_options *opt) {
+    if (opt == nullptr) return fail(SWA_ERR_INVALID_ARG, "opt is NULL");
+    opt->force_kernel = g_opt_force.load(std::memory_order_relaxed);
+    opt->pdl = g_opt_pdl.load(std::memory_order_relaxed);
+    opt->wait_limit_cycles = g_opt_wait_limit.load(std::memory_order_relaxed);
+    opt->withhold_fill = g_opt_withhold.load(std::memory_order_relaxed);
+    opt->reserved = 0;
+    return SWA_OK;
+}
+
 }  // extern "C"
+
+bool swa::pdl_enabled() { return g_opt_pdl.load(std::memory_order_relaxed) != 0; }
 
 // ------------------------------------------------ greedy verification
 
@@ -759,97 +839,12 @@ swa_status swa_greedy_accept(const void *logits, const int32_t *keep_ids, const 
 }  // extern "C"
 
 // ------------------------------------------------- allocation-free variant
-//
-// Split partials of swa_verify_attn_noalloc live in this fixed array instead
-// of a cudaMalloc'd workspace.  In host code `g_noalloc_scratch` only names
-// the symbol; its device address comes from cudaGetSymbolAddress.
-
-static __device__ __align__(256) unsigned char g_noalloc_scratch[SWA_NOALLOC_SCRATCH_BYTES];
-
-namespace {
-
-std::mutex g_noalloc_mutex;
-void *g_noalloc_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on device `dev` (which must be the
-// current device), resolved once per device.
-swa_status noalloc_scratch(int dev, void **ptr) {
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (g_noalloc_ptr[dev] == nullptr) {
-        void *p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(noalloc scratch)");
-        g_noalloc_ptr[dev] = p;
-    }
-    *ptr = g_noalloc_ptr[dev];
-    return SWA_OK;
-}
-
-}  // namespace
 
 extern "C" swa_status swa_verify_attn_noalloc(const void *q, const void *k_cache,
                                               const void *v_cache, const int32_t *seq_lens,
                                               const int32_t *q_pos, int32_t window, float scale,
                                               void *out, float *lse, const swa_dims *dims,
                                               swa_stream_t stream) {
-    swa_status st = validate_dims(dims, window);
-    if (st != SWA_OK) return st;
-    if (!q || !k_cache || !v_cache || !seq_lens || !q_pos || !out)
-        return fail(SWA_ERR_INVALID_ARG, "a required pointer is NULL");
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-        return fail(SWA_ERR_INVALID_ARG, "q, k_cache, v_cache and out must be 16-byte aligned");
-    if ((reinterpret_cast<uintptr_t>(seq_lens) & 3u) || (reinterpret_cast<uintptr_t>(q_pos) & 3u) ||
-        (reinterpret_cast<uintptr_t>(lse) & 3u))
-        return fail(SWA_ERR_INVALID_ARG, "seq_lens, q_pos and lse must be 4-byte aligned");
-    if (!(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
-        return fail(SWA_ERR_INVALID_ARG, "scale must be finite");
-
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev >= kMaxDevices) return fail(SWA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
-    uint32_t *fault = fault_word_ptr(dev);
-    if (fault == nullptr) return fail(SWA_ERR_CUDA, "cannot resolve the device fault word");
-    const Plan pl = make_plan(dims, window, device_sms(dev));
-    if (pl.workspace > (long long)SWA_NOALLOC_SCRATCH_BYTES)
-        return fail(SWA_ERR_WORKSPACE,
-                    "this call's %d-way split needs %lld bytes of scratch, above the fixed "
-                    "%zu-byte maximum of swa_verify_attn_noalloc; pass fewer splits "
-                    "(num_splits = 1 needs none)",
-                    pl.splits, pl.workspace, (size_t)SWA_NOALLOC_SCRATCH_BYTES);
-    void *scratch = nullptr;
-    st = noalloc_scratch(dev, &scratch);
-    if (st != SWA_OK) return st;
-
-    swa::AttnParams P{};
-    P.q = static_cast<const __nv_bfloat16 *>(q);
-    P.k = static_cast<const __nv_bfloat16 *>(k_cache);
-    P.v = static_cast<const __nv_bfloat16 *>(v_cache);
-    P.seq_lens = seq_lens;
-    P.q_pos = q_pos;
-    P.out = static_cast<__nv_bfloat16 *>(out);
-    P.lse = lse;
-    P.B = dims->batch;
-    P.q_len = dims->q_len;
-    P.Hq = dims->num_q_heads;
-    P.Hkv = dims->num_kv_heads;
-    P.G = dims->num_q_heads / dims->num_kv_heads;
-    P.L = dims->max_len;
-    P.window = window;
-    P.R = P.q_len * P.G;
-    P.splits = pl.splits;
-    P.chunk = pl.chunk;
-    P.row_tiles = pl.row_tiles;
-    P.rows_per_tile = pl.rows_per_tile;
-    P.qk_scale = scale * swa::kLog2e;
-    P.fault = fault;
-    if (pl.splits > 1) {
-        P.part_acc = static_cast<float *>(scratch);
-        P.part_ml = P.part_acc + (size_t)P.B * P.Hkv * P.splits * P.R * dims->head_dim;
-    }
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    st = launch_plan(pl, dims, P, q, k_cache, v_cache, s);
-    if (st != SWA_OK) return st;
-    t_last_error[0] = '\0';
-    return SWA_OK;
+    return verify_impl(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out, lse, dims, stream,
+                       nullptr, nullptr, nullptr, /*noalloc=*/true);
 }

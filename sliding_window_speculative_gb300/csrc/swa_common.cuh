@@ -12,7 +12,9 @@ namespace swa {
 // reads it through swa_read_device_errors).
 constexpr uint32_t kFaultCopyTimeout = 1u;
 
-// ~1 s at the GB300 SM clock; a healthy copy completes in microseconds.
+// Default limit of every bounded wait: ~1 s at the GB300 SM clock (a healthy
+// copy completes in microseconds).  Kernels take the limit as a parameter so
+// that a test can shorten it.
 constexpr long long kWaitLimitCycles = 2000000000LL;
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -73,15 +75,15 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete, giving up after
-// kWaitLimitCycles.  Returns false (and ORs `bit` into *fault_word) on
-// giving up.
+// Wait for phase `parity` of `bar` to complete, giving up after `limit` SM
+// cycles.  Returns false (and ORs `bit` into *fault_word) on giving up.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
-                                                  uint32_t *fault_word, uint32_t bit) {
+                                                  uint32_t *fault_word, uint32_t bit,
+                                                  long long limit) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
             atomicOr(fault_word, bit);
             return false;
         }

@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
                 }
                 if (progressed) {
                     idle_since = clock64();
-                } else if (clock64() - idle_since > kWaitLimitCycles) {
+                } else if (clock64() - idle_since > P.wait_limit) {
                     atomicOr(P.fault, kFaultCopyTimeout);
                     ok = false;
                     break;
@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
             // all issued MMAs complete before TMEM is released
             if (leader) {
                 mma_commit(&bars[C::B_DRAIN]);
-                mbar_wait_bounded(&bars[C::B_DRAIN], 0, P.fault, kFaultCopyTimeout);
+                mbar_wait_bounded(&bars[C::B_DRAIN], 0, P.fault, kFaultCopyTimeout, P.wait_limit);
             }
             __syncwarp();
         }
@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
                 for (int t = 0; t < it.n_tiles; ++t, ++g) {
                     const uint32_t sb = g & 1;
                     ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[C::B_SFULL + sb], (g >> 1) & 1,
-                                                                   P.fault, kFaultCopyTimeout));
+                                                                   P.fault, kFaultCopyTimeout, P.wait_limit));
                     if (!ok) break;
                     fence_after_sync();
                     // this thread's 64 scores (keys kh .. kh + 63 of the tile), masked
@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
                         const uint32_t gp = g - 1;
                         ok = __all_sync(0xffffffffu,
                                         mbar_wait_bounded(&bars[C::B_PVDONE + (gp & 1)], (gp >> 1) & 1,
-                                                          P.fault, kFaultCopyTimeout));
+                                                          P.fault, kFaultCopyTimeout, P.wait_limit));
                         if (!ok) break;
                         fence_after_sync();
                         const float al = raise ? fast_exp2(mref - mt) : 1.f;
@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
                 const uint32_t gl = g - 1;  // the item's last tile
                 ok = __all_sync(0xffffffffu, mbar_wait_bounded(&bars[C::B_PVDONE + (gl & 1)],
                                                                (gl >> 1) & 1, P.fault,
-                                                               kFaultCopyTimeout));
+                                                               kFaultCopyTimeout, P.wait_limit));
                 if (!ok) break;
                 fence_after_sync();
                 const uint32_t oc = tl + C::O_COL + ob * D + half * DH;

@@ -48,6 +48,13 @@ struct AttnParams {
     int B, q_len, Hq, Hkv, G, L, window, R;
     int splits, chunk, row_tiles, rows_per_tile;
     float qk_scale;   // scale * log2(e)
+    // bounded waits give up after this many SM cycles (kWaitLimitCycles
+    // unless a test shortened it)
+    long long wait_limit;
+    // tests of the bounded waits only (-1 otherwise): the producer of the
+    // first CTA posts this fill (K/V tile, or stage) but never issues its
+    // copies, so every wait on it runs out
+    int withhold_fill;
 };
 
 // Chunk `split` [lo, hi) of sequence b's window span (clamped to the
@@ -218,6 +225,7 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
         const uint32_t bytes = (uint32_t)n * D * 2;
         uint8_t *dst = ring + s * C::STAGE_BYTES;
         mbar_arrive_expect_tx(&full[s], 2 * bytes);
+        if (P.withhold_fill == t && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) return;
         // one copy per run of rows contiguous in the cache (a page's rows, or
         // the whole tile of a contiguous cache); a new row of a fused append
         // is one copy from k_new / v_new
@@ -293,7 +301,13 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
             issue(t + C::STAGES - 1);
         }
         const int s = t % C::STAGES;
-        if (!mbar_wait_bounded(&full[s], (t / C::STAGES) & 1, P.fault, kFaultCopyTimeout)) {
+        if (!mbar_wait_bounded(&full[s], (t / C::STAGES) & 1, P.fault, kFaultCopyTimeout,
+                               P.wait_limit)) {
+            // the stages issued after this one land before the CTA leaves
+            if (tid == 0)
+                for (int t2 = t + 1; t2 < n_tiles && t2 < t + C::STAGES; ++t2)
+                    mbar_wait_bounded(&full[t2 % C::STAGES], (t2 / C::STAGES) & 1, P.fault,
+                                      kFaultCopyTimeout, P.wait_limit);
             ok = false;
             break;
         }

@@ -365,7 +365,7 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
         const uint32_t qb = k % QB, quse = k / QB;
         auto load_q = [&]() -> bool {
             if (!mbar_wait_bounded(&bars[C::B_QEMPTY + qb], (quse & 1) ^ 1, P.fault,
-                                   kFaultCopyTimeout))
+                                   kFaultCopyTimeout, P.wait_limit))
                 return false;
             mbar_arrive_expect_tx(&bars[C::B_QFULL + qb], C::SLABS * T.rows_per_tile * 128);
             for (int s = 0; s < C::SLABS; ++s)
@@ -404,7 +404,7 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
                             }
                         }
                         if (slot >= 0) break;
-                        if (clock64() - w0 > kWaitLimitCycles) {
+                        if (clock64() - w0 > P.wait_limit) {
                             atomicOr(P.fault, kFaultCopyTimeout);
                             break;
                         }
@@ -426,6 +426,12 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
                 if (lane == 0)
                     mbar_arrive_expect_tx(bar, (uint32_t)(a_m + natoms - a_n) * C::ATOM_BYTES);
                 if (coop) __syncwarp();  // the expected bytes are posted before any copy
+                // (tests of the bounded waits: this fill's copies are never issued)
+                const bool withhold = P.withhold_fill == (int)f && blockIdx.x == 0;
+                if (withhold) {
+                    ++f;
+                    continue;
+                }
                 if (a_m > 0)
                     tile_copies<C::ATOM_BYTES>(P, M, kv, it.b, it.h, p,
                                                a_m < natoms ? 8 * a_m : n_valid, dst, bar,
@@ -457,16 +463,16 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
     for (int s2 = 0; s2 < NT; ++s2) {
         if (uses[s2] > 0)
             mbar_wait_bounded(&bars[C::B_FULL + s2], (uses[s2] - 1) & 1, P.fault,
-                              kFaultCopyTimeout);
+                              kFaultCopyTimeout, P.wait_limit);
         if ((mix_used >> s2) & 1u)
             mbar_wait_bounded(&bars[C::B_MIX + s2], ((mix_n >> s2) & 1u) ^ 1u, P.fault,
-                              kFaultCopyTimeout);
+                              kFaultCopyTimeout, P.wait_limit);
     }
     const uint32_t nq = k < (uint32_t)QB ? k : (uint32_t)QB;
     for (uint32_t q = 0; q < nq; ++q) {
         const uint32_t kq = k - 1 - q;
         mbar_wait_bounded(&bars[C::B_QFULL + kq % QB], (kq / QB) & 1, P.fault,
-                          kFaultCopyTimeout);
+                          kFaultCopyTimeout, P.wait_limit);
     }
 }
 
@@ -532,7 +538,7 @@ __device__ __forceinline__ void append_worker(const TcParams &T, const TcItem *m
                     e = ftab[fill % kFillTab];
                     const long long w0 = clock64();
                     while ((e >> 8) != (fill & 0xffffffu)) {
-                        if (clock64() - w0 > kWaitLimitCycles) {
+                        if (clock64() - w0 > P.wait_limit) {
                             atomicOr(P.fault, kFaultCopyTimeout);
                             found = false;
                             break;
@@ -545,7 +551,7 @@ __device__ __forceinline__ void append_worker(const TcParams &T, const TcItem *m
                 const int slot = (int)(__shfl_sync(0xffffffffu, e, 0) & 15u);
                 const bool landed = mbar_wait_bounded(&bars[C::B_MIX + slot],
                                                       (mixpar >> slot) & 1u, P.fault,
-                                                      kFaultCopyTimeout);
+                                                      kFaultCopyTimeout, P.wait_limit);
                 if (!__all_sync(0xffffffffu, landed)) return;
                 mixpar ^= 1u << slot;
                 uint8_t *atom = ring + slot * C::TILE_BYTES + a_m * C::ATOM_BYTES;
@@ -958,7 +964,7 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
                 if (progressed) {
                     idle_since = clock64();
                     idle = 0;
-                } else if (clock64() - idle_since < kWaitLimitCycles) {
+                } else if (clock64() - idle_since < P.wait_limit) {
                     ++idle;
                 } else {
                     atomicOr(P.fault, kFaultCopyTimeout);
@@ -970,7 +976,7 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
             // all issued MMAs complete before TMEM is released
             if (leader) {
                 mma_commit(&bars[C::B_DRAIN]);
-                mbar_wait_bounded(&bars[C::B_DRAIN], 0, P.fault, kFaultCopyTimeout);
+                mbar_wait_bounded(&bars[C::B_DRAIN], 0, P.fault, kFaultCopyTimeout, P.wait_limit);
             }
             __syncwarp();
         }
@@ -1034,7 +1040,7 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
                 // (a failed wait is voted on together with the raise below: one
                 // group barrier per tile when nothing is raised)
                 const bool got = mbar_wait_bounded(&bars[C::B_SFULL + sb], suse & 1, P.fault,
-                                                   kFaultCopyTimeout);
+                                                   kFaultCopyTimeout, P.wait_limit);
                 fence_after_sync();
                 const int j0 = it.t0 + kTcTileKeys * t;
                 const int n_valid = min(kTcTileKeys, it.cr.c_hi - j0);
@@ -1126,7 +1132,7 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
                         const uint32_t gp = g - 1;
                         ok = !group_any(wg, !mbar_wait_bounded(&bars[C::B_PVDONE + gp % PB],
                                                                (gp / PB) & 1, P.fault,
-                                                               kFaultCopyTimeout));
+                                                               kFaultCopyTimeout, P.wait_limit));
                         if (!ok) break;
                         fence_after_sync();  // (the vote also published alpha_sm)
 #pragma unroll 1
@@ -1153,7 +1159,7 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
                     const uint32_t gp = g - PB;
                     ok = !group_any(wg, !mbar_wait_bounded(&bars[C::B_PVDONE + pb],
                                                            (gp / PB) & 1, P.fault,
-                                                           kFaultCopyTimeout));
+                                                           kFaultCopyTimeout, P.wait_limit));
                     if (!ok) break;
                 }
                 // the previous item's epilogue staged its output in the P buffers
@@ -1218,7 +1224,7 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
             }
             const uint32_t gl = g - 1;  // the item's last tile
             ok = !group_any(wg, !mbar_wait_bounded(&bars[C::B_PVDONE + gl % PB], (gl / PB) & 1,
-                                                   P.fault, kFaultCopyTimeout));
+                                                   P.fault, kFaultCopyTimeout, P.wait_limit));
             if (!ok) break;
             fence_after_sync();  // (the vote also published linv)
             // O^T through shared memory (the P buffers are idle now) into

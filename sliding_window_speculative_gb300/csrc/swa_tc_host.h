@@ -4,7 +4,6 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
-#include <stdlib.h>
 
 #include <utility>
 
@@ -56,14 +55,9 @@ struct TcLaunch {
 // Kernels are launched with programmatic stream serialization (programmatic
 // dependent launch): each may begin its prologue while the previous kernel
 // in the stream finishes, and waits (griddepcontrol.wait) before it reads
-// any caller memory.  SWA_PDL=0 in the environment turns it off.
-inline bool pdl_enabled() {
-    static const bool on = [] {
-        const char *v = getenv("SWA_PDL");
-        return !(v != nullptr && v[0] == '0');
-    }();
-    return on;
-}
+// any caller memory.  On unless a test or sweep turned it off through
+// swa_set_debug_options (defined with the C ABI).
+bool pdl_enabled();
 
 template <typename... Params, typename... Args>
 cudaError_t launch_kernel(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,

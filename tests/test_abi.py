@@ -9,6 +9,7 @@ import pytest
 
 import sliding_window_speculative_gb300 as swa
 from sliding_window_speculative_gb300 import build
+from tests.helpers import forced_kernel
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "swa.h")
@@ -129,7 +130,7 @@ def test_plan_invariants(lib, B, q_len, Hq, Hkv, D, L, W, sms):
         assert p["workspace_bytes"] == B * Hkv * p["num_splits"] * R * (D + 2) * 4
 
 
-def test_plan_kernel_choice(lib, monkeypatch):
+def test_plan_kernel_choice(lib):
     q8 = swa.make_dims(1, 8, 8, 2, 256, 4096)
     assert swa.swa_plan(q8, 188, 152)["kernel"] == 2            # 32 packed rows: tensor cores
     q1 = swa.make_dims(1, 1, 8, 2, 256, 4096)
@@ -144,20 +145,57 @@ def test_plan_kernel_choice(lib, monkeypatch):
     assert q64["kernel"] == 3 and q64["row_tiles"] == 2 and q64["rows_per_tile"] == 128
     q16 = swa.swa_plan(swa.make_dims(64, 16, 8, 2, 256, 4096), 188, 152)
     assert q16["kernel"] == 3 and q16["row_tiles"] == 1 and q16["rows_per_tile"] == 64
-    monkeypatch.setenv("SWA_FORCE_KERNEL", "simt")
-    assert swa.swa_plan(q8, 188, 152)["kernel"] == 1
-    monkeypatch.setenv("SWA_FORCE_KERNEL", "tc")
-    assert swa.swa_plan(q1, 188, 152)["kernel"] == 2
-    assert swa.swa_plan(d64, 16, 152)["kernel"] == 1
+    with forced_kernel("simt"):
+        assert swa.swa_plan(q8, 188, 152)["kernel"] == 1
+    with forced_kernel("tc"):
+        assert swa.swa_plan(q1, 188, 152)["kernel"] == 2
+        assert swa.swa_plan(d64, 16, 152)["kernel"] == 1
+    with forced_kernel("rows"):
+        assert swa.swa_plan(q1, 188, 152)["kernel"] == 3
+    assert swa.swa_plan(q8, 188, 152)["kernel"] == 2  # back to the plan's choice
 
 
-def test_plan_forced_splits(lib, monkeypatch):
-    monkeypatch.setenv("SWA_FORCE_KERNEL", "simt")
-    dims = swa.make_dims(1, 8, 8, 2, 256, 4096, 5)
-    p = swa.swa_plan(dims, 188, 152)
-    assert p["num_splits"] == 5 and p["chunk_keys"] == 39
-    dims = swa.make_dims(1, 8, 8, 2, 256, 4096, 500)
-    assert swa.swa_plan(dims, 188, 152)["num_splits"] <= 64
+def test_plan_forced_splits(lib):
+    with forced_kernel("simt"):
+        dims = swa.make_dims(1, 8, 8, 2, 256, 4096, 5)
+        p = swa.swa_plan(dims, 188, 152)
+        assert p["num_splits"] == 5 and p["chunk_keys"] == 39
+        dims = swa.make_dims(1, 8, 8, 2, 256, 4096, 500)
+        assert swa.swa_plan(dims, 188, 152)["num_splits"] <= 64
+
+
+def test_debug_options_round_trip_and_validation(lib):
+    """The test controls replace environment variables: the library reads
+    none.  Defaults, a round trip, range checks and the reset."""
+    assert swa.swa_get_debug_options() == {"force_kernel": 0, "pdl": 1, "wait_limit_cycles": 0,
+                                           "withhold_fill": -1, "reserved": 0}
+    swa.swa_set_debug_options(force_kernel="rows", pdl=0, wait_limit_cycles=100000,
+                              withhold_fill=3)
+    try:
+        assert swa.swa_get_debug_options() == {"force_kernel": 3, "pdl": 0,
+                                               "wait_limit_cycles": 100000, "withhold_fill": 3,
+                                               "reserved": 0}
+    finally:
+        swa.swa_set_debug_options()
+    assert swa.swa_get_debug_options()["force_kernel"] == 0
+    for bad in ({"force_kernel": 4}, {"force_kernel": -1}, {"pdl": 2},
+                {"wait_limit_cycles": -5}, {"withhold_fill": -2}):
+        with pytest.raises(swa.SwaError) as e:
+            swa.swa_set_debug_options(**bad)
+        assert e.value.status == swa.SWA_ERR_INVALID_ARG
+    opt = swa.SwaDebugOptions(0, 1, 0, -1, 7)
+    assert lib.swa_set_debug_options(ctypes.byref(opt)) == swa.SWA_ERR_INVALID_ARG
+    assert lib.swa_set_debug_options(None) == swa.SWA_OK
+    assert lib.swa_get_debug_options(None) == swa.SWA_ERR_INVALID_ARG
+
+
+def test_library_reads_no_environment():
+    """No source of the CUDA library calls getenv: test and sweep controls
+    go through swa_set_debug_options only."""
+    csrc = os.path.join(ROOT, "sliding_window_speculative_gb300", "csrc")
+    for name in os.listdir(csrc):
+        text = open(os.path.join(csrc, name)).read()
+        assert "getenv" not in text, name
 
 
 def test_plan_splits_long_spans_of_one_sequence(lib):

@@ -16,7 +16,7 @@ import torch
 
 import oracle
 from sliding_window_speculative_gb300 import inputs
-from tests.helpers import compare, oracle_reference
+from tests.helpers import compare, forced_kernel, oracle_reference
 from tests.test_paged_gpu import paginate
 
 pytestmark = pytest.mark.gpu
@@ -34,9 +34,9 @@ def _built():
 
 
 @pytest.fixture(params=["simt", "tc", "rows"])
-def kernel(request, monkeypatch):
-    monkeypatch.setenv("SWA_FORCE_KERNEL", request.param)
-    return request.param
+def kernel(request):
+    with forced_kernel(request.param):
+        yield request.param
 
 
 def take_block(case):

@@ -60,8 +60,9 @@ LAYOUT = r"""
 #include "swa.h"
 #define F(T, f) printf(#T "." #f " %zu %zu\n", offsetof(T, f), sizeof(((T *)0)->f))
 int main(void) {
-    printf("swa_dims %zu\nswa_paged %zu\nswa_plan_info %zu\n", sizeof(swa_dims),
-           sizeof(swa_paged), sizeof(swa_plan_info));
+    printf("swa_dims %zu\nswa_paged %zu\nswa_plan_info %zu\nswa_debug_options %zu\n",
+           sizeof(swa_dims), sizeof(swa_paged), sizeof(swa_plan_info),
+           sizeof(swa_debug_options));
     F(swa_dims, batch); F(swa_dims, q_len); F(swa_dims, num_q_heads);
     F(swa_dims, num_kv_heads); F(swa_dims, head_dim); F(swa_dims, max_len);
     F(swa_dims, num_splits);
@@ -70,6 +71,9 @@ int main(void) {
     F(swa_plan_info, kernel); F(swa_plan_info, num_splits); F(swa_plan_info, chunk_keys);
     F(swa_plan_info, row_tiles); F(swa_plan_info, rows_per_tile); F(swa_plan_info, grid_ctas);
     F(swa_plan_info, merge); F(swa_plan_info, workspace_bytes);
+    F(swa_debug_options, force_kernel); F(swa_debug_options, pdl);
+    F(swa_debug_options, wait_limit_cycles); F(swa_debug_options, withhold_fill);
+    F(swa_debug_options, reserved);
     return 0;
 }
 """
@@ -88,7 +92,8 @@ def test_binding_structs_match_the_c_layout(tmp_path):
                     str(exe)], check=True)
     out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout
     mirrors = {"swa_dims": _binding.SwaDims, "swa_paged": _binding.SwaPaged,
-               "swa_plan_info": _binding.SwaPlanInfo}
+               "swa_plan_info": _binding.SwaPlanInfo,
+               "swa_debug_options": _binding.SwaDebugOptions}
     seen = 0
     for line in out.splitlines():
         parts = line.split()
@@ -99,7 +104,7 @@ def test_binding_structs_match_the_c_layout(tmp_path):
             desc = getattr(mirrors[struct], field)
             assert (desc.offset, desc.size) == (int(parts[1]), int(parts[2])), line
         seen += 1
-    assert seen == 3 + 7 + 4 + 8
+    assert seen == 4 + 7 + 4 + 8 + 5
 
 
 def _prototypes():

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from sliding_window_speculative_gb300 import inputs
-from tests.helpers import compare, oracle_reference
+from tests.helpers import compare, forced_kernel, oracle_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -23,9 +23,9 @@ def _built():
 
 
 @pytest.fixture(params=["simt", "tc", "rows"])
-def kernel(request, monkeypatch):
-    monkeypatch.setenv("SWA_FORCE_KERNEL", request.param)
-    return request.param
+def kernel(request):
+    with forced_kernel(request.param):
+        yield request.param
 
 
 def paginate(case, page_size, spare=5, seed=0, poison=float("nan")):

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 from sliding_window_speculative_gb300 import inputs
-from tests.helpers import compare, oracle_reference, run_gpu
+from tests.helpers import compare, forced_kernel, oracle_reference, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -27,13 +27,13 @@ def _built():
 
 
 @pytest.fixture(params=["simt", "tc", "rows"])
-def kernel(request, monkeypatch):
+def kernel(request):
     """Runs the test once per kernel: the CUDA-core chunk kernel, the
     key-major tensor-core kernel and the rows-major tensor-core kernel
     (shapes the tensor-core kernels do not cover, head_dim 64, fall back to
     the CUDA-core kernel)."""
-    monkeypatch.setenv("SWA_FORCE_KERNEL", request.param)
-    return request.param
+    with forced_kernel(request.param):
+        yield request.param
 
 
 def _check(case, num_splits=0, seqs=None, what=None):

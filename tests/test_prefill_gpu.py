@@ -10,7 +10,7 @@ import pytest
 import torch
 
 from sliding_window_speculative_gb300 import inputs
-from tests.helpers import compare, oracle_reference, run_gpu
+from tests.helpers import compare, forced_kernel, oracle_reference, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -25,9 +25,9 @@ def _built():
 
 
 @pytest.fixture(params=["simt", "tc", "rows"])
-def kernel(request, monkeypatch):
-    monkeypatch.setenv("SWA_FORCE_KERNEL", request.param)
-    return request.param
+def kernel(request):
+    with forced_kernel(request.param):
+        yield request.param
 
 
 @pytest.mark.parametrize("D,q_len,window", [(64, 100, 37), (128, 256, 188), (256, 512, 188),
@@ -67,11 +67,7 @@ def test_prefill_with_fused_append():
     """A 256-token prefill chunk whose K/V rows are appended by the same call."""
     from tests.test_append_gpu import check_contiguous
     for kernel in ("simt", "tc", "rows"):
-        import os
-        os.environ["SWA_FORCE_KERNEL"] = kernel
-        try:
+        with forced_kernel(kernel):
             case = inputs.make_case("prefill", 2, 8, 2, 256, 256, 188, [256, 700], 1024, seed=3,
                                     device="cuda")
             check_contiguous(case, 0, f"prefill append {kernel}")
-        finally:
-            del os.environ["SWA_FORCE_KERNEL"]
