@@ -235,21 +235,38 @@ class Replicas:
                         out=self.out[r], lse=self.lse[r], num_splits=num_splits)
 
 
-def replica_count(case, bytes_per_call):
-    l2 = getattr(torch.cuda.get_device_properties(case.q.device), "L2_cache_size", 0) or (126 << 20)
+def replica_count(case, bytes_per_call, steps, l2=None):
+    """Input replicas that keep every timed call's reads out of L2.
+
+    Returns (n, l2, distinct).  distinct: the timed calls each read their
+    own replica (n >= steps) and L2 is flushed before the timed replay.
+    Otherwise the calls cycle through n replicas that together hold at least
+    twice the L2 size.  n = 1 when one call alone reads more than L2."""
+    if l2 is None:
+        l2 = (getattr(torch.cuda.get_device_properties(case.q.device), "L2_cache_size", 0) or
+              (126 << 20))
     if bytes_per_call >= l2:
-        return 1, l2
-    n = math.ceil(2 * l2 / bytes_per_call)
+        return 1, l2, False
     slab = case.k_cache.numel() * 2 * 2 + case.q.numel() * 2 * 2
-    n = max(2, min(n, 2048, int((16 << 30) // max(slab, 1))))
-    return n, l2
+    cap = max(2, int((16 << 30) // max(slab, 1)))   # replicas fit in 16 GiB
+    cycle = math.ceil(2 * l2 / bytes_per_call)
+    if steps < cycle and steps <= cap:
+        return max(2, steps), l2, True
+    return min(cycle, cap), l2, False
 
 
 def time_device(case, steps, warmup, num_splits=0, graph_len=1000, dist=None, append=None):
     """Device time of `steps` calls (graph replays), L2 defeated by replicas.
-    Returns dict with total seconds and per-call microseconds."""
+
+    With fewer timed calls than one cycle of replicas needs, every timed
+    call reads its own replica and a write of twice the L2 size runs between
+    the graph's warm-up replay and the timed replay, so no timed call finds
+    its inputs in L2.  Otherwise the graph cycles through replicas holding at
+    least twice the L2 size, so between two uses of one replica the other
+    calls read that much.  Returns dict with total seconds and per-call
+    microseconds."""
     kv, total = workload_bytes(case)
-    nrep, l2 = replica_count(case, total)
+    nrep, l2, distinct = replica_count(case, total, steps)
     rep = Replicas(case, nrep, append)
     stream = torch.cuda.Stream()
     torch.cuda.synchronize()
@@ -257,25 +274,32 @@ def time_device(case, steps, warmup, num_splits=0, graph_len=1000, dist=None, ap
         for i in range(max(warmup, 3)):
             rep.call(i, num_splits)
     stream.synchronize()
-    g_len = max(1, min(graph_len, steps))
-    graphs = {}
 
-    def capture(n):
+    def capture(idx):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for i in range(n):
+            for i in idx:
                 rep.call(i, num_splits)
         return g
 
-    full, rest = divmod(steps, g_len)
-    if full:
-        graphs["full"] = capture(g_len)
-    if rest:
-        graphs["rest"] = capture(rest)
-    # warm the graphs themselves
+    flush = None
+    if distinct:
+        timed = [capture(range(steps))]
+        flush = torch.empty(2 * l2, dtype=torch.uint8, device=case.q.device)
+        scheme = (f"each timed call reads its own replica ({steps} of {nrep}); {2 * l2 >> 20} MiB "
+                  f"written between the warm-up and the timed replay")
+    else:
+        g_len = nrep * max(1, min(graph_len, steps) // nrep) if nrep <= steps else steps
+        full, rest = divmod(steps, g_len)
+        timed = [capture(range(g_len))] * full + ([capture(range(rest))] if rest else [])
+        scheme = (f"calls cycle through {nrep} replicas ({nrep * total >> 20} MiB per cycle)"
+                  if nrep > 1 else "every call reads more than L2")
+    # warm the graphs themselves (first replays upload them), then flush L2
     with torch.cuda.stream(stream):
-        for g in graphs.values():
+        for g in dict.fromkeys(timed):
             g.replay()
+        if flush is not None:
+            flush.zero_()
     stream.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -285,19 +309,18 @@ def time_device(case, steps, warmup, num_splits=0, graph_len=1000, dist=None, ap
     t0 = time.time()
     with torch.cuda.stream(stream):
         start.record(stream)
-        for _ in range(full):
-            graphs["full"].replay()
-        if rest:
-            graphs["rest"].replay()
+        for g in timed:
+            g.replay()
         end.record(stream)
     torch.cuda.synchronize()
     t1 = time.time()
     if dist is not None:
         dist.barrier()
     ms = start.elapsed_time(end)
-    del graphs, rep
+    del timed, flush, rep
     return {"seconds": ms / 1e3, "us_per_call": ms * 1e3 / steps, "replicas": nrep,
-            "l2_bytes": l2, "wall": (t0, t1), "kv_bytes": kv, "bytes": total}
+            "l2_bytes": l2, "l2_scheme": scheme, "wall": (t0, t1), "kv_bytes": kv,
+            "bytes": total}
 
 
 def _packed(parts, device=None, pin=False, align=256):
@@ -486,40 +509,67 @@ def time_accept(B, q_len, V, steps=2000, warmup=5, seed=0, graph_len=1000):
             "logit_gbs": round(nbytes / (us * 1e-6) / 1e9, 1), "replicas": nrep}
 
 
-def oracle_sample(case, budget_s=10.0, max_calls=None, threads=None):
-    """Times the fp64 oracle on whole calls of the workload (sequences
-    sampled if one call is too long).  Returns per-call seconds scaled to the
-    full batch, the sample description and the threads used."""
+def oracle_window(case, seqs):
+    """Host copies of the windows of sequences `seqs` (the oracle's input)
+    and their KV bytes."""
+    from oracle.slices import host_slices
+    d = case.dims
+    kv = 0
+    for b in seqs:
+        lo = max(0, case.q_pos_host[b] - case.window + 1)
+        hi = min(case.q_pos_host[b] + d["q_len"], case.seq_lens_host[b])
+        kv += d["num_kv_heads"] * max(0, hi - lo) * 2 * d["head_dim"] * 2
+    return host_slices(case, seqs, margin=0), kv
+
+
+def time_oracle(case, budget_s, threads=None, steps=None, warmup=0):
+    """The fp64 oracle (``oracle.attention``, as it stands) timed on the host
+    cores over a bounded sample of the workload: the first n sequences (all
+    heads and draft rows of each), n sized from one sequence's cost so a call
+    takes about a quarter of the budget.  Runs `steps` calls after `warmup`
+    untimed ones, or calls until the budget is spent.  Both the CPU-baseline
+    leg and the reference arm use this routine.  Returns seconds per call,
+    the KV GB/s of the sample, and how it was sampled."""
     import oracle
-    from tests.helpers import host_slices
     B = case.q.shape[0]
-    kv, _ = workload_bytes(case)
     threads = threads or oracle.default_threads()
-    seqs = list(range(B))
-    # estimate cost per sequence from its window span to bound the sample
-    q, k, v, base, sl, qp = host_slices(case, seqs[:1], margin=0)
+    (q, k, v, base, sl, qp), _ = oracle_window(case, [0])
     t0 = time.perf_counter()
     oracle.attention(q, k, v, sl, qp, case.window, case.scale, base=base, threads=threads)
     per_seq = max(time.perf_counter() - t0, 1e-6)
-    n_seq = max(1, min(B, int(budget_s / 4 / per_seq)))
-    seqs = seqs[:n_seq]
-    q, k, v, base, sl, qp = host_slices(case, seqs, margin=0)
+    per_call_budget = budget_s / 4 if steps is None else budget_s / max(steps + warmup, 1)
+    n_seq = max(1, min(B, int(per_call_budget / per_seq)))
+    (q, k, v, base, sl, qp), kv = oracle_window(case, list(range(n_seq)))
+    for _ in range(warmup):
+        oracle.attention(q, k, v, sl, qp, case.window, case.scale, base=base, threads=threads)
     calls = 0
     t0 = time.perf_counter()
     while True:
         oracle.attention(q, k, v, sl, qp, case.window, case.scale, base=base, threads=threads)
         calls += 1
         el = time.perf_counter() - t0
-        if el >= budget_s or (max_calls and calls >= max_calls):
+        if (steps is not None and calls >= steps) or (steps is None and el >= budget_s):
             break
-    per_call_sample = el / calls
-    frac = n_seq / B
-    per_call_full = per_call_sample / frac
+    per_call = el / calls
     used = min(threads, n_seq * case.q.shape[2])
-    sample = (f"{calls} oracle calls over {n_seq} of {B} sequences (all rows and heads of "
-              f"each), {el:.1f} s, scaled to the full batch")
-    return {"seconds_per_call": per_call_full, "sample": sample, "cores": used,
-            "kv_gbs": kv / per_call_full / 1e9}
+    sample = (f"{calls} fp64 oracle calls over {n_seq} of {B} sequences (all heads and draft rows "
+              f"of each), {el:.2f} s, {used} threads busy of {threads} started")
+    return {"seconds_per_call": per_call, "kv_gbs": kv / per_call / 1e9, "sample": sample,
+            "threads_used": used, "sequences": n_seq}
+
+
+def cpu_baseline(case, budget_s):
+    """The oracle at all host threads and at one thread (a third of the
+    budget), reported in the metric's unit (KV GB/s of the sampled
+    sequences)."""
+    host = os.cpu_count() or 1
+    a = time_oracle(case, budget_s)
+    one = time_oracle(case, max(0.2, budget_s / 3), threads=1)
+    return {"value": round(a["kv_gbs"], 6), "unit": UNIT, "cores": a["threads_used"],
+            "threads_used": a["threads_used"], "host_cores": host, "kind": "oracle",
+            "sample": a["sample"],
+            "single_thread": {"value": round(one["kv_gbs"], 6), "unit": UNIT, "cores": 1,
+                              "sample": one["sample"]}}
 
 
 # ------------------------------------------------------------------- main
@@ -619,6 +669,12 @@ def launch_floor_stream(steps):
 
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal bandwidth
 
+# every configuration of the workload table beside the headline one: tiny
+# (q_len 1 and 8), window-vs-full (W 188 and the whole context), the batched
+# verify, and the nine bandwidth-stress combinations
+ALSO_DEFAULT = (["tiny_q1", "tiny_q8", "window_vs_full_w188", "window_vs_full_w4096", "batched"] +
+                [f"stress_w{w}_q{q}" for w in (188, 512, 1024) for q in (1, 8, 64)])
+
 
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -640,10 +696,11 @@ def tensor_peak():
         return 1900.0, "fallback"
 
 
-def extra_entry(name, dev, peak, tpeak, sms, steps=None):
+def extra_entry(name, dev, peak, tpeak, sms, steps=None, cpu_budget=0.0):
     """One more workload measured like the main one (device time, graph
     replay, L2 defeated): time per call, HBM and tensor-pipe fractions of
-    the peaks, and the plan the library picks for it."""
+    the peaks, the plan the library picks for it and, with a CPU budget, the
+    oracle on a sample of it at all host threads and at one."""
     import sliding_window_speculative_gb300 as swa
     case = make_workload(name, dev)
     kv, total = workload_bytes(case)
@@ -660,8 +717,10 @@ def extra_entry(name, dev, peak, tpeak, sms, steps=None):
              "frac_nominal": round(ach / NOMINAL_HBM_GBS, 4),
              "useful_tflops": round(tf, 3), "tensor_frac": round(tf / tpeak, 5),
              "tokens_per_s": round(case.q.shape[0] * case.q.shape[1] / sec),
-             "steps": steps, "replicas": r["replicas"],
+             "steps": steps, "replicas": r["replicas"], "l2": r["l2_scheme"],
              "splits": plan["num_splits"], "traffic": ncu_traffic(name)[0]}
+    if cpu_budget > 0:
+        entry["cpu_baseline"] = cpu_baseline(case, cpu_budget)
     del case
     torch.cuda.empty_cache()
     return entry
@@ -677,10 +736,12 @@ def main():
     ap.add_argument("--splits", type=int, default=0, help="force a split count (0 = heuristic)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--also",
-                    default="tiny_q8,window_vs_full_w188,window_vs_full_w4096,batched,stress_w188_q8",
+    ap.add_argument("--also", default=",".join(ALSO_DEFAULT),
                     help="extra workloads measured the same way (rank 0, device time)")
-    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle time for the headline workload's CPU baseline")
+    ap.add_argument("--also-cpu-budget", type=float, default=1.2,
+                    help="seconds of oracle time for each extra workload's CPU baseline")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -730,8 +791,8 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, **case.dims, "window": case.window,
                    "kv_bytes_per_call": kv, "bytes_per_call": total,
-                   "l2": f"defeated by {r['replicas']} input replicas"
-                         if r["replicas"] > 1 else "inputs larger than L2",
+                   "l2": (f"defeated by {r['replicas']} input replicas: {r['l2_scheme']}"
+                          if r["replicas"] > 1 else "inputs larger than L2"),
                    "timing": "CUDA graph of calls, CUDA events on the launching stream",
                    "plan": plan, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "kernel": KERNEL_NAMES.get(plan["kernel"], "?") +
@@ -764,7 +825,8 @@ def main():
                        "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
     if rank == 0 and world == 1 and args.also:
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        line["also"] = {name: extra_entry(name, dev, peak, tpeak, sms)
+        budget = 0.0 if args.no_cpu_baseline else args.also_cpu_budget
+        line["also"] = {name: extra_entry(name, dev, peak, tpeak, sms, cpu_budget=budget)
                         for name in args.also.split(",") if name and name != args.workload}
         # greedy verification of the draft block over a Gemma-size vocabulary
         # (one sequence, and a 64-sequence batch)
@@ -778,13 +840,7 @@ def main():
         line["append"] = [time_append("single_stream"), time_append("batched"),
                           time_append("stress_w188_q8", steps=200)]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = oracle_sample(case, args.cpu_budget)
-        line["cpu_baseline"] = {"value": round(cb["kv_gbs"], 6), "unit": UNIT,
-                                "cores": cb["cores"], "kind": "oracle", "sample": cb["sample"]}
-        # the same oracle on one host thread, over a shorter sample
-        c1 = oracle_sample(case, max(1.0, args.cpu_budget / 3), threads=1)
-        line["cpu_baseline"]["single_thread"] = {"value": round(c1["kv_gbs"], 6), "unit": UNIT,
-                                                 "cores": 1, "sample": c1["sample"]}
+        line["cpu_baseline"] = cpu_baseline(case, args.cpu_budget)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -795,50 +851,26 @@ def main():
 def main_reference(args, world, rank):
     """The oracle as the reference arm: each step is one oracle call over a
     bounded sample of the workload's sequences (all heads and rows of each),
-    sized so that warm-up plus K steps stay within about three minutes."""
+    sized so that warm-up plus K steps stay within about three minutes; timed
+    by the same routine as the CPU-baseline leg of the GPU arm."""
     if rank != 0:
         return
-    import oracle
     from oracle import build as oraclebuild
-    from tests.helpers import host_slices
     oraclebuild.build()
     case = make_workload(args.workload, "cpu")
-    B = case.q.shape[0]
-    threads = oracle.default_threads()
-    q, k, v, base, sl, qp = host_slices(case, [0], margin=0)
-    t0 = time.perf_counter()
-    oracle.attention(q, k, v, sl, qp, case.window, case.scale, base=base, threads=threads)
-    per_seq = max(time.perf_counter() - t0, 1e-6)
-    budget = 150.0 / max(args.steps + args.warmup, 1)
-    n_seq = max(1, min(B, int(budget / per_seq)))
-    seqs = list(range(n_seq))
-    q, k, v, base, sl, qp = host_slices(case, seqs, margin=0)
-    sub_kv = 0
-    d = case.dims
-    for b in seqs:
-        lo = max(0, case.q_pos_host[b] - case.window + 1)
-        hi = min(case.q_pos_host[b] + d["q_len"], case.seq_lens_host[b])
-        sub_kv += d["num_kv_heads"] * max(0, hi - lo) * 2 * d["head_dim"] * 2
-    for _ in range(args.warmup):
-        oracle.attention(q, k, v, sl, qp, case.window, case.scale, base=base, threads=threads)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.attention(q, k, v, sl, qp, case.window, case.scale, base=base, threads=threads)
-    el = time.perf_counter() - t0
-    per_step = el / args.steps
-    value = sub_kv / per_step / 1e9
-    used = min(threads, n_seq * case.q.shape[2])
-    sample = (f"each step: one fp64 oracle call over {n_seq} of {B} sequences "
-              f"(all heads and draft rows), {threads} threads")
+    r = time_oracle(case, 150.0, steps=args.steps, warmup=args.warmup)
+    per_step = r["seconds_per_call"]
+    value = r["kv_gbs"]
     line = {
         "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
         "config": {"workload": args.workload, **case.dims, "window": case.window,
-                   "sampled_sequences": n_seq},
-        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": used,
-                         "kind": "oracle", "sample": sample},
+                   "sampled_sequences": r["sequences"]},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": r["threads_used"],
+                         "threads_used": r["threads_used"], "host_cores": os.cpu_count() or 1,
+                         "kind": "oracle", "sample": r["sample"]},
         "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

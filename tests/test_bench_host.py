@@ -26,7 +26,8 @@ def test_extra_entry_from_a_fixed_time(monkeypatch):
     from sliding_window_speculative_gb300 import build
     build.build()
     monkeypatch.setattr(bench, "time_device",
-                        lambda case, steps, warmup: {"us_per_call": 10.0, "replicas": 3})
+                        lambda case, steps, warmup: {"us_per_call": 10.0, "replicas": 3,
+                                                     "l2_scheme": "x"})
     e = bench.extra_entry("single_stream", "cpu", peak=6660.0, tpeak=1884.6, sms=152)
     assert e["us_per_call"] == 10.0 and e["replicas"] == 3
     assert e["kv_gbs"] == pytest.approx(399_360 / 10e-6 / 1e9, abs=0.01)
@@ -65,3 +66,38 @@ def test_source_digest_covers_the_kernel_sources(tmp_path, monkeypatch):
     with open(pkg / "csrc" / "swa_tc.cuh", "a") as f:
         f.write("\n")
     assert bench.source_digest() != before
+
+
+@pytest.mark.parametrize("steps", [1, 20, 300, 1000, 20000])
+@pytest.mark.parametrize("name", ["tiny_q1", "tiny_q8", "single_stream", "batched"])
+def test_replicas_keep_timed_calls_out_of_l2(name, steps):
+    """Whatever the step count: either every timed call reads its own
+    replica (and L2 is flushed before the timed replay), or one cycle
+    through the replicas reads at least twice L2; the replicas fit in
+    16 GiB."""
+    case = bench.make_workload(name, "cpu")
+    _, total = bench.workload_bytes(case)
+    l2 = 126 << 20
+    n, _, distinct = bench.replica_count(case, total, steps, l2=l2)
+    slab = case.k_cache.numel() * 4 + case.q.numel() * 4
+    assert n * slab <= 16 << 30
+    if distinct:
+        assert n >= steps
+    else:
+        assert n * total >= 2 * l2
+
+
+def test_replicas_not_needed_above_l2():
+    case = bench.make_workload("tiny_q8", "cpu")
+    assert bench.replica_count(case, 200 << 20, 20, l2=126 << 20) == (1, 126 << 20, False)
+
+
+def test_cpu_baseline_reports_threads_and_host_cores():
+    import os
+    case = bench.make_workload("tiny_q8", "cpu")
+    cb = bench.cpu_baseline(case, 0.3)
+    assert cb["kind"] == "oracle" and cb["unit"] == "GB/s" and cb["value"] > 0
+    assert cb["host_cores"] == (os.cpu_count() or 1)
+    # tiny: one sequence of 2 query heads -> at most 2 threads have work
+    assert cb["threads_used"] == cb["cores"] == min(2, os.cpu_count() or 1)
+    assert cb["single_thread"]["cores"] == 1 and cb["single_thread"]["value"] > 0
