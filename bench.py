@@ -341,15 +341,19 @@ def _packed(parts, device=None, pin=False, align=256):
     return buf, views
 
 
-def time_e2e(case, steps, warmup):
+def time_e2e(case, steps, warmup, graph=False):
     """Through the public call with host buffers: each step copies the
     step's inputs (q, the q_len new K/V rows of every sequence and KV head,
     seq_lens, q_pos), packed in one pinned host buffer, to the device in one
-    copy; calls swa_append_verify_attn, which writes the new rows into the
-    cache and attends over it; and copies out and lse, packed in one device
-    buffer, back to pinned host memory in one copy.  Timed with CUDA events
+    copy; issues swa_append_verify_attn (prepared once: validated and
+    marshalled outside the loop), which writes the new rows into the cache
+    and attends over it; and copies out and lse, packed in one device
+    buffer, back to pinned host memory in one copy.  With graph=True the
+    three operations of a step are captured once as one CUDA graph and each
+    step is one replay (the single-graph decode step of the pages,
+    ONEGRAPH): the copies still run every step.  Timed with CUDA events
     around all steps."""
-    from sliding_window_speculative_gb300 import swa_append_verify_attn
+    from sliding_window_speculative_gb300 import prepare, swa_append_verify_attn
     B, q_len, Hq, D = case.q.shape
     Hkv = case.k_cache.shape[1]
     dev = case.q.device
@@ -371,29 +375,48 @@ def time_e2e(case, steps, warmup):
     stream = torch.cuda.Stream()
     h2d = h_in.numel()
     d2h = h_out.numel()
+    call = prepare(swa_append_verify_attn, d_q, d_kn, d_vn, case.k_cache, case.v_cache, d_sl,
+                   d_qp, case.window, case.scale, out=out, lse=lse, stream=stream)
 
     def step():
         d_in.copy_(h_in, non_blocking=True)
-        swa_append_verify_attn(d_q, d_kn, d_vn, case.k_cache, case.v_cache, d_sl, d_qp,
-                               case.window, case.scale, out=out, lse=lse, stream=stream)
+        call()
         h_out.copy_(d_out, non_blocking=True)
 
     with torch.cuda.stream(stream):
         for _ in range(max(warmup, 3)):
             step()
     stream.synchronize()
+    run = step
+    if graph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        with torch.cuda.stream(stream):
+            g.replay()
+        stream.synchronize()
+        run = g.replay
+    h_o.zero_()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(steps):
-            step()
+            run()
         end.record(stream)
     torch.cuda.synchronize()
     ms = start.elapsed_time(end)
     return {"us_per_call": ms * 1e3 / steps, "h2d": h2d, "d2h": d2h, "steps": steps,
-            "out": h_o, "lse": h_l}
+            "out": h_o.clone(), "lse": h_l.clone()}
+
+
+def e2e_entry(case, steps, warmup, graph):
+    kv, _ = workload_bytes(case)
+    e = time_e2e(case, steps, warmup, graph=graph)
+    return {"value": round(kv / (e["us_per_call"] * 1e-6) / 1e9, 3), "unit": UNIT,
+            "us_per_call": round(e["us_per_call"], 3), "h2d_bytes_per_step": e["h2d"],
+            "d2h_bytes_per_step": e["d2h"]}
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -819,10 +842,20 @@ def main():
         "gpu_launches": launches_per_call * args.steps,
     }
     if rank == 0 and not args.no_e2e:
-        e = time_e2e(case, min(args.steps, 2000), args.warmup)
-        line["e2e"] = {"value": round(kv / (e["us_per_call"] * 1e-6) / 1e9, 3), "unit": UNIT,
-                       "us_per_call": round(e["us_per_call"], 3),
-                       "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
+        # host loop: per step one input copy, the prepared call, one output copy
+        n_e2e = min(args.steps, 2000)
+        line["e2e"] = e2e_entry(case, n_e2e, args.warmup, graph=False)
+        line["e2e"]["how"] = ("host loop per step: H2D copy of the packed inputs from pinned "
+                              "memory, the prepared swa_append_verify_attn call, D2H copy of "
+                              "out and lse into pinned memory")
+        # the same step captured once as one CUDA graph, replayed per step
+        line["e2e"]["graph"] = e2e_entry(case, n_e2e, args.warmup, graph=True)
+        if world == 1 and args.workload != "batched":
+            bcase = make_workload("batched", dev)
+            line["e2e"]["batched"] = e2e_entry(bcase, min(n_e2e, 500), args.warmup, graph=False)
+            line["e2e"]["batched"]["graph"] = e2e_entry(bcase, min(n_e2e, 500), args.warmup,
+                                                        graph=True)
+            del bcase
     if rank == 0 and world == 1 and args.also:
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         budget = 0.0 if args.no_cpu_baseline else args.also_cpu_budget

@@ -113,16 +113,14 @@ class SwaPaged(ctypes.Structure):
                 ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32)]
 
 
-def swa_verify_attn_paged(q, k_pages, v_pages, block_table, seq_lens, q_pos, window, scale,
-                          out=None, lse=None, num_splits=0, stream=None):
-    """Windowed verify attention over a paged cache (C entry point
-    swa_verify_attn_paged).
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
-    k_pages, v_pages bf16 [num_pages, Hkv, page_size, D]; block_table int32
-    [B, max_blocks] (device): block k of sequence b is page
-    block_table[b, k].  Everything else as swa_verify_attn.
-    """
-    lib = load_library()
+
+def _marshal_paged(q, k_pages, v_pages, block_table, seq_lens, q_pos, window, scale,
+                   out=None, lse=None, num_splits=0, stream=None):
     B, q_len, Hq, D = q.shape
     pq = _dev_tensor(q, "q", torch.bfloat16, 4)
     pk = _dev_tensor(k_pages, "k_pages", torch.bfloat16, 4)
@@ -144,24 +142,33 @@ def swa_verify_attn_paged(q, k_pages, v_pages, block_table, seq_lens, q_pos, win
     max_blocks = block_table.shape[1]
     paged = SwaPaged(pt, max_blocks, page_size, num_pages)
     dims = make_dims(B, q_len, Hq, Hkv, D, max_blocks * page_size, num_splits)
-    if stream is None:
-        stream = torch.cuda.current_stream(q.device)
-    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    _check(lib.swa_verify_attn_paged(pq, pk, pv, ctypes.byref(paged), ps, pp, int(window),
-                                     float(scale), po, pl, ctypes.byref(dims), handle))
-    return out, lse
+    handle = _stream_handle(stream, q.device)
+    args = (pq, pk, pv, ctypes.byref(paged), ps, pp, int(window), float(scale), po, pl,
+            ctypes.byref(dims), handle)
+    keep = (q, k_pages, v_pages, block_table, seq_lens, q_pos, out, lse, paged, dims)
+    return "swa_verify_attn_paged", args, keep, (out, lse)
 
 
-def swa_append_verify_attn(q, k_new, v_new, k_cache, v_cache, seq_lens, q_pos, window, scale,
-                           block_table=None, out=None, lse=None, num_splits=0, stream=None):
-    """Fused KV append + windowed verify attention (C entry point
-    swa_append_verify_attn): writes k_new / v_new bf16 [B, q_len, Hkv, D]
-    into the cache at positions q_pos + i, then attends over the updated
-    cache.  Without block_table the caches are [B, Hkv, max_len, D]; with it
-    they are page pools [num_pages, Hkv, page_size, D] as in
-    swa_verify_attn_paged.  The caches are modified in place.
+def swa_verify_attn_paged(q, k_pages, v_pages, block_table, seq_lens, q_pos, window, scale,
+                          out=None, lse=None, num_splits=0, stream=None):
+    """Windowed verify attention over a paged cache (C entry point
+    swa_verify_attn_paged).
+
+    k_pages, v_pages bf16 [num_pages, Hkv, page_size, D]; block_table int32
+    [B, max_blocks] (device): block k of sequence b is page
+    block_table[b, k].  Everything else as swa_verify_attn.
     """
-    lib = load_library()
+    return _issue(*_marshal_paged(q, k_pages, v_pages, block_table, seq_lens, q_pos, window,
+                                  scale, out, lse, num_splits, stream))
+
+
+def _issue(entry, args, keep, result):
+    _check(getattr(load_library(), entry)(*args))
+    return result
+
+
+def _marshal_append(q, k_new, v_new, k_cache, v_cache, seq_lens, q_pos, window, scale,
+                    block_table=None, out=None, lse=None, num_splits=0, stream=None):
     B, q_len, Hq, D = q.shape
     pq = _dev_tensor(q, "q", torch.bfloat16, 4)
     pkn = _dev_tensor(k_new, "k_new", torch.bfloat16, 4)
@@ -192,14 +199,25 @@ def swa_append_verify_attn(q, k_new, v_new, k_cache, v_cache, seq_lens, q_pos, w
     else:
         max_len = k_cache.shape[2]
     dims = make_dims(B, q_len, Hq, Hkv, D, max_len, num_splits)
-    if stream is None:
-        stream = torch.cuda.current_stream(q.device)
-    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    _check(lib.swa_append_verify_attn(pq, pkn, pvn, pk, pv,
-                                      ctypes.byref(paged) if paged is not None else None, ps, pp,
-                                      int(window), float(scale), po, pl, ctypes.byref(dims),
-                                      handle))
-    return out, lse
+    handle = _stream_handle(stream, q.device)
+    args = (pq, pkn, pvn, pk, pv, ctypes.byref(paged) if paged is not None else None, ps, pp,
+            int(window), float(scale), po, pl, ctypes.byref(dims), handle)
+    keep = (q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, q_pos, out, lse, paged,
+            dims)
+    return "swa_append_verify_attn", args, keep, (out, lse)
+
+
+def swa_append_verify_attn(q, k_new, v_new, k_cache, v_cache, seq_lens, q_pos, window, scale,
+                           block_table=None, out=None, lse=None, num_splits=0, stream=None):
+    """Fused KV append + windowed verify attention (C entry point
+    swa_append_verify_attn): writes k_new / v_new bf16 [B, q_len, Hkv, D]
+    into the cache at positions q_pos + i, then attends over the updated
+    cache.  Without block_table the caches are [B, Hkv, max_len, D]; with it
+    they are page pools [num_pages, Hkv, page_size, D] as in
+    swa_verify_attn_paged.  The caches are modified in place.
+    """
+    return _issue(*_marshal_append(q, k_new, v_new, k_cache, v_cache, seq_lens, q_pos, window,
+                                   scale, block_table, out, lse, num_splits, stream))
 
 
 def make_dims(batch, q_len, num_q_heads, num_kv_heads, head_dim, max_len, num_splits=0):
@@ -226,16 +244,8 @@ def _dev_tensor(t, name, dtype, ndim):
     return t.data_ptr()
 
 
-def swa_verify_attn(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out=None, lse=None,
-                    num_splits=0, stream=None, want_lse=True, _entry="swa_verify_attn"):
-    """Windowed verify attention through the C entry point swa_verify_attn.
-
-    q bf16 [B, q_len, Hq, D]; k_cache, v_cache bf16 [B, Hkv, L, D];
-    seq_lens, q_pos int32 [B] (device).  Returns (out, lse); out/lse are
-    allocated if not given (lse only if want_lse).  Enqueued on `stream`
-    (default: torch's current stream); does not synchronise.
-    """
-    lib = load_library()
+def _marshal_verify(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out=None, lse=None,
+                    num_splits=0, stream=None, want_lse=True, entry="swa_verify_attn"):
     B, q_len, Hq, D = q.shape
     pq = _dev_tensor(q, "q", torch.bfloat16, 4)
     pk = _dev_tensor(k_cache, "k_cache", torch.bfloat16, 4)
@@ -261,12 +271,31 @@ def swa_verify_attn(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out=Non
         if tuple(lse.shape) != (B, q_len, Hq):
             raise ValueError("lse must be [B, q_len, Hq]")
     dims = dims_of(q, k_cache, num_splits)
-    if stream is None:
-        stream = torch.cuda.current_stream(q.device)
-    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    _check(getattr(lib, _entry)(pq, pk, pv, ps, pp, int(window), float(scale), po, pl,
-                                ctypes.byref(dims), handle))
-    return out, lse
+    handle = _stream_handle(stream, q.device)
+    args = (pq, pk, pv, ps, pp, int(window), float(scale), po, pl, ctypes.byref(dims), handle)
+    keep = (q, k_cache, v_cache, seq_lens, q_pos, out, lse, dims)
+    return entry, args, keep, (out, lse)
+
+
+def swa_verify_attn(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out=None, lse=None,
+                    num_splits=0, stream=None, want_lse=True):
+    """Windowed verify attention through the C entry point swa_verify_attn.
+
+    q bf16 [B, q_len, Hq, D]; k_cache, v_cache bf16 [B, Hkv, L, D];
+    seq_lens, q_pos int32 [B] (device).  Returns (out, lse); out/lse are
+    allocated if not given (lse only if want_lse).  Enqueued on `stream`
+    (default: torch's current stream); does not synchronise.
+    """
+    return _issue(*_marshal_verify(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out, lse,
+                                   num_splits, stream, want_lse))
+
+
+def _marshal_noalloc(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out, lse=None,
+                     num_splits=0, stream=None):
+    if out is None:
+        raise ValueError("swa_verify_attn_noalloc writes into a caller-given out tensor")
+    return _marshal_verify(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out, lse,
+                           num_splits, stream, want_lse=False, entry="swa_verify_attn_noalloc")
 
 
 def swa_verify_attn_noalloc(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out, lse=None,
@@ -279,11 +308,50 @@ def swa_verify_attn_noalloc(q, k_cache, v_cache, seq_lens, q_pos, window, scale,
     owns every allocation, a path that cannot take cudaMalloc's device
     synchronisation).  Overlapping calls on one device share the scratch and
     race; make the first call on a device outside stream capture."""
-    if out is None:
-        raise ValueError("swa_verify_attn_noalloc writes into a caller-given out tensor")
-    return swa_verify_attn(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out=out,
-                           lse=lse, num_splits=num_splits, stream=stream, want_lse=False,
-                           _entry="swa_verify_attn_noalloc")
+    return _issue(*_marshal_noalloc(q, k_cache, v_cache, seq_lens, q_pos, window, scale, out,
+                                    lse, num_splits, stream))
+
+
+class PreparedCall:
+    """One attention call validated and marshalled once (see prepare()).
+
+    Calling the object re-issues the same C call with the same pointers,
+    shapes, window, scale and stream; the tensors' contents may change
+    between calls (a serving loop writes the next step's rows into the same
+    buffers).  Returns the (out, lse) tensors the call writes.  The object
+    keeps every tensor it points at alive."""
+
+    def __init__(self, entry, args, keep, result):
+        self._fn = getattr(load_library(), entry)
+        self.entry = entry
+        self._args = args
+        self._keep = keep
+        self.result = result
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st != SWA_OK:
+            _check(st)
+        return self.result
+
+
+_MARSHAL = {"swa_verify_attn": _marshal_verify, "swa_verify_attn_noalloc": _marshal_noalloc,
+            "swa_verify_attn_paged": _marshal_paged, "swa_append_verify_attn": _marshal_append}
+
+
+def prepare(fn, *args, **kwargs):
+    """Validate and marshal a call of swa_verify_attn, swa_verify_attn_noalloc,
+    swa_verify_attn_paged or swa_append_verify_attn once, with the same
+    arguments the function takes, and return a PreparedCall that issues it.
+
+    The per-call host cost is then one C call: no tensor checks, no struct
+    building, no stream lookup (the stream is the one given, or torch's
+    current stream at prepare time).  Outputs are allocated here if not
+    given."""
+    name = fn if isinstance(fn, str) else fn.__name__
+    if name not in _MARSHAL:
+        raise ValueError(f"cannot prepare {name}; one of {sorted(_MARSHAL)}")
+    return PreparedCall(*_MARSHAL[name](*args, **kwargs))
 
 
 def swa_greedy_accept(logits, draft=None, keep_ids=None, argmax=None, accepted=None,
