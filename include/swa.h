@@ -229,7 +229,12 @@ typedef struct {
                                   its n-th K/V fill but never issues the copies, so every wait
                                   on that fill runs out and the call reports bit 0 through
                                   swa_read_device_errors (the test of the bounded waits) */
-    int32_t reserved;          /* must be 0 */
+    int32_t rows_per_item;     /* 0 (default): the plan's packed rows per tensor-core work
+                                  item; n > 0: n capped at the kernel's maximum (64
+                                  key-major, 128 rows-major) and at q_len * Hq / Hkv,
+                                  then rounded down to a multiple of Hq / Hkv (at least
+                                  one); no effect on CUDA-core plans or when num_splits
+                                  is forced */
 } swa_debug_options;
 
 /* Set the controls above (NULL restores the defaults).  Returns

@@ -40,7 +40,7 @@ class SwaDebugOptions(ctypes.Structure):
     """swa_debug_options of include/swa.h (test and sweep controls)."""
     _fields_ = [("force_kernel", ctypes.c_int32), ("pdl", ctypes.c_int32),
                 ("wait_limit_cycles", ctypes.c_int64), ("withhold_fill", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("rows_per_item", ctypes.c_int32)]
 
 
 # force_kernel values of swa_debug_options
@@ -430,13 +430,16 @@ def swa_version():
     return load_library().swa_version().decode()
 
 
-def swa_set_debug_options(force_kernel=0, pdl=1, wait_limit_cycles=0, withhold_fill=-1):
+def swa_set_debug_options(force_kernel=0, pdl=1, wait_limit_cycles=0, withhold_fill=-1,
+                          rows_per_item=0):
     """Test and sweep controls of the C entry point swa_set_debug_options
     (not for serving).  force_kernel: 0 or "plan", 1 or "simt", 2 or "tc",
     3 or "rows"; pdl 1/0; wait_limit_cycles 0 (default ~2e9) or the bounded
-    waits' limit; withhold_fill -1 or the fill the first CTA never copies."""
+    waits' limit; withhold_fill -1 or the fill the first CTA never copies;
+    rows_per_item 0 (the plan's) or packed rows per tensor-core work item."""
     fk = KERNEL_IDS[force_kernel] if isinstance(force_kernel, str) else int(force_kernel)
-    opt = SwaDebugOptions(fk, int(pdl), int(wait_limit_cycles), int(withhold_fill), 0)
+    opt = SwaDebugOptions(fk, int(pdl), int(wait_limit_cycles), int(withhold_fill),
+                          int(rows_per_item))
     _check(load_library().swa_set_debug_options(ctypes.byref(opt)))
 
 

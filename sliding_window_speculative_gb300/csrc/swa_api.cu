@@ -83,6 +83,7 @@ struct Plan {
     long long workspace;
     long long grid;   // CTAs of the attention kernel
     long long items;  // tensor-core path: work items
+    int sms;          // SMs of the device the plan is for
 };
 
 int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
@@ -93,6 +94,7 @@ std::atomic<int> g_opt_force{0};
 std::atomic<int> g_opt_pdl{1};
 std::atomic<long long> g_opt_wait_limit{0};
 std::atomic<int> g_opt_withhold{-1};
+std::atomic<int> g_opt_rows{0};
 
 // Kernel override of a test or sweep: 0 none, 1 CUDA-core, 2 key-major, 3 rows-major.
 int forced_kernel() { return g_opt_force.load(std::memory_order_relaxed); }
@@ -113,6 +115,7 @@ int forced_kernel() { return g_opt_force.load(std::memory_order_relaxed); }
 // Chunks are multiples of 16 keys; at most kMaxSplits chunks.
 Plan make_plan_with(const swa_dims *d, int32_t window, int num_sms, int force) {
     Plan p{};
+    p.sms = num_sms;
     const int G = d->num_q_heads / d->num_kv_heads;
     const int R = d->q_len * G;
     const int D = d->head_dim;
@@ -214,6 +217,21 @@ Plan make_plan_with(const swa_dims *d, int32_t window, int num_sms, int force) {
                     p.tc_n = 16 * ((rows + 15) / 16);
                     break;
                 }
+            }
+        }
+        const int force_rows = g_opt_rows.load(std::memory_order_relaxed);
+        if (force_rows > 0 && d->num_splits == 0) {
+            // a sweep's override of the rows per item
+            const int max_rows = use_rows ? 128 : 64;
+            int rows = force_rows < max_rows ? force_rows : max_rows;
+            rows = rows < R ? rows : R;
+            rows = rows < G ? G : (rows / G) * G;
+            if (rows <= max_rows) {
+                p.rows_per_tile = rows;
+                p.q_rows_per_tile = rows / G;
+                p.row_tiles = ceil_div(d->q_len, p.q_rows_per_tile);
+                p.tc_n = use_rows ? (rows <= 32 ? 32 : rows <= 64 ? 64 : 128)
+                                  : 16 * ((rows + 15) / 16);
             }
         }
         p.items = (long long)splits * d->batch * d->num_kv_heads * p.row_tiles;
@@ -372,6 +390,16 @@ swa_status launch_plan(const Plan &pl, const swa_dims *dims, const swa::AttnPara
         L.T.rows_per_tile = pl.rows_per_tile;
         L.T.q_rows_per_tile = pl.q_rows_per_tile;
         L.T.items = (int)pl.items;
+        // contiguous blocks of items per CTA for the key-major kernel (measured
+        // on GB300, stress W188: q8 50.6 -> 48.8 us, q1 41.1 -> 40.0 us); the
+        // rows-major kernel deals them round-robin (blocks: W188 q64 127.2 ->
+        // 128.6 us, W1024 q64 405.5 -> 440.5 us)
+        L.T.items_per_cta = pl.kernel == 2 ? (int)(pl.items / pl.grid) : 0;
+        L.T.items_extra = pl.kernel == 2 ? (int)(pl.items % pl.grid) : 0;
+        // measured on GB300: single_stream (8 CTAs) 7.86 -> 7.33 us with every
+        // first fill issued at once; batched (128 CTAs) 11.6 -> 10.9 us with the
+        // first K tile alone ahead (11.4 us with all)
+        L.T.early_max = pl.grid * 2 >= pl.sms ? 1 : 8;
         L.D = dims->head_dim;
         L.N = pl.tc_n;
         L.rows_major = pl.kernel == 3;
@@ -710,11 +738,13 @@ swa_status swa_set_debug_options(const swa_debug_options *opt) {
                     (long long)d.wait_limit_cycles);
     if (d.withhold_fill < -1)
         return fail(SWA_ERR_INVALID_ARG, "withhold_fill %d < -1", d.withhold_fill);
-    if (d.reserved != 0) return fail(SWA_ERR_INVALID_ARG, "reserved must be 0");
+    if (d.rows_per_item < 0)
+        return fail(SWA_ERR_INVALID_ARG, "rows_per_item %d < 0", d.rows_per_item);
     g_opt_force.store(d.force_kernel, std::memory_order_relaxed);
     g_opt_pdl.store(d.pdl, std::memory_order_relaxed);
     g_opt_wait_limit.store(d.wait_limit_cycles, std::memory_order_relaxed);
     g_opt_withhold.store(d.withhold_fill, std::memory_order_relaxed);
+    g_opt_rows.store(d.rows_per_item, std::memory_order_relaxed);
     return SWA_OK;
 }
 
@@ -724,7 +754,7 @@ swa_status swa_get_debug_options(swa_debug_options *opt) {
     opt->pdl = g_opt_pdl.load(std::memory_order_relaxed);
     opt->wait_limit_cycles = g_opt_wait_limit.load(std::memory_order_relaxed);
     opt->withhold_fill = g_opt_withhold.load(std::memory_order_relaxed);
-    opt->reserved = 0;
+    opt->rows_per_item = g_opt_rows.load(std::memory_order_relaxed);
     return SWA_OK;
 }
 

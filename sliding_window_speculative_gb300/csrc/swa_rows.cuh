@@ -152,10 +152,8 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
     }
     grid_dep_wait();
     grid_dep_trigger();
-    for (int j = tid; j < kTcMetaItems; j += NTHR) {
-        const long long item = (long long)blockIdx.x + (long long)j * gridDim.x;
-        if (item < T.items) meta[j] = tc_decode_global<AP>(T, (int)item);
-    }
+    for (int j = tid; j < kTcMetaItems; j += NTHR)
+        if (j < cta_items(T)) meta[j] = tc_decode_global<AP>(T, cta_item(T, j));
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -163,7 +161,7 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
 
     if (warp == 0) {
         // ======================================================= producer
-        tile_producer<C, NT, QB, AP>(T, M, meta, ftab, ring, qs, bars);
+        tile_producer<C, NT, QB, AP>(T, M, meta, ftab, ring, qs, bars, false);
     } else if (warp == 1) {
         // ============================================================ MMA
         // Two cursors over the tile sequence: S = Q K^T of the next tile and
@@ -193,8 +191,10 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
                 c.par = (e >> 4) & 1u;
                 return true;
             };
+            const int n_items = cta_items(T);
             auto seek = [&](Cursor &c) {
-                for (; c.item < T.items; c.item += gridDim.x, ++c.j) {
+                for (; c.j < n_items; ++c.j) {
+                    c.item = cta_item(T, c.j);
                     const TcItem it = tc_decode<AP>(T, c.item, c.j, meta);
                     if (it.n_tiles > 0) {
                         c.n_tiles = it.n_tiles;
@@ -212,11 +212,10 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
                 c.slot = -1;
                 if (++c.t < c.n_tiles) return;
                 ++c.k;
-                c.item += gridDim.x;
                 ++c.j;
                 seek(c);
             };
-            Cursor qc{(int)blockIdx.x, 0, 0, 0, 0, 0, 0u, 0u, false, -1, 0u};
+            Cursor qc{0, 0, 0, 0, 0, 0, 0u, 0u, false, -1, 0u};
             seek(qc);
             Cursor pc = qc;
             bool ok = true;
@@ -366,9 +365,9 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
             };
             uint32_t g = 0, k = 0;
             bool ok = true;
-            int j = 0;
-            for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
-                const TcItem it = tc_decode<AP>(T, item, j, meta);
+            const int n_items = cta_items(T);
+            for (int j = 0; j < n_items && ok; ++j) {
+                const TcItem it = tc_decode<AP>(T, cta_item(T, j), j, meta);
                 const bool live = r < it.rows;
                 const int rg = it.row0 + r;  // packed row of the (sequence, KV head)
                 const int i = rg / P.G, gg = rg - i * P.G;
@@ -628,7 +627,7 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
     fence_after_sync();
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
     if constexpr (AP) {
-        if (T.items > 2 * (int)gridDim.x) append_flush<D>(T, meta, ring, NT * C::TILE_BYTES, NTHR);
+        if (cta_items(T) > 2) append_flush<D>(T, meta, ring, NT * C::TILE_BYTES, NTHR);
     }
 }
 

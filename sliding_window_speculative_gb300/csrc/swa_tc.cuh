@@ -133,6 +133,19 @@ struct TcCfg {
 };
 
 
+// The work items of this CTA, numbered j = 0, 1, ...: a contiguous block of
+// the item list (T.items_per_cta > 0: neighbouring (sequence, KV head) units
+// run back to back on one SM) or every gridDim.x-th item (round-robin).
+__device__ __forceinline__ int cta_items(const TcParams &T) {
+    if (T.items_per_cta > 0) return T.items_per_cta + ((int)blockIdx.x < T.items_extra ? 1 : 0);
+    return (T.items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+}
+__device__ __forceinline__ int cta_item(const TcParams &T, int j) {
+    if (T.items_per_cta > 0)
+        return (int)blockIdx.x * T.items_per_cta + min((int)blockIdx.x, T.items_extra) + j;
+    return (int)blockIdx.x + j * (int)gridDim.x;
+}
+
 // Work item `item` (its sequence's seq_len / q_pos read from global memory).
 template <bool AP>
 __device__ __forceinline__ TcItem tc_decode_global(const TcParams &T, int item) {
@@ -324,6 +337,54 @@ __device__ __forceinline__ void append_split(const AttnParams &P, int qp, int p,
     a_n = qp > p && ((qp - p) & 7) ? a_m + 1 : a_m;
 }
 
+// Fills of the CTA's first work item issued ahead of the producer loop:
+// its first min(NT, early_max, 2 * n_tiles) K/V fills (fill 2t + kv into
+// ring slot 2t + kv) and its Q rows; 0 if none (paged cache, fused append,
+// no item, an empty first item).  The producer loop computes the same count.
+template <int NT, bool AP>
+__device__ __forceinline__ int early_fills(const TcParams &T, const TcItem &it) {
+    if (AP || T.a.block_table != nullptr || it.n_tiles == 0) return 0;
+    return min(min(NT, T.early_max), 2 * it.n_tiles);
+}
+
+// Right after griddepcontrol.wait, lane 0 of warp w < early_fills issues
+// fill w of the CTA's first item (and warp NT the item's Q rows), each warp
+// decoding the item itself: the copies go out in parallel from separate
+// warps, ahead of the CTA's set-up barrier and of the producer loop (whose
+// first fills would otherwise leave one at a time).  The barriers and the
+// fill table must be initialised and a CTA barrier passed beforehand; no
+// other thread writes the bytes these copies land in (the Q rows TMA writes
+// are never zeroed).  A withheld fill (tests of the bounded waits) is
+// posted on its barrier but not copied.
+template <class C, int NT, bool AP>
+__device__ __forceinline__ void issue_early_fills(const TcParams &T, const TcMaps &M,
+                                                  volatile uint32_t *ftab, uint8_t *ring,
+                                                  uint8_t *qs, uint64_t *bars, int warp) {
+    using namespace tc;
+    const AttnParams &P = T.a;
+    if (AP || P.block_table != nullptr || warp > NT || cta_items(T) < 1) return;
+    const TcItem it = tc_decode_global<AP>(T, cta_item(T, 0));
+    const int n = early_fills<NT, AP>(T, it);
+    if (n == 0) return;
+    if (warp == NT) {
+        mbar_arrive_expect_tx(&bars[C::B_QFULL], C::SLABS * T.rows_per_tile * 128);
+        for (int s = 0; s < C::SLABS; ++s)
+            tma_load_3d(qs + s * C::Q_SLAB, &M.q, 64 * s, it.h * P.G, it.b * P.q_len + it.i0,
+                        &bars[C::B_QFULL]);
+        return;
+    }
+    if (warp >= n) return;
+    const int t = warp >> 1, kv = warp & 1;
+    const int p = it.t0 + kTcTileKeys * t;
+    const int n_valid = min(kTcTileKeys, it.cr.c_hi - p);
+    ftab[warp] = ((uint32_t)warp << 8) | (uint32_t)warp;  // fill w -> slot w, use parity 0
+    mbar_arrive_expect_tx(&bars[C::B_FULL + warp], (uint32_t)((n_valid + 7) >> 3) * C::ATOM_BYTES);
+    if (P.withhold_fill == warp && blockIdx.x == 0) return;
+    const uint64_t policy = P.row_tiles > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
+    tile_copies<C::ATOM_BYTES>(P, M, kv, it.b, it.h, p, n_valid, ring + warp * C::TILE_BYTES,
+                               &bars[C::B_FULL + warp], policy, 0);
+}
+
 // The TMA producer (warp 0) of both tensor-core kernels: lane 0 runs the
 // control (slots, barriers, the fill table, Q and the fused append's extra
 // copies) and the warp issues each tile's copies.  For every item of the
@@ -332,12 +393,14 @@ __device__ __forceinline__ void append_split(const AttnParams &P, int qp, int p,
 // the item's first K tile so a single Q buffer does not hold back the K
 // stream.  With a fused append, the atoms of a tile from the first new row
 // on (a mixed atom from the cache, new-row atoms from k_new / v_new) land on
-// B_MIX, for the append worker to complete the fill.  Waits for every copy
-// it issued before returning.
+// B_MIX, for the append worker to complete the fill.  With `early`, the
+// first item's first early_fills() fills and its Q rows were issued already
+// (issue_early_fills).  Waits for every copy it issued before returning.
 template <class C, int NT, int QB, bool AP>
 __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M,
                                               const TcItem *meta, volatile uint32_t *ftab,
-                                              uint8_t *ring, uint8_t *qs, uint64_t *bars) {
+                                              uint8_t *ring, uint8_t *qs, uint64_t *bars,
+                                              bool early) {
     using namespace tc;
     const AttnParams &P = T.a;
     const int lane = (int)(threadIdx.x & 31);
@@ -345,7 +408,7 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
     // cache) or the CTA has one item (latency-bound calls: measured faster);
     // a long run of items over a contiguous cache is faster with lane 0
     // alone (no per-fill warp synchronisation).
-    const bool coop = P.block_table != nullptr || T.items <= (int)gridDim.x;
+    const bool coop = P.block_table != nullptr || cta_items(T) <= 1;
     if (!coop && lane != 0) return;
     // K/V are read once per row tile: with one row tile nothing reads a line
     // again (evict first); with several, the row tiles of a (sequence, KV
@@ -357,10 +420,15 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
     uint32_t uses[NT];              // fills handed to each slot so far
 #pragma unroll
     for (int s2 = 0; s2 < NT; ++s2) uses[s2] = 0;
+    const int n_items = cta_items(T);
+    const int n_early = early && n_items > 0 ? early_fills<NT, AP>(T, tc_decode<AP>(T, cta_item(T, 0), 0, meta)) : 0;
+#pragma unroll
+    for (int s2 = 0; s2 < NT; ++s2)
+        if (s2 < n_early) uses[s2] = 1;  // fill s2 went to slot s2
+    f = (uint32_t)n_early;
     bool ok = true;
-    int j = 0;
-    for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
-        const TcItem it = tc_decode<AP>(T, item, j, meta);
+    for (int j = 0; j < n_items && ok; ++j) {
+        const TcItem it = tc_decode<AP>(T, cta_item(T, j), j, meta);
         if (it.n_tiles == 0) continue;
         const uint32_t qb = k % QB, quse = k / QB;
         auto load_q = [&]() -> bool {
@@ -382,7 +450,8 @@ __device__ __forceinline__ void tile_producer(const TcParams &T, const TcMaps &M
             if constexpr (AP) append_split(P, it.cr.qp, p, n_valid, a_m, a_n);
             const bool worker_full = AP && a_n > a_m;  // the append worker completes a mixed atom
             for (int kv = 0; kv < 2 && ok; ++kv) {
-                if (t == 0 && kv == 1) {
+                if (j == 0 && 2 * t + kv < n_early) continue;  // issued ahead of the loop
+                if (t == 0 && kv == 1 && !(j == 0 && n_early > 0)) {
                     if (lane == 0) ok = load_q();
                     if (coop) ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
                     if (!ok) break;
@@ -498,9 +567,9 @@ __device__ __forceinline__ void append_worker(const TcParams &T, const TcItem *m
     constexpr int U = 16;                       // pieces per lane in flight while storing
     const int t = (int)(threadIdx.x & 31);
     uint32_t f = 0, mixpar = 0;                 // fills seen; use parity of B_MIX per slot
-    int j = 0;
-    for (int item = blockIdx.x; item < T.items; item += gridDim.x, ++j) {
-        const TcItem it = tc_decode<true>(T, item, j, meta);
+    const int n_items = cta_items(T);
+    for (int j = 0; j < n_items; ++j) {
+        const TcItem it = tc_decode<true>(T, cta_item(T, j), j, meta);
         if (it.n_tiles == 0) continue;
         int ap_lo, ap_hi;
         append_range(P, it.cr, it.i0, (it.row0 + it.rows - 1) / P.G, ap_lo, ap_hi);
@@ -572,7 +641,7 @@ __device__ __forceinline__ void append_worker(const TcParams &T, const TcItem *m
         // with at most two items per CTA (latency-bound calls) the item's new
         // rows go to the cache here, overlapped with the attention; otherwise
         // the whole CTA stores them at the end (append_flush)
-        if (T.items > 2 * (int)gridDim.x || ap_lo >= ap_hi) continue;
+        if (n_items > 2 || ap_lo >= ap_hi) continue;
         const int half = (ap_hi - ap_lo) * PR, n = 2 * half;  // K then V
         for (int b0 = 0; b0 < n; b0 += 32 * U) {
             uint4 v[U];
@@ -624,13 +693,13 @@ __device__ __forceinline__ void append_flush(const TcParams &T, const TcItem *me
     constexpr int U = 8;
     const int tid = threadIdx.x;
     AppendChunk *tab = reinterpret_cast<AppendChunk *>(scratch);
-    const int n_items = (T.items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int n_items = cta_items(T);
     const int cap = scratch_bytes / (int)sizeof(AppendChunk) - 1;
     for (int k0 = 0; k0 < n_items; k0 += cap) {
         const int nk = min(cap, n_items - k0);
         for (int k = tid; k < nk; k += nthreads) {
             const int j = k0 + k;
-            const TcItem it = tc_decode<true>(T, (int)blockIdx.x + j * (int)gridDim.x, j, meta);
+            const TcItem it = tc_decode<true>(T, cta_item(T, j), j, meta);
             int lo, hi;
             append_range(P, it.cr, it.i0, (it.row0 + it.rows - 1) / P.G, lo, hi);
             const bool own = lo < hi;
@@ -746,22 +815,30 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
         fence_barrier_init();
     }
     // Q rows past an item's rows stay zero for the whole kernel (TMA writes
-    // only the first rows_per_tile rows of each slab).
-    for (int i = tid; i < QB * C::Q_BUF / 16; i += NTHR)
-        reinterpret_cast<uint4 *>(qs)[i] = make_uint4(0, 0, 0, 0);
+    // only the first rows_per_tile rows of each slab, and those are never
+    // zeroed, so the first Q copy may land before this block's barrier).
+    {
+        const int zr = (N - T.rows_per_tile) * 8;  // 16-byte pieces per slab
+        for (int i = tid; i < QB * SLABS * zr; i += NTHR) {
+            const int sl = i / zr, r = i - sl * zr;
+            reinterpret_cast<uint4 *>(qs + sl * C::Q_SLAB + T.rows_per_tile * 128)[r] =
+                make_uint4(0, 0, 0, 0);
+        }
+    }
     fence_proxy_async_smem();
+    for (int i = tid; i < kFillTab; i += NTHR) ftab[i] = 0xffffffffu;
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
+    __syncthreads();  // barriers and fill table ready for the early fills
     grid_dep_wait();
     grid_dep_trigger();
-    // metadata of this CTA's first items
-    for (int i = tid; i < kFillTab; i += NTHR) ftab[i] = 0xffffffffu;
-    for (int j = tid; j < kTcMetaItems; j += NTHR) {
-        const long long item = (long long)blockIdx.x + (long long)j * gridDim.x;
-        if (item < T.items) meta[j] = tc_decode_global<AP>(T, (int)item);
-    }
+    // the first item's first fills and Q rows go out before anything else,
+    // one warp each; then the metadata of this CTA's first items
+    if (lane == 0) issue_early_fills<C, NT, AP>(T, M, ftab, ring, qs, bars, warp);
+    for (int j = tid; j < kTcMetaItems; j += NTHR)
+        if (j < cta_items(T)) meta[j] = tc_decode_global<AP>(T, cta_item(T, j));
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
@@ -769,7 +846,7 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
 
     if (warp == 0) {
         // ======================================================= producer
-        tile_producer<C, NT, QB, AP>(T, M, meta, ftab, ring, qs, bars);
+        tile_producer<C, NT, QB, AP>(T, M, meta, ftab, ring, qs, bars, true);
     } else if (warp == 1) {
         // ============================================================ MMA
         // An event loop over two cursors on the same tile sequence: S = K Q^T
@@ -804,8 +881,10 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
                 return true;
             };
             // first tile of the next non-empty item at or after (item, j)
+            const int n_items = cta_items(T);
             auto seek = [&](Cursor &c) {
-                for (; c.item < T.items; c.item += gridDim.x, ++c.j) {
+                for (; c.j < n_items; ++c.j) {
+                    c.item = cta_item(T, c.j);
                     const TcItem it = tc_decode<AP>(T, c.item, c.j, meta);
                     if (it.n_tiles > 0) {
                         c.n_tiles = it.n_tiles;
@@ -823,11 +902,10 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
                 c.slot = -1;
                 if (++c.t < c.n_tiles) return;
                 ++c.k;
-                c.item += gridDim.x;
                 ++c.j;
                 seek(c);
             };
-            Cursor qc{(int)blockIdx.x, 0, 0, 0, 0, 0, 0u, 0u, false, -1, 0u};
+            Cursor qc{0, 0, 0, 0, 0, 0, 0u, 0u, false, -1, 0u};
             seek(qc);
             Cursor pc = qc;
             bool ok = true;
@@ -999,9 +1077,9 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
         const uint32_t p_chunk = (uint32_t)(lk & 63) >> 3;
         uint32_t g = 0, k = 0;
         bool ok = true;
-        int j = 0;
-        for (int item = blockIdx.x; item < T.items && ok; item += gridDim.x, ++j) {
-            const TcItem it = tc_decode<AP>(T, item, j, meta);
+        const int n_items = cta_items(T);
+        for (int j = 0; j < n_items && ok; ++j) {
+            const TcItem it = tc_decode<AP>(T, cta_item(T, j), j, meta);
             const size_t bh = (size_t)it.b * P.Hkv + it.h;
             const int my_rows = min(HN, it.rows - r0);  // rows of this group in the item
             if (it.n_tiles == 0) {
@@ -1315,7 +1393,7 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
     fence_after_sync();
     if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
     if constexpr (AP) {
-        if (T.items > 2 * (int)gridDim.x) append_flush<D>(T, meta, ring, NT * C::TILE_BYTES, NTHR);
+        if (cta_items(T) > 2) append_flush<D>(T, meta, ring, NT * C::TILE_BYTES, NTHR);
     }
 }
 

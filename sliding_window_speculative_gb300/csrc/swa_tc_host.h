@@ -17,6 +17,14 @@ struct TcParams {
     int rows_per_tile;    // packed rows per item (a multiple of G, <= N)
     int q_rows_per_tile;  // draft rows per item
     int items;            // splits * Hkv * row_tiles * B
+    // items_per_cta > 0: CTA c takes the contiguous block of items_per_cta (+1
+    // for c < items_extra) items starting at c * items_per_cta +
+    // min(c, items_extra); 0: CTA c takes items c, c + grid, c + 2 grid, ...
+    int items_per_cta, items_extra;
+    // fills of a CTA's first item issued ahead of the producer loop, at most
+    // (1 when the launch covers half the SMs or more: every CTA loading at
+    // once saturates HBM and the first K tile should land first)
+    int early_max;
 };
 
 // TMA tensor maps of one call.  The cache is viewed as rows of D bf16

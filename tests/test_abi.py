@@ -168,25 +168,47 @@ def test_debug_options_round_trip_and_validation(lib):
     """The test controls replace environment variables: the library reads
     none.  Defaults, a round trip, range checks and the reset."""
     assert swa.swa_get_debug_options() == {"force_kernel": 0, "pdl": 1, "wait_limit_cycles": 0,
-                                           "withhold_fill": -1, "reserved": 0}
+                                           "withhold_fill": -1, "rows_per_item": 0}
     swa.swa_set_debug_options(force_kernel="rows", pdl=0, wait_limit_cycles=100000,
-                              withhold_fill=3)
+                              withhold_fill=3, rows_per_item=64)
     try:
         assert swa.swa_get_debug_options() == {"force_kernel": 3, "pdl": 0,
                                                "wait_limit_cycles": 100000, "withhold_fill": 3,
-                                               "reserved": 0}
+                                               "rows_per_item": 64}
     finally:
         swa.swa_set_debug_options()
     assert swa.swa_get_debug_options()["force_kernel"] == 0
     for bad in ({"force_kernel": 4}, {"force_kernel": -1}, {"pdl": 2},
-                {"wait_limit_cycles": -5}, {"withhold_fill": -2}):
+                {"wait_limit_cycles": -5}, {"withhold_fill": -2}, {"rows_per_item": -1}):
         with pytest.raises(swa.SwaError) as e:
             swa.swa_set_debug_options(**bad)
         assert e.value.status == swa.SWA_ERR_INVALID_ARG
-    opt = swa.SwaDebugOptions(0, 1, 0, -1, 7)
-    assert lib.swa_set_debug_options(ctypes.byref(opt)) == swa.SWA_ERR_INVALID_ARG
     assert lib.swa_set_debug_options(None) == swa.SWA_OK
     assert lib.swa_get_debug_options(None) == swa.SWA_ERR_INVALID_ARG
+
+
+def test_rows_per_item_override(lib):
+    """The sweep override of rows per item: rounded to whole query groups,
+    capped per kernel, ignored for CUDA-core plans and forced splits."""
+    q64 = swa.make_dims(512, 64, 8, 2, 256, 32768)
+    assert swa.swa_plan(q64, 188, 152)["rows_per_tile"] == 128
+    try:
+        for want, got in ((64, 64), (32, 32), (30, 28), (3, 4), (500, 128)):
+            swa.swa_set_debug_options(force_kernel="rows", rows_per_item=want)
+            p = swa.swa_plan(q64, 188, 152)
+            assert p["kernel"] == 3 and p["rows_per_tile"] == got, (want, p)
+            assert p["row_tiles"] == -(-64 // (got // 4))
+        swa.swa_set_debug_options(rows_per_item=48)
+        q8 = swa.make_dims(64, 8, 8, 2, 256, 4096)
+        p = swa.swa_plan(q8, 188, 152)
+        assert p["kernel"] == 2 and p["rows_per_tile"] == 32      # all 32 rows, below the cap
+        swa.swa_set_debug_options(rows_per_item=16)
+        assert swa.swa_plan(q8, 188, 152)["rows_per_tile"] == 16
+        assert swa.swa_plan(swa.make_dims(64, 8, 8, 2, 256, 4096, 3), 188, 152)["rows_per_tile"] == 32
+        d64 = swa.make_dims(1, 8, 2, 1, 64, 40)
+        assert swa.swa_plan(d64, 16, 152)["kernel"] == 1
+    finally:
+        swa.swa_set_debug_options()
 
 
 def test_library_reads_no_environment():

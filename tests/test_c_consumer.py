@@ -73,7 +73,7 @@ int main(void) {
     F(swa_plan_info, merge); F(swa_plan_info, workspace_bytes);
     F(swa_debug_options, force_kernel); F(swa_debug_options, pdl);
     F(swa_debug_options, wait_limit_cycles); F(swa_debug_options, withhold_fill);
-    F(swa_debug_options, reserved);
+    F(swa_debug_options, rows_per_item);
     return 0;
 }
 """
