@@ -235,6 +235,16 @@ class Replicas:
                         out=self.out[r], lse=self.lse[r], num_splits=num_splits)
 
 
+def hold_stream(stream, us=500.0):
+    """Queue a sleep kernel of about `us` microseconds on `stream` ahead of
+    a timed region, so that the host has submitted the region's work before
+    the device reaches the start event: the events then bracket device
+    execution only, not the host's launch latency (the end-to-end timing
+    keeps its host costs on purpose and does not use this)."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(us * 2.1e3))  # cycles at up to 2.1 GHz
+
+
 def replica_count(case, bytes_per_call, steps, l2=None):
     """Input replicas that keep every timed call's reads out of L2.
 
@@ -259,7 +269,7 @@ def time_device(case, steps, warmup, num_splits=0, graph_len=1000, dist=None, ap
     """Device time of `steps` calls (graph replays), L2 defeated by replicas.
 
     With fewer timed calls than one cycle of replicas needs, every timed
-    call reads its own replica and a write of twice the L2 size runs between
+    call reads its own replica and a read of twice the L2 size runs between
     the graph's warm-up replay and the timed replay, so no timed call finds
     its inputs in L2.  Otherwise the graph cycles through replicas holding at
     least twice the L2 size, so between two uses of one replica the other
@@ -285,21 +295,23 @@ def time_device(case, steps, warmup, num_splits=0, graph_len=1000, dist=None, ap
     flush = None
     if distinct:
         timed = [capture(range(steps))]
-        flush = torch.empty(2 * l2, dtype=torch.uint8, device=case.q.device)
+        flush = torch.empty(2 * l2 // 8, dtype=torch.int64, device=case.q.device)
         scheme = (f"each timed call reads its own replica ({steps} of {nrep}); {2 * l2 >> 20} MiB "
-                  f"written between the warm-up and the timed replay")
+                  f"read between the warm-up and the timed replay (a read leaves no dirty lines "
+                  f"to write back during the timed calls)")
     else:
         g_len = nrep * max(1, min(graph_len, steps) // nrep) if nrep <= steps else steps
         full, rest = divmod(steps, g_len)
         timed = [capture(range(g_len))] * full + ([capture(range(rest))] if rest else [])
         scheme = (f"calls cycle through {nrep} replicas ({nrep * total >> 20} MiB per cycle)"
                   if nrep > 1 else "every call reads more than L2")
-    # warm the graphs themselves (first replays upload them), then flush L2
+    # warm the graphs themselves (first replays upload them), then push every
+    # replica out of L2 by reading a buffer twice its size
     with torch.cuda.stream(stream):
         for g in dict.fromkeys(timed):
             g.replay()
         if flush is not None:
-            flush.zero_()
+            flush.sum()
     stream.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -307,6 +319,7 @@ def time_device(case, steps, warmup, num_splits=0, graph_len=1000, dist=None, ap
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
+    hold_stream(stream)
     with torch.cuda.stream(stream):
         start.record(stream)
         for g in timed:
@@ -460,6 +473,7 @@ def time_paged(name, page_size, steps=50, warmup=5, seed=0):
     stream.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    hold_stream(stream)
     with torch.cuda.stream(stream):
         start.record(stream)
         graph.replay()
@@ -521,6 +535,7 @@ def time_accept(B, q_len, V, steps=2000, warmup=5, seed=0, graph_len=1000):
     reps = max(1, steps // n)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    hold_stream(stream)
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(reps):
@@ -660,6 +675,7 @@ def launch_floor(steps, graph_len=1000):
     reps = max(1, steps // n)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    hold_stream(stream)
     with torch.cuda.stream(stream):
         start.record(stream)
         for _ in range(reps):
@@ -816,7 +832,9 @@ def main():
                    "kv_bytes_per_call": kv, "bytes_per_call": total,
                    "l2": (f"defeated by {r['replicas']} input replicas: {r['l2_scheme']}"
                           if r["replicas"] > 1 else "inputs larger than L2"),
-                   "timing": "CUDA graph of calls, CUDA events on the launching stream",
+                   "timing": ("CUDA graph of calls, CUDA events on the launching stream; a "
+                              "sleep kernel ahead of the start event lets the host queue the "
+                              "replays first, so the events bracket device execution"),
                    "plan": plan, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "kernel": KERNEL_NAMES.get(plan["kernel"], "?") +
                      (" + swa_merge_kernel" if plan["merge"] else ""),
