@@ -210,7 +210,19 @@ const char *swa_last_error(void);
  * Bit 0: a K/V tile copy did not complete within the wait limit. */
 swa_status swa_read_device_errors(uint32_t *flags);
 
-/* Library version, e.g. "swa 0.1.0 sm_103a". */
+/* Out-of-range index attempts counted since the last read by a library built
+ * with SWA_DEBUG_CHECKS (libswa_debug.so): indices that come from device-side
+ * inputs, which the header states as preconditions and the kernels otherwise
+ * do not check: a block-table page outside [0, num_pages) (the kernel reads
+ * page 0 instead, and a fused append drops the store) and a sequence length
+ * outside [0, max_len] (clamped, as in every build).  Nothing traps.  Reading
+ * synchronises the device and clears the count.  A library built without the
+ * checks sets *count to 0 and returns SWA_ERR_UNSUPPORTED; NULL count:
+ * SWA_ERR_INVALID_ARG. */
+swa_status swa_read_debug_checks(uint32_t *count);
+
+/* Library version, e.g. "swa 0.1.0 sm_103a" ("... debug-checks" for the
+ * build with SWA_DEBUG_CHECKS). */
 const char *swa_version(void);
 
 /* Test and sweep controls.  Not for serving: every call uses the defaults
@@ -235,6 +247,12 @@ typedef struct {
                                   then rounded down to a multiple of Hq / Hkv (at least
                                   one); no effect on CUDA-core plans or when num_splits
                                   is forced */
+    int32_t fail_launch;       /* 0 (default); n > 0: the n-th kernel launch the library
+                                  makes from now on is not made and reports
+                                  cudaErrorLaunchOutOfResources to its call, which returns
+                                  SWA_ERR_CUDA (the test of the host's launch-error path);
+                                  the field then returns to 0 */
+    int32_t reserved;          /* must be 0 */
 } swa_debug_options;
 
 /* Set the controls above (NULL restores the defaults).  Returns

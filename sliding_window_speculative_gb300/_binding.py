@@ -12,6 +12,8 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libswa.so")
+# the same library built with SWA_DEBUG_CHECKS (load it first, in its own process)
+DEBUG_LIB_PATH = os.path.join(_HERE, "libswa_debug.so")
 
 SWA_OK = 0
 SWA_ERR_INVALID_ARG = 1
@@ -40,7 +42,8 @@ class SwaDebugOptions(ctypes.Structure):
     """swa_debug_options of include/swa.h (test and sweep controls)."""
     _fields_ = [("force_kernel", ctypes.c_int32), ("pdl", ctypes.c_int32),
                 ("wait_limit_cycles", ctypes.c_int64), ("withhold_fill", ctypes.c_int32),
-                ("rows_per_item", ctypes.c_int32)]
+                ("rows_per_item", ctypes.c_int32), ("fail_launch", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 # force_kernel values of swa_debug_options
@@ -81,6 +84,8 @@ def load_library(path=LIB_PATH):
     lib.swa_last_error.restype = ctypes.c_char_p
     lib.swa_read_device_errors.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
     lib.swa_read_device_errors.restype = ctypes.c_int
+    lib.swa_read_debug_checks.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    lib.swa_read_debug_checks.restype = ctypes.c_int
     lib.swa_version.argtypes = []
     lib.swa_version.restype = ctypes.c_char_p
     lib.swa_verify_attn_noalloc.argtypes = lib.swa_verify_attn.argtypes
@@ -426,20 +431,31 @@ def swa_read_device_errors():
     return flags.value
 
 
+def swa_read_debug_checks():
+    """Out-of-range index attempts counted since the last read (C entry point
+    swa_read_debug_checks; needs the SWA_DEBUG_CHECKS build, else SwaError
+    with SWA_ERR_UNSUPPORTED).  Synchronises the device."""
+    count = ctypes.c_uint32(0)
+    _check(load_library().swa_read_debug_checks(ctypes.byref(count)))
+    return count.value
+
+
 def swa_version():
     return load_library().swa_version().decode()
 
 
 def swa_set_debug_options(force_kernel=0, pdl=1, wait_limit_cycles=0, withhold_fill=-1,
-                          rows_per_item=0):
+                          rows_per_item=0, fail_launch=0):
     """Test and sweep controls of the C entry point swa_set_debug_options
     (not for serving).  force_kernel: 0 or "plan", 1 or "simt", 2 or "tc",
     3 or "rows"; pdl 1/0; wait_limit_cycles 0 (default ~2e9) or the bounded
     waits' limit; withhold_fill -1 or the fill the first CTA never copies;
-    rows_per_item 0 (the plan's) or packed rows per tensor-core work item."""
+    rows_per_item 0 (the plan's) or packed rows per tensor-core work item;
+    fail_launch 0 or n: the n-th library launch from now on is not made and
+    its call fails (then back to 0)."""
     fk = KERNEL_IDS[force_kernel] if isinstance(force_kernel, str) else int(force_kernel)
     opt = SwaDebugOptions(fk, int(pdl), int(wait_limit_cycles), int(withhold_fill),
-                          int(rows_per_item))
+                          int(rows_per_item), int(fail_launch), 0)
     _check(load_library().swa_set_debug_options(ctypes.byref(opt)))
 
 

@@ -15,8 +15,10 @@
 #include "swa_tc_host.h"
 
 // Fault word of each device that loads the library; kernels receive its
-// address and OR bits into it when a bounded wait gives up.
-__device__ uint32_t g_fault_word = 0;
+// address and OR bits into it when a bounded wait gives up.  The word after
+// it counts out-of-range index attempts in a library built with
+// SWA_DEBUG_CHECKS.
+__device__ uint32_t g_fault_word[2] = {0, 0};
 
 namespace {
 
@@ -95,6 +97,7 @@ std::atomic<int> g_opt_pdl{1};
 std::atomic<long long> g_opt_wait_limit{0};
 std::atomic<int> g_opt_withhold{-1};
 std::atomic<int> g_opt_rows{0};
+std::atomic<int> g_opt_fail_launch{0};
 
 // Kernel override of a test or sweep: 0 none, 1 CUDA-core, 2 key-major, 3 rows-major.
 int forced_kernel() { return g_opt_force.load(std::memory_order_relaxed); }
@@ -574,6 +577,7 @@ swa_status verify_impl(const void *q, const void *k_cache, const void *v_cache,
         P.block_table = paged->block_table;
         P.page_size = paged->page_size;
         P.max_blocks = paged->max_blocks;
+        P.num_pages = paged->num_pages;
         cache_rows = (long long)paged->num_pages * P.Hkv * paged->page_size;
     }
 
@@ -725,10 +729,28 @@ swa_status swa_read_device_errors(uint32_t *flags) {
     return SWA_OK;
 }
 
-const char *swa_version(void) { return "swa 0.1.0 sm_103a"; }
+swa_status swa_read_debug_checks(uint32_t *count) {
+    if (count == nullptr) return fail(SWA_ERR_INVALID_ARG, "count is NULL");
+    *count = 0;
+    if (!swa::kDebugChecks)
+        return fail(SWA_ERR_UNSUPPORTED, "the library was built without SWA_DEBUG_CHECKS");
+    uint32_t v = 0, zero = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+    e = cudaMemcpyFromSymbol(&v, g_fault_word, sizeof v, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "read debug-check count");
+    e = cudaMemcpyToSymbol(g_fault_word, &zero, sizeof zero, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "clear debug-check count");
+    *count = v;
+    return SWA_OK;
+}
+
+const char *swa_version(void) {
+    return swa::kDebugChecks ? "swa 0.1.0 sm_103a debug-checks" : "swa 0.1.0 sm_103a";
+}
 
 swa_status swa_set_debug_options(const swa_debug_options *opt) {
-    swa_debug_options d{0, 1, 0, -1, 0};
+    swa_debug_options d{0, 1, 0, -1, 0, 0, 0};
     if (opt != nullptr) d = *opt;
     if (d.force_kernel < 0 || d.force_kernel > 3)
         return fail(SWA_ERR_INVALID_ARG, "force_kernel %d outside [0, 3]", d.force_kernel);
@@ -740,11 +762,15 @@ swa_status swa_set_debug_options(const swa_debug_options *opt) {
         return fail(SWA_ERR_INVALID_ARG, "withhold_fill %d < -1", d.withhold_fill);
     if (d.rows_per_item < 0)
         return fail(SWA_ERR_INVALID_ARG, "rows_per_item %d < 0", d.rows_per_item);
+    if (d.fail_launch < 0)
+        return fail(SWA_ERR_INVALID_ARG, "fail_launch %d < 0", d.fail_launch);
+    if (d.reserved != 0) return fail(SWA_ERR_INVALID_ARG, "reserved %d is not 0", d.reserved);
     g_opt_force.store(d.force_kernel, std::memory_order_relaxed);
     g_opt_pdl.store(d.pdl, std::memory_order_relaxed);
     g_opt_wait_limit.store(d.wait_limit_cycles, std::memory_order_relaxed);
     g_opt_withhold.store(d.withhold_fill, std::memory_order_relaxed);
     g_opt_rows.store(d.rows_per_item, std::memory_order_relaxed);
+    g_opt_fail_launch.store(d.fail_launch, std::memory_order_relaxed);
     return SWA_OK;
 }
 
@@ -755,12 +781,22 @@ swa_status swa_get_debug_options(swa_debug_options *opt) {
     opt->wait_limit_cycles = g_opt_wait_limit.load(std::memory_order_relaxed);
     opt->withhold_fill = g_opt_withhold.load(std::memory_order_relaxed);
     opt->rows_per_item = g_opt_rows.load(std::memory_order_relaxed);
+    opt->fail_launch = g_opt_fail_launch.load(std::memory_order_relaxed);
+    opt->reserved = 0;
     return SWA_OK;
 }
 
 }  // extern "C"
 
 bool swa::pdl_enabled() { return g_opt_pdl.load(std::memory_order_relaxed) != 0; }
+
+bool swa::launch_fault_due() {
+    int n = g_opt_fail_launch.load(std::memory_order_relaxed);
+    while (n > 0)
+        if (g_opt_fail_launch.compare_exchange_weak(n, n - 1, std::memory_order_relaxed))
+            return n == 1;
+    return false;
+}
 
 // ------------------------------------------------ greedy verification
 

@@ -12,6 +12,22 @@ namespace swa {
 // reads it through swa_read_device_errors).
 constexpr uint32_t kFaultCopyTimeout = 1u;
 
+// A library built with SWA_DEBUG_CHECKS checks the indices that come from
+// device-side inputs (a block-table page outside the pool, a sequence length
+// outside [0, max_len]) and counts each out-of-range attempt in the word
+// after the fault word (swa_read_debug_checks), then keeps the access in
+// bounds (page 0 is read, a store is dropped).  Other builds compile the
+// checks away: those inputs are then the header's preconditions.
+#ifdef SWA_DEBUG_CHECKS
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
+__device__ __forceinline__ void debug_oob(uint32_t *fault) {
+    if constexpr (kDebugChecks) atomicAdd(fault + 1, 1u);
+}
+
 // Default limit of every bounded wait: ~1 s at the GB300 SM clock (a healthy
 // copy completes in microseconds).  Kernels take the limit as a parameter so
 // that a test can shorten it.

@@ -39,7 +39,7 @@ struct AttnParams {
     // paged cache (block_table non-null): k/v are [pages, Hkv, page_size, D]
     // and key position j of sequence b lives in page block_table[b][j / page_size]
     const int32_t *block_table;  // [B, max_blocks]
-    int page_size, max_blocks;
+    int page_size, max_blocks, num_pages;
     // fused append (k_new non-null): the q_len new rows [B, q_len, Hkv, D] of
     // every KV head, key positions q_pos + i, are attended from here and
     // stored to the cache; k / v then point at writable caches
@@ -69,6 +69,8 @@ struct ChunkRange {
 __device__ __forceinline__ ChunkRange chunk_range_of(const AttnParams &P, long long qp,
                                                      long long sl, int split) {
     ChunkRange c;
+    if constexpr (kDebugChecks)
+        if (sl < 0 || sl > P.L) debug_oob(P.fault);
     long long hi = qp + P.q_len;
     if (hi > sl) hi = sl;
     if (hi > P.L) hi = P.L;
@@ -101,11 +103,27 @@ __device__ __forceinline__ ChunkRange chunk_range(const AttnParams &P, int b, in
     return c;
 }
 
+// A block-table page, checked in SWA_DEBUG_CHECKS builds: one outside
+// [0, num_pages) is counted, `bad` set and page 0 used instead.
+__device__ __forceinline__ int checked_page(const AttnParams &P, int page, bool *bad) {
+    if constexpr (kDebugChecks) {
+        if (page < 0 || page >= P.num_pages) {
+            debug_oob(P.fault);
+            if (bad != nullptr) *bad = true;
+            return 0;
+        }
+    }
+    return page;
+}
+
 // Cache row (in rows of D elements) of key position j of (sequence b, KV
 // head h): contiguous [B, Hkv, L] or, with a block table, the page's row.
-__device__ __forceinline__ long long cache_row(const AttnParams &P, int b, int h, int j) {
+// `bad` (stores pass it) is set when a debug check replaced the page.
+__device__ __forceinline__ long long cache_row(const AttnParams &P, int b, int h, int j,
+                                               bool *bad = nullptr) {
     if (P.block_table == nullptr) return ((long long)b * P.Hkv + h) * P.L + j;
-    const int page = P.block_table[(long long)b * P.max_blocks + j / P.page_size];
+    const int page =
+        checked_page(P, P.block_table[(long long)b * P.max_blocks + j / P.page_size], bad);
     return ((long long)page * P.Hkv + h) * P.page_size + (j % P.page_size);
 }
 
@@ -325,7 +343,9 @@ __global__ void __launch_bounds__(kSimtThreads) swa_simt_kernel(const AttnParams
                 const int r = r0 + rest / PR, c = rest % PR;
                 const uint4 w = *reinterpret_cast<const uint4 *>((kv ? Vs : Ks) + (size_t)r * D + c * 8);
                 __nv_bfloat16 *cache = const_cast<__nv_bfloat16 *>(kv ? P.v : P.k);
-                *reinterpret_cast<uint4 *>(cache + cache_row(P, b, h, j0 + r) * D + c * 8) = w;
+                bool bad = false;
+                const long long row = cache_row(P, b, h, j0 + r, &bad);
+                if (!bad) *reinterpret_cast<uint4 *>(cache + row * D + c * 8) = w;
             }
         }
         const int kb0 = kg * C::KB;

@@ -317,7 +317,8 @@ __device__ __forceinline__ void tile_copies(const AttnParams &P, const TcMaps &M
     run = run < natoms - a ? run : natoms - a;
     int whole = full - a;
     whole = whole < 0 ? 0 : (whole > run ? run : whole);
-    const int pg = __ldg(P.block_table + (long long)b * P.max_blocks + k0 + lane);
+    const int pg = checked_page(P, __ldg(P.block_table + (long long)b * P.max_blocks + k0 + lane),
+                                nullptr);
     const int y = (pg * P.Hkv + h) * ps + (lane == 0 ? p % ps : 0);
     atom_run<AB>(m4, m1, y, whole, run > whole, dst + a * AB, bar, policy);
 }
@@ -662,9 +663,9 @@ __device__ __forceinline__ void append_worker(const TcParams &T, const TcItem *m
                 if (e < n) {
                     const int kv = e >= half, rest = e - kv * half;
                     __nv_bfloat16 *cache = const_cast<__nv_bfloat16 *>(kv ? P.v : P.k);
-                    *reinterpret_cast<uint4 *>(
-                        cache + cache_row(P, it.b, it.h, ap_lo + rest / PR) * D +
-                        (rest % PR) * 8) = v[u];
+                    bool bad = false;
+                    const long long row = cache_row(P, it.b, it.h, ap_lo + rest / PR, &bad);
+                    if (!bad) *reinterpret_cast<uint4 *>(cache + row * D + (rest % PR) * 8) = v[u];
                 }
             }
         }
@@ -733,7 +734,9 @@ __device__ __forceinline__ void append_flush(const TcParams &T, const TcItem *me
                     v[u] = __ldg(reinterpret_cast<const uint4 *>(
                         (kv ? P.v_new : P.k_new) +
                         (((long long)c.b * P.q_len + (pos - c.qp)) * P.Hkv + c.h) * D + pc * 8));
-                    dst[u] = ((cache_row(P, c.b, c.h, pos) * D + pc * 8) << 1) | kv;
+                    bool bad = false;
+                    const long long row = cache_row(P, c.b, c.h, pos, &bad);
+                    if (!bad) dst[u] = ((row * D + pc * 8) << 1) | kv;
                 }
             }
 #pragma unroll

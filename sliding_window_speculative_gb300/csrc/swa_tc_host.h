@@ -67,6 +67,10 @@ struct TcLaunch {
 // swa_set_debug_options (defined with the C ABI).
 bool pdl_enabled();
 
+// True when a test asked (swa_set_debug_options, fail_launch) that this
+// launch not be made; counts the launches down to it.
+bool launch_fault_due();
+
 template <typename... Params, typename... Args>
 cudaError_t launch_kernel(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
                           cudaStream_t stream, Args &&...args) {
@@ -80,6 +84,7 @@ cudaError_t launch_kernel(void (*kern)(Params...), dim3 grid, dim3 block, size_t
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl_enabled() ? 1 : 0;
+    if (launch_fault_due()) return cudaErrorLaunchOutOfResources;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 

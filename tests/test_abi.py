@@ -46,6 +46,25 @@ def test_binding_uses_the_c_names():
 
 def test_version(lib):
     assert "sm_103a" in swa.swa_version()
+    assert "debug-checks" not in swa.swa_version()
+
+
+def test_debug_checks_only_in_the_debug_build(lib):
+    """The release library answers swa_read_debug_checks with
+    SWA_ERR_UNSUPPORTED (no CUDA call); the SWA_DEBUG_CHECKS build exports
+    the same symbols and names itself in its version."""
+    c = ctypes.c_uint32(5)
+    assert lib.swa_read_debug_checks(ctypes.byref(c)) == swa.SWA_ERR_UNSUPPORTED and c.value == 0
+    assert "SWA_DEBUG_CHECKS" in swa.swa_last_error()
+    assert lib.swa_read_debug_checks(None) == swa.SWA_ERR_INVALID_ARG
+    dbg_path = build.build(debug_checks=True)
+    dbg = ctypes.CDLL(dbg_path)
+    for name in declared_functions():
+        assert hasattr(dbg, name), f"{name} not exported by the debug build"
+    dbg.swa_version.restype = ctypes.c_char_p
+    assert dbg.swa_version().decode() == "swa 0.1.0 sm_103a debug-checks"
+    dbg.swa_read_debug_checks.argtypes = [ctypes.c_void_p]
+    assert dbg.swa_read_debug_checks(None) == swa.SWA_ERR_INVALID_ARG
 
 
 def _call_raw(lib, dims, window=188, q=16, k=32, v=48, sl=64, qp=128, out=256, lse=None,
@@ -168,21 +187,28 @@ def test_debug_options_round_trip_and_validation(lib):
     """The test controls replace environment variables: the library reads
     none.  Defaults, a round trip, range checks and the reset."""
     assert swa.swa_get_debug_options() == {"force_kernel": 0, "pdl": 1, "wait_limit_cycles": 0,
-                                           "withhold_fill": -1, "rows_per_item": 0}
+                                           "withhold_fill": -1, "rows_per_item": 0,
+                                           "fail_launch": 0, "reserved": 0}
     swa.swa_set_debug_options(force_kernel="rows", pdl=0, wait_limit_cycles=100000,
-                              withhold_fill=3, rows_per_item=64)
+                              withhold_fill=3, rows_per_item=64, fail_launch=2)
     try:
         assert swa.swa_get_debug_options() == {"force_kernel": 3, "pdl": 0,
                                                "wait_limit_cycles": 100000, "withhold_fill": 3,
-                                               "rows_per_item": 64}
+                                               "rows_per_item": 64, "fail_launch": 2,
+                                               "reserved": 0}
     finally:
         swa.swa_set_debug_options()
     assert swa.swa_get_debug_options()["force_kernel"] == 0
+    assert swa.swa_get_debug_options()["fail_launch"] == 0
     for bad in ({"force_kernel": 4}, {"force_kernel": -1}, {"pdl": 2},
-                {"wait_limit_cycles": -5}, {"withhold_fill": -2}, {"rows_per_item": -1}):
+                {"wait_limit_cycles": -5}, {"withhold_fill": -2}, {"rows_per_item": -1},
+                {"fail_launch": -1}):
         with pytest.raises(swa.SwaError) as e:
             swa.swa_set_debug_options(**bad)
         assert e.value.status == swa.SWA_ERR_INVALID_ARG
+    # the reserved field must stay 0 (raw C call)
+    opt = swa._binding.SwaDebugOptions(0, 1, 0, -1, 0, 0, 7)
+    assert lib.swa_set_debug_options(ctypes.byref(opt)) == swa.SWA_ERR_INVALID_ARG
     assert lib.swa_set_debug_options(None) == swa.SWA_OK
     assert lib.swa_get_debug_options(None) == swa.SWA_ERR_INVALID_ARG
 

@@ -73,7 +73,8 @@ int main(void) {
     F(swa_plan_info, merge); F(swa_plan_info, workspace_bytes);
     F(swa_debug_options, force_kernel); F(swa_debug_options, pdl);
     F(swa_debug_options, wait_limit_cycles); F(swa_debug_options, withhold_fill);
-    F(swa_debug_options, rows_per_item);
+    F(swa_debug_options, rows_per_item); F(swa_debug_options, fail_launch);
+    F(swa_debug_options, reserved);
     return 0;
 }
 """
@@ -104,7 +105,7 @@ def test_binding_structs_match_the_c_layout(tmp_path):
             desc = getattr(mirrors[struct], field)
             assert (desc.offset, desc.size) == (int(parts[1]), int(parts[2])), line
         seen += 1
-    assert seen == 4 + 7 + 4 + 8 + 5
+    assert seen == 4 + 7 + 4 + 8 + 7
 
 
 def _prototypes():
