@@ -1197,15 +1197,21 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
                         tm[r4 + 3] = fmaxf(fmaxf(a0.w, a1.w), fmaxf(a2.w, a3.w));
                     }
                     float my_alpha = 1.f;
+                    if (!rescale) {
+                        // the item's first tile: its maxima are the references (the
+                        // row sums are still 0, so nothing is rescaled)
 #pragma unroll
-                    for (int r = 0; r < HN; ++r) {
-                        const float mo = mref[r];
-                        const float mn = fmaxf(mo, tm[r]);
-                        // (on the item's first tile the row sums are still 0)
-                        const float al = (t == 0 || mn == mo) ? 1.f : fast_exp2(mo - mn);
-                        if (gtid == r) my_alpha = al;
-                        lrow[r] *= al;
-                        mref[r] = mn;
+                        for (int r = 0; r < HN; ++r) mref[r] = fmaxf(mref[r], tm[r]);
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < HN; ++r) {
+                            const float mo = mref[r];
+                            const float mn = fmaxf(mo, tm[r]);
+                            const float al = mn == mo ? 1.f : fast_exp2(mo - mn);
+                            if (gtid == r) my_alpha = al;
+                            lrow[r] *= al;
+                            mref[r] = mn;
+                        }
                     }
                     if (rescale && gtid < HN) alpha_sm[r0 + gtid] = my_alpha;
                     if (rescale) {
