@@ -345,15 +345,9 @@ template <int D, int RPW, int NRG, bool AP>
 cudaError_t launch_simt_ap(const swa::AttnParams &P, cudaStream_t stream) {
     using C = swa::SimtCfg<D, RPW, NRG>;
     auto kern = swa::swa_simt_kernel<D, RPW, NRG, AP>;
-    static bool attr_done[kMaxDevices] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (!attr_done[dev]) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
+    static std::atomic<bool> attr_done[kMaxDevices];
+    cudaError_t e = swa::raise_smem_limit(kern, C::SMEM_BYTES, attr_done);
+    if (e != cudaSuccess) return e;
     dim3 grid(P.splits, P.Hkv * P.row_tiles, P.B);
     return swa::launch_kernel(kern, grid, dim3(swa::kSimtThreads), C::SMEM_BYTES, stream, P);
 }

@@ -49,15 +49,9 @@ cudaError_t launch_ap(const TcLaunch &L, const TcMaps &maps, cudaStream_t stream
     using Cf = Conf<D, N>;
     using C = typename Cf::C;
     auto kern = swa_tc_kernel<D, N, Cf::NT, Cf::QB, Cf::PB, Cf::OB, AP>;
-    static bool attr_done[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
+    static std::atomic<bool> attr_done[64];
+    cudaError_t e = raise_smem_limit(kern, C::SMEM_BYTES, attr_done);
+    if (e != cudaSuccess) return e;
     return launch_kernel(kern, dim3(L.grid), dim3(AP ? kTcThreads + 32 : kTcThreads),
                          C::SMEM_BYTES, stream, L.T, maps);
 }
@@ -83,15 +77,9 @@ cudaError_t launch_rows_ap(const TcLaunch &L, const TcMaps &maps, cudaStream_t s
     using Cf = RowsConf<D, QR>;
     using C = typename Cf::C;
     auto kern = swa_rows_kernel<D, QR, Cf::NT, Cf::QB, AP>;
-    static bool attr_done[64] = {};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && !attr_done[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             C::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_done[dev] = true;
-    }
+    static std::atomic<bool> attr_done[64];
+    cudaError_t e = raise_smem_limit(kern, C::SMEM_BYTES, attr_done);
+    if (e != cudaSuccess) return e;
     return launch_kernel(kern, dim3(L.grid), dim3(AP ? kRowsThreads + 32 : kRowsThreads),
                          C::SMEM_BYTES, stream, L.T, maps);
 }

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 
+#include <atomic>
 #include <utility>
 
 #include "swa_simt.cuh"
@@ -70,6 +71,22 @@ bool pdl_enabled();
 // True when a test asked (swa_set_debug_options, fail_launch) that this
 // launch not be made; counts the launches down to it.
 bool launch_fault_due();
+
+// A kernel's dynamic shared memory limit raised to `smem` on the current
+// device, once per device: `done` holds one flag per device (NDEV of them;
+// devices past that set the attribute on every call).  Calls racing on a
+// device's first launch may both set it, which is harmless.
+template <typename K, int NDEV>
+cudaError_t raise_smem_limit(K kern, int smem, std::atomic<bool> (&done)[NDEV]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool cached = dev >= 0 && dev < NDEV;
+    if (cached && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess && cached) done[dev].store(true, std::memory_order_release);
+    return e;
+}
 
 template <typename... Params, typename... Args>
 cudaError_t launch_kernel(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
