@@ -1,7 +1,6 @@
 """Shared test plumbing: the oracle on a workload's window slices, the
 tolerance check, a GPU-path runner and the kernel override."""
 import contextlib
-import math
 
 import torch
 
@@ -33,7 +32,3 @@ def forced_kernel(name):
         yield name
     finally:
         swa_set_debug_options()
-
-
-def ln_count(n):
-    return math.log(n)
