@@ -365,7 +365,8 @@ def time_e2e(case, steps, warmup, graph=False):
     three operations of a step are captured once as one CUDA graph and each
     step is one replay (the single-graph decode step of the pages,
     ONEGRAPH): the copies still run every step.  Timed with CUDA events
-    around all steps."""
+    around all steps, three times over; the median of the three is kept (a
+    host stall inside one short run moves its mean by tens of percent)."""
     from sliding_window_speculative_gb300 import prepare, swa_append_verify_attn
     B, q_len, Hq, D = case.q.shape
     Hkv = case.k_cache.shape[1]
@@ -409,18 +410,22 @@ def time_e2e(case, steps, warmup, graph=False):
             g.replay()
         stream.synchronize()
         run = g.replay
-    h_o.zero_()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(steps):
-            run()
-        end.record(stream)
-    torch.cuda.synchronize()
-    ms = start.elapsed_time(end)
+    runs = []
+    for _ in range(3):
+        h_o.zero_()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(steps):
+                run()
+            end.record(stream)
+        torch.cuda.synchronize()
+        runs.append(start.elapsed_time(end))
+    ms = sorted(runs)[1]
     return {"us_per_call": ms * 1e3 / steps, "h2d": h2d, "d2h": d2h, "steps": steps,
+            "runs_us": [round(r * 1e3 / steps, 3) for r in runs],
             "out": h_o.clone(), "lse": h_l.clone()}
 
 
@@ -428,8 +433,8 @@ def e2e_entry(case, steps, warmup, graph):
     kv, _ = workload_bytes(case)
     e = time_e2e(case, steps, warmup, graph=graph)
     return {"value": round(kv / (e["us_per_call"] * 1e-6) / 1e9, 3), "unit": UNIT,
-            "us_per_call": round(e["us_per_call"], 3), "h2d_bytes_per_step": e["h2d"],
-            "d2h_bytes_per_step": e["d2h"]}
+            "us_per_call": round(e["us_per_call"], 3), "runs_us": e["runs_us"],
+            "h2d_bytes_per_step": e["h2d"], "d2h_bytes_per_step": e["d2h"]}
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -865,7 +870,8 @@ def main():
         line["e2e"] = e2e_entry(case, n_e2e, args.warmup, graph=False)
         line["e2e"]["how"] = ("host loop per step: H2D copy of the packed inputs from pinned "
                               "memory, the prepared swa_append_verify_attn call, D2H copy of "
-                              "out and lse into pinned memory")
+                              "out and lse into pinned memory; the K steps timed three times, "
+                              "the median kept")
         # the same step captured once as one CUDA graph, replayed per step
         line["e2e"]["graph"] = e2e_entry(case, n_e2e, args.warmup, graph=True)
         if world == 1 and args.workload != "batched":
