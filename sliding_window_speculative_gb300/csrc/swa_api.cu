@@ -201,19 +201,23 @@ Plan make_plan_with(const swa_dims *d, int32_t window, int num_sms, int force) {
         p.chunk = (int)chunk;
         if (use_tc && !use_rows && d->num_splits == 0) {
             // Key-major kernel, key split fixed: cut the rows into smaller
-            // items while SMs would stay idle, so more SMs share each tile's
-            // softmax (the row tiles' extra K/V reads come from L2): 8 rows
-            // while all items fit in half the SMs, else 16 while they fit in
-            // the SMs.  Measured on GB300 (q8, 4:1 GQA, us): W188 one sequence
-            // 9.0 -> 7.5, 8 sequences 9.2 -> 8.0, 16: 9.3 -> 8.3, 32: 9.9 ->
-            // 9.2; W1024 one sequence 10.1 -> 9.0; W4096 one sequence 10.8 ->
-            // 10.6 (16 rows; 8 rows, with fewer key chunks, was 13.0).
+            // items while many SMs would stay idle, so more SMs share each
+            // tile's softmax (the row tiles' extra K/V reads come from L2): 8
+            // rows while the 8-row items fill at most a sixteenth of the SMs,
+            // else 16 while the 16-row items fill at most ~60% of them.
+            // Measured on GB300 (q8, 4:1 GQA, us, rows 8 / 16 / 32): W188 one
+            // sequence 7.21 / 7.38 / 8.66, 2 sequences 7.50 / 7.33 / 8.66, 8:
+            // 7.90 / 7.70 / 8.87, 16: 9.77 / 8.07 / 8.95, 24: 13.99 / 10.01 /
+            // 9.21, 32: 14.78 / 10.34 / 9.62; W512 4 sequences 13.07 / 9.71 /
+            // 10.33; W1024 one sequence 9.40 / 9.14 / 9.87, 4: 14.48 / 11.29 /
+            // 10.66; W4096 one sequence 15.5 / 10.48 / 10.34.
             const long long per_unit = (long long)d->batch * d->num_kv_heads * splits;
             for (int r : {8, 16}) {
                 const int rows = r < G ? G : (r / G) * G;
                 if (rows >= p.rows_per_tile) break;
                 const long long rt = ceil_div(d->q_len, rows / G);
-                if (per_unit * rt * (r == 8 ? 2 : 1) <= num_sms) {
+                const long long n = per_unit * rt;
+                if (r == 8 ? n * 16 <= num_sms : n * 5 <= 3LL * num_sms) {
                     p.rows_per_tile = rows;
                     p.q_rows_per_tile = rows / G;
                     p.row_tiles = (int)rt;

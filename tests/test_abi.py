@@ -340,8 +340,10 @@ def test_plan_prefill_chunk_reads_row_windows(lib):
 
 def test_plan_few_units_prefer_small_key_major_items(lib):
     # few (sequence, KV head) units: the key-major kernel with 8- or 16-row
-    # items, even above 32 packed rows; full batches keep the rows-major kernel
-    for B, q_len, rows in ((1, 8, 8), (1, 16, 8), (1, 64, 8), (8, 16, 16), (16, 8, 16)):
+    # items, even above 32 packed rows (8 rows only while those items fill at
+    # most a sixteenth of the SMs); full batches keep the rows-major kernel
+    for B, q_len, rows in ((1, 8, 8), (1, 16, 16), (1, 64, 16), (2, 8, 16), (8, 16, 16),
+                           (16, 8, 16), (24, 8, 32)):
         p = swa.swa_plan(swa.make_dims(B, q_len, 8, 2, 256, 4096), 188, 152)
         assert p["kernel"] == 2 and p["rows_per_tile"] == rows, (B, q_len, p)
         assert p["grid_ctas"] <= 152
