@@ -285,16 +285,20 @@ Plan make_plan_with(const swa_dims *d, int32_t window, int num_sms, int force) {
 }
 
 // The plan of a call.  More than 32 packed rows go to the rows-major kernel
-// unless the call leaves so many SMs idle that the key-major kernel cuts its
-// rows into 8- or 16-row items: then the key-major plan is taken (measured on
-// GB300, W188: one sequence q16 11.5 -> 7.8 us, q64 12.5 -> 7.9 us; eight
-// sequences q16 11.7 -> 8.2 us).
+// unless the key-major kernel's items (up to 64 rows each) fit in one wave of
+// its persistent CTAs, one item per SM, or it cuts its rows into 8- or
+// 16-row items: then the key-major plan is taken.  Measured on GB300, W188,
+// us, rows-major / key-major: q16 one sequence 11.5 / 7.3, 8 sequences 12.1 /
+// 8.0, 16: 12.4 / 11.9, 64: 14.9 / 13.7, 128 (256 key-major items): 23.0 /
+// 22.8; q32 8 sequences 13.3 / 12.0, 32: 14.7 / 14.0, 64 (256 items): 17.4 /
+// 23.4; q64 4 sequences 13.3 / 11.8, 16: 14.4 / 13.8, 32 (256 items): 16.6 /
+// 22.7; a 512-token prefill chunk of one sequence 13.6 / 12.1.
 Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
     const int force = forced_kernel();
     Plan p = make_plan_with(d, window, num_sms, force);
     if (force == 0 && p.kernel == 3) {
         const Plan k = make_plan_with(d, window, num_sms, 2);
-        if (k.kernel == 2 && k.rows_per_tile <= 16) return k;
+        if (k.kernel == 2 && (k.rows_per_tile <= 16 || k.items <= (long long)num_sms)) return k;
     }
     return p;
 }

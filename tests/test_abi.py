@@ -138,9 +138,10 @@ def test_plan_invariants(lib, B, q_len, Hq, Hkv, D, L, W, sms):
         assert p["grid_ctas"] == units
     else:                                   # persistent grid over the work items
         assert p["kernel"] in (2, 3) and 1 <= p["grid_ctas"] <= min(units, sms)
-        # rows-major above 32 packed rows, unless few units take small
-        # key-major items
-        assert p["kernel"] == (3 if R > 32 else 2) or (p["kernel"] == 2 and p["rows_per_tile"] <= 16)
+        # rows-major above 32 packed rows, unless the key-major items fit in
+        # one wave of the SMs or are small (8 or 16 rows)
+        assert p["kernel"] == (3 if R > 32 else 2) or (
+            p["kernel"] == 2 and (p["rows_per_tile"] <= 16 or units <= sms))
         assert p["rows_per_tile"] <= (128 if p["kernel"] == 3 else 64)
         assert p["rows_per_tile"] % (Hq // Hkv) == 0
     assert p["merge"] == (1 if p["num_splits"] > 1 else 0)
@@ -162,8 +163,10 @@ def test_plan_kernel_choice(lib):
     assert swa.swa_plan(d64, 16, 152)["kernel"] == 1            # head_dim 64: CUDA cores
     q64 = swa.swa_plan(swa.make_dims(512, 64, 8, 2, 256, 32768), 1024, 152)
     assert q64["kernel"] == 3 and q64["row_tiles"] == 2 and q64["rows_per_tile"] == 128
-    q16 = swa.swa_plan(swa.make_dims(64, 16, 8, 2, 256, 4096), 188, 152)
+    q16 = swa.swa_plan(swa.make_dims(128, 16, 8, 2, 256, 4096), 188, 152)
     assert q16["kernel"] == 3 and q16["row_tiles"] == 1 and q16["rows_per_tile"] == 64
+    q16 = swa.swa_plan(swa.make_dims(64, 16, 8, 2, 256, 4096), 188, 152)   # one wave
+    assert q16["kernel"] == 2 and q16["row_tiles"] == 1 and q16["rows_per_tile"] == 64
     with forced_kernel("simt"):
         assert swa.swa_plan(q8, 188, 152)["kernel"] == 1
     with forced_kernel("tc"):
@@ -329,11 +332,15 @@ def test_paged_verify_rejects_bad_tables(lib):
 
 
 def test_plan_prefill_chunk_reads_row_windows(lib):
-    # a 512-row prefill chunk at W = 188: a row tile's rows see W + 31 keys,
-    # so no split although the whole span is 699 keys; at W = 4096 the row
-    # tiles' windows (4127 keys) are split to reach the SMs
+    # a 512-row prefill chunk at W = 188: a row tile's rows see W + 15 keys
+    # (key-major, 64-row items: 16 draft rows each, one wave of the SMs) or
+    # W + 31 (rows-major, 128 rows), so no split although the whole span is
+    # 699 keys; at W = 4096 the row tiles' windows are split to reach the SMs
     p = swa.swa_plan(swa.make_dims(1, 512, 8, 2, 256, 4096), 188, 152)
-    assert p["kernel"] == 3 and p["row_tiles"] == 16 and p["num_splits"] == 1
+    assert p["kernel"] == 2 and p["row_tiles"] == 32 and p["num_splits"] == 1
+    with forced_kernel("rows"):
+        p = swa.swa_plan(swa.make_dims(1, 512, 8, 2, 256, 4096), 188, 152)
+        assert p["kernel"] == 3 and p["row_tiles"] == 16 and p["num_splits"] == 1
     p = swa.swa_plan(swa.make_dims(1, 512, 8, 2, 128, 8192), 4096, 152)
     assert p["num_splits"] > 1 and p["chunk_keys"] < 4096 + 31
 
@@ -347,7 +354,12 @@ def test_plan_few_units_prefer_small_key_major_items(lib):
         p = swa.swa_plan(swa.make_dims(B, q_len, 8, 2, 256, 4096), 188, 152)
         assert p["kernel"] == 2 and p["rows_per_tile"] == rows, (B, q_len, p)
         assert p["grid_ctas"] <= 152
-    for B, q_len in ((512, 16), (512, 64), (64, 16), (1, 512)):
+    # more than 32 rows: the key-major kernel while its items (up to 64 rows)
+    # fit in one wave of the SMs, else the rows-major kernel
+    for B, q_len in ((16, 16), (64, 16), (8, 32), (32, 32), (4, 64), (16, 64), (1, 512)):
+        p = swa.swa_plan(swa.make_dims(B, q_len, 8, 2, 256, 4096), 188, 152)
+        assert p["kernel"] == 2 and p["grid_ctas"] <= 152, (B, q_len, p)
+    for B, q_len in ((512, 16), (512, 64), (128, 16), (64, 32), (32, 64), (64, 512)):
         p = swa.swa_plan(swa.make_dims(B, q_len, 8, 2, 256, 4096), 188, 152)
         assert p["kernel"] == 3, (B, q_len, p)
     p = swa.swa_plan(swa.make_dims(64, 8, 8, 2, 256, 4096), 188, 152)
