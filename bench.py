@@ -55,7 +55,7 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-KERNEL_NAMES = {1: "swa_simt_kernel", 2: "swa_tc_kernel", 3: "swa_rows_kernel"}
+KERNEL_NAMES = {1: "swa_simt_kernel", 2: "swa_tc_kernel", 3: "swa_rows_kernel", 4: "swa_pair_kernel"}
 METRIC = "verify-attn µs/call and KV GB/s (% of GB300 HBM peak) at W=188, q_len=8"
 UNIT = "GB/s"
 

@@ -188,11 +188,14 @@ swa_status swa_release_workspace(void);
  * SMs (pure host arithmetic, no CUDA call). */
 typedef struct {
     int32_t kernel;        /* 1 = CUDA-core (SIMT) chunk kernel, 2 = key-major tensor-core
-                              (tcgen05) kernel, 3 = rows-major tensor-core kernel */
+                              (tcgen05) kernel, 3 = rows-major tensor-core kernel, 4 = the
+                              rows-major kernel on CTA pairs (clusters of two CTAs, 2 x 128
+                              packed rows per item; swa_verify_attn only: a paged or fused-
+                              append call with these dims takes kernel 3 instead) */
     int32_t num_splits;    /* chunks per (sequence, KV head)                    */
     int32_t chunk_keys;    /* keys per chunk                                    */
-    int32_t row_tiles;     /* CTAs along the packed rows R = q_len * G          */
-    int32_t rows_per_tile; /* packed rows per CTA                               */
+    int32_t row_tiles;     /* work items along the packed rows R = q_len * G    */
+    int32_t rows_per_tile; /* packed rows per work item (kernel 4: two CTAs')   */
     int32_t grid_ctas;     /* CTAs of the attention kernel                      */
     int32_t merge;         /* 0 none, 1 separate log-sum-exp merge kernel       */
     int64_t workspace_bytes; /* global scratch this plan uses                   */
@@ -231,8 +234,10 @@ const char *swa_version(void);
  * no environment variable. */
 typedef struct {
     int32_t force_kernel;      /* 0 (default): the plan's kernel; 1 CUDA-core, 2 key-major
-                                  tensor-core, 3 rows-major tensor-core (a shape the forced
-                                  kernel does not take runs the plan's kernel) */
+                                  tensor-core, 3 rows-major tensor-core, 4 rows-major on CTA
+                                  pairs (a shape the forced kernel does not take runs the
+                                  plan's kernel; 4 falls back to 3 off head_dim 256, on a
+                                  paged cache and under a fused append) */
     int32_t pdl;               /* 1 (default): launches with programmatic dependent launch;
                                   0: plain stream-ordered launches */
     int64_t wait_limit_cycles; /* 0 (default): every bounded wait inside the kernels gives up

@@ -47,7 +47,7 @@ class SwaDebugOptions(ctypes.Structure):
 
 
 # force_kernel values of swa_debug_options
-KERNEL_IDS = {"plan": 0, "simt": 1, "tc": 2, "rows": 3}
+KERNEL_IDS = {"plan": 0, "simt": 1, "tc": 2, "rows": 3, "pairs": 4}
 
 
 class SwaError(RuntimeError):
@@ -448,7 +448,7 @@ def swa_set_debug_options(force_kernel=0, pdl=1, wait_limit_cycles=0, withhold_f
                           rows_per_item=0, fail_launch=0):
     """Test and sweep controls of the C entry point swa_set_debug_options
     (not for serving).  force_kernel: 0 or "plan", 1 or "simt", 2 or "tc",
-    3 or "rows"; pdl 1/0; wait_limit_cycles 0 (default ~2e9) or the bounded
+    3 or "rows", 4 or "pairs"; pdl 1/0; wait_limit_cycles 0 (default ~2e9) or the bounded
     waits' limit; withhold_fill -1 or the fill the first CTA never copies;
     rows_per_item 0 (the plan's) or packed rows per tensor-core work item;
     fail_launch 0 or n: the n-th library launch from now on is not made and

@@ -76,7 +76,8 @@ swa_status validate_dims(const swa_dims *d, int32_t window) {
 }
 
 struct Plan {
-    int kernel;       // 1 = CUDA-core (SIMT) chunk kernel, 2 = tensor-core kernel
+    int kernel;       // 1 = CUDA-core (SIMT) chunk kernel, 2 = key-major tensor-core kernel,
+                      // 3 = rows-major tensor-core kernel, 4 = its CTA-pair form
     int rpw, nrg;     // SIMT row layout
     int rows_per_tile, row_tiles;
     int q_rows_per_tile;  // tensor-core path: draft rows per item
@@ -99,7 +100,8 @@ std::atomic<int> g_opt_withhold{-1};
 std::atomic<int> g_opt_rows{0};
 std::atomic<int> g_opt_fail_launch{0};
 
-// Kernel override of a test or sweep: 0 none, 1 CUDA-core, 2 key-major, 3 rows-major.
+// Kernel override of a test or sweep: 0 none, 1 CUDA-core, 2 key-major, 3 rows-major,
+// 4 rows-major on CTA pairs.
 int forced_kernel() { return g_opt_force.load(std::memory_order_relaxed); }
 
 // Split heuristic.  Host-only: seq_lens live on the device, so the
@@ -116,7 +118,7 @@ int forced_kernel() { return g_opt_force.load(std::memory_order_relaxed); }
 //  - CUDA-core path: enough CTAs to cover every SM about twice, chunks of at
 //    least one 32-key tile.
 // Chunks are multiples of 16 keys; at most kMaxSplits chunks.
-Plan make_plan_with(const swa_dims *d, int32_t window, int num_sms, int force) {
+Plan make_plan_with(const swa_dims *d, int32_t window, int num_sms, int force, bool pairs_ok) {
     Plan p{};
     p.sms = num_sms;
     const int G = d->num_q_heads / d->num_kv_heads;
@@ -143,8 +145,19 @@ Plan make_plan_with(const swa_dims *d, int32_t window, int num_sms, int force) {
     // kernel: its softmax keeps a row in one thread pair and P in TMEM, and
     // an item holds up to 128 rows, so K/V are re-read less often; up to 32
     // rows the key-major kernel's eight warps share the work better.
-    const bool use_rows = tc_shape && (force == 3 || (force == 0 && R > 32));
-    if (use_rows) {
+    const bool use_rows = tc_shape && (force == 3 || force == 4 || (force == 0 && R > 32));
+    // More than 128 packed rows (two or more row tiles of a (sequence, KV
+    // head)) at head_dim 256 over a contiguous cache: the rows-major kernel on
+    // CTA pairs, 2 x 128 rows per item, each K/V byte read once per item.
+    const bool use_pairs = use_rows && pairs_ok && D == 256 && (force == 4 || (force == 0 && R > 128));
+    if (use_pairs) {
+        p.kernel = 4;
+        const int cta_rows = (128 / G) * G;
+        p.rows_per_tile = 2 * cta_rows;
+        p.q_rows_per_tile = 2 * (128 / G);
+        p.row_tiles = ceil_div(d->q_len, p.q_rows_per_tile);
+        p.tc_n = 128;
+    } else if (use_rows) {
         // rows-major kernel: up to 128 packed rows per item (the MMA's M)
         p.kernel = 3;
         const int max_rows = 128;
@@ -164,8 +177,9 @@ Plan make_plan_with(const swa_dims *d, int32_t window, int num_sms, int force) {
         p.tc_n = p.rows_per_tile <= 16 ? 16 : p.rows_per_tile <= 32 ? 32 : 64;
     }
     if (use_rows || use_tc) {
-        const int ctas_per_sm = 1;  // both tensor-core kernels: one persistent CTA per SM
-        const long long units = (long long)d->batch * d->num_kv_heads * p.row_tiles;
+        const int ctas_per_sm = 1;  // the tensor-core kernels: one persistent CTA per SM
+        const int unit_ctas = use_pairs ? 2 : 1;  // CTAs that work on one item at once
+        const long long units = (long long)d->batch * d->num_kv_heads * p.row_tiles * unit_ctas;
         long long item_span = (long long)window + p.q_rows_per_tile - 1;
         if (item_span > span) item_span = span;
         long long chunk;
@@ -227,7 +241,7 @@ Plan make_plan_with(const swa_dims *d, int32_t window, int num_sms, int force) {
             }
         }
         const int force_rows = g_opt_rows.load(std::memory_order_relaxed);
-        if (force_rows > 0 && d->num_splits == 0) {
+        if (force_rows > 0 && d->num_splits == 0 && !use_pairs) {
             // a sweep's override of the rows per item
             const int max_rows = use_rows ? 128 : 64;
             int rows = force_rows < max_rows ? force_rows : max_rows;
@@ -242,8 +256,9 @@ Plan make_plan_with(const swa_dims *d, int32_t window, int num_sms, int force) {
             }
         }
         p.items = (long long)splits * d->batch * d->num_kv_heads * p.row_tiles;
-        const long long slots = (long long)num_sms * ctas_per_sm;
-        p.grid = p.items < slots ? p.items : slots;
+        long long slots = (long long)num_sms * ctas_per_sm / unit_ctas;
+        if (slots < 1) slots = 1;
+        p.grid = (p.items < slots ? p.items : slots) * unit_ctas;
     } else {
         p.kernel = 1;
         if (R <= 4) { p.rpw = 4; p.nrg = 1; }
@@ -293,11 +308,11 @@ Plan make_plan_with(const swa_dims *d, int32_t window, int num_sms, int force) {
 // 22.8; q32 8 sequences 13.3 / 12.0, 32: 14.7 / 14.0, 64 (256 items): 17.4 /
 // 23.4; q64 4 sequences 13.3 / 11.8, 16: 14.4 / 13.8, 32 (256 items): 16.6 /
 // 22.7; a 512-token prefill chunk of one sequence 13.6 / 12.1.
-Plan make_plan(const swa_dims *d, int32_t window, int num_sms) {
+Plan make_plan(const swa_dims *d, int32_t window, int num_sms, bool pairs_ok) {
     const int force = forced_kernel();
-    Plan p = make_plan_with(d, window, num_sms, force);
-    if (force == 0 && p.kernel == 3) {
-        const Plan k = make_plan_with(d, window, num_sms, 2);
+    Plan p = make_plan_with(d, window, num_sms, force, pairs_ok);
+    if (force == 0 && p.kernel >= 3) {
+        const Plan k = make_plan_with(d, window, num_sms, 2, pairs_ok);
         if (k.kernel == 2 && (k.rows_per_tile <= 16 || k.items <= (long long)num_sms)) return k;
     }
     return p;
@@ -407,7 +422,13 @@ swa_status launch_plan(const Plan &pl, const swa_dims *dims, const swa::AttnPara
         L.T.early_max = pl.grid * 2 >= pl.sms ? 1 : 8;
         L.D = dims->head_dim;
         L.N = pl.tc_n;
-        L.rows_major = pl.kernel == 3;
+        L.rows_major = pl.kernel >= 3;
+        L.pairs = pl.kernel == 4;
+        if (L.pairs) {
+            // the kernel takes one CTA's share of an item's rows
+            L.T.rows_per_tile = pl.rows_per_tile / 2;
+            L.T.q_rows_per_tile = pl.q_rows_per_tile / 2;
+        }
         L.grid = (int)pl.grid;
         L.cache_rows = cache_rows >= 0 ? cache_rows : (long long)P.B * P.Hkv * P.L;
         L.q = q;
@@ -546,7 +567,8 @@ swa_status verify_impl(const void *q, const void *k_cache, const void *v_cache,
 
     uint32_t *fault = fault_word_ptr(dev);
     if (fault == nullptr) return fail(SWA_ERR_CUDA, "cannot resolve the device fault word");
-    const Plan pl = make_plan(dims, window, device_sms(dev));
+    // the CTA-pair kernel reads a contiguous cache without a fused append
+    const Plan pl = make_plan(dims, window, device_sms(dev), paged == nullptr && k_new == nullptr);
     swa::AttnParams P{};
     P.q = static_cast<const __nv_bfloat16 *>(q);
     P.k = static_cast<const __nv_bfloat16 *>(k_cache);
@@ -704,7 +726,7 @@ swa_status swa_plan(const swa_dims *dims, int32_t window, int32_t num_sms, swa_p
     if (st != SWA_OK) return st;
     if (plan == nullptr) return fail(SWA_ERR_INVALID_ARG, "plan is NULL");
     if (num_sms < 1) return fail(SWA_ERR_INVALID_ARG, "num_sms %d < 1", num_sms);
-    const Plan p = make_plan(dims, window, num_sms);
+    const Plan p = make_plan(dims, window, num_sms, true);
     plan->kernel = p.kernel;
     plan->num_splits = p.splits;
     plan->chunk_keys = p.chunk;
@@ -754,8 +776,8 @@ const char *swa_version(void) {
 swa_status swa_set_debug_options(const swa_debug_options *opt) {
     swa_debug_options d{0, 1, 0, -1, 0, 0, 0};
     if (opt != nullptr) d = *opt;
-    if (d.force_kernel < 0 || d.force_kernel > 3)
-        return fail(SWA_ERR_INVALID_ARG, "force_kernel %d outside [0, 3]", d.force_kernel);
+    if (d.force_kernel < 0 || d.force_kernel > 4)
+        return fail(SWA_ERR_INVALID_ARG, "force_kernel %d outside [0, 4]", d.force_kernel);
     if (d.pdl != 0 && d.pdl != 1) return fail(SWA_ERR_INVALID_ARG, "pdl %d is not 0 or 1", d.pdl);
     if (d.wait_limit_cycles < 0)
         return fail(SWA_ERR_INVALID_ARG, "wait_limit_cycles %lld < 0",

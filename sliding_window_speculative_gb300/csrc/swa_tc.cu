@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <mutex>
 
+#include "swa_pair.cuh"
 #include "swa_rows.cuh"
 #include "swa_tc.cuh"
 #include "swa_tc_host.h"
@@ -98,6 +99,48 @@ cudaError_t launch_rows_d(const TcLaunch &L, const TcMaps &maps, cudaStream_t s)
         case 128: return launch_rows<D, 128>(L, maps, s);
         default: return cudaErrorInvalidConfiguration;
     }
+}
+
+// CTA-pair kernel: clusters of two CTAs, as many pairs as the plan's grid
+// holds and the device runs at once (queried once per device).
+template <int D>
+cudaError_t launch_pairs(const TcLaunch &L, const TcMaps &maps, const PairMaps &pm,
+                         cudaStream_t stream) {
+    using C = PairCfg<D, kPairSlots>;
+    auto kern = swa_pair_kernel<D, kPairSlots>;
+    static std::atomic<bool> attr_done[64];
+    static std::atomic<int> max_pairs[64];
+    cudaError_t e = raise_smem_limit(kern, C::SMEM_BYTES, attr_done);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.blockDim = dim3(kPairThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int fit = dev >= 0 && dev < 64 ? max_pairs[dev].load(std::memory_order_acquire) : 0;
+    if (fit == 0) {
+        cfg.gridDim = dim3((unsigned)L.grid);
+        cfg.numAttrs = 1;
+        e = cudaOccupancyMaxActiveClusters(&fit, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (fit < 1) return cudaErrorInvalidConfiguration;
+        if (dev >= 0 && dev < 64) max_pairs[dev].store(fit, std::memory_order_release);
+    }
+    const int pairs = L.grid / 2 < fit ? L.grid / 2 : fit;
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    cfg.numAttrs = pdl_enabled() ? 2 : 1;
+    if (launch_fault_due()) return cudaErrorLaunchOutOfResources;
+    return cudaLaunchKernelEx(&cfg, kern, L.T, maps, pm);
 }
 
 template <int D>
@@ -211,6 +254,32 @@ cudaError_t tc_launch(const TcLaunch &L, cudaStream_t stream, char *err, size_t 
                 return cudaErrorInvalidValue;
             }
         }
+    }
+    if (L.pairs) {
+        // V as D / 2 head dims per CTA: boxes of half the slabs, otherwise as
+        // the full maps above
+        if (D != 256 || L.grid < 2) return cudaErrorInvalidConfiguration;
+        PairMaps pm{};
+        for (int bi = 0; bi < 5; ++bi) {
+            const bool atom = bi == 4;
+            const cuuint32_t A = atom ? 1u : (16u >> bi);
+            cuuint64_t dims[4] = {64, rows, slabs, 16};
+            cuuint64_t strides[3] = {(cuuint64_t)D * 2, 128, (cuuint64_t)D * 2 * 8};
+            cuuint32_t box[4] = {64, 8, slabs / 2, A};
+            cuuint32_t es[4] = {1, 1, 1, 1};
+            CUresult r = g_encode(atom ? &pm.vh_atom : &pm.vh_atoms[bi],
+                                  CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, atom ? 3 : 4,
+                                  const_cast<void *>(L.v), dims, strides, box, es,
+                                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) {
+                snprintf(err, errlen, "cuTensorMapEncodeTiled(V cache halves, %u-atom box) failed: %d",
+                         (unsigned)A, (int)r);
+                return cudaErrorInvalidValue;
+            }
+        }
+        return launch_pairs<256>(L, maps, pm, stream);
     }
     if (L.rows_major) {
         if (D == 256) return launch_rows_d<256>(L, maps, stream);

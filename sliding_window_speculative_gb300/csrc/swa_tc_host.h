@@ -55,6 +55,10 @@ struct TcConfInfo {
 struct TcLaunch {
     TcParams T;
     int rows_major;  // 1: the kernel with packed rows as the MMA's M (swa_rows_kernel)
+    // 1 (with rows_major): the CTA-pair kernel (swa_pair_kernel), clusters of
+    // two CTAs; T.rows_per_tile / T.q_rows_per_tile are one CTA's rows, an
+    // item holds twice that, and grid counts CTAs (two per item at once)
+    int pairs;
     int D, N;   // head_dim, padded rows per item (rows kernel: 32, 64 or 128)
     int grid;   // persistent CTAs
     long long cache_rows;  // rows of D elements in each of the K and V tensors

@@ -220,6 +220,142 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ------------------------------------------------------ CTA pairs (2-CTA MMA)
+//
+// A cluster of two CTAs on two SMs shares one MMA of M = 256 rows: the even
+// CTA (rank 0) issues it, A's rows 0..127 come from rank 0's shared memory
+// or TMEM and rows 128..255 from rank 1's, B's columns are split in halves
+// the same way (N/2 from each CTA, both at the same shared-memory offset),
+// and each CTA's TMEM receives the D rows of its own A rows.  Every tcgen05
+// instruction of such a kernel takes .cta_group::2.
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// The shared::cluster address of the same shared-memory offset in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void *p, uint32_t rank) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
+    return a;
+}
+
+// Both CTAs of the cluster: every thread arrives (release) and waits (acquire).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive (release at cluster scope) on an mbarrier given by its
+// shared::cluster address (another CTA's, or this CTA's own): the thread's
+// earlier memory accesses, its pending global stores included, are made
+// visible to the cluster first.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)
+                 : "memory");
+}
+
+// The same arrival without ordering the thread's memory accesses: for
+// signals about tensor memory, whose loads and stores tcgen05.wait has
+// already completed (with tcgen05.fence::before_thread_sync before it).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t caddr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr)
+                 : "memory");
+}
+
+// Non-blocking test of phase `parity` of this CTA's `bar` with acquire at
+// cluster scope: pairs with arrivals made from the other CTA.
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// TMEM allocation of the pair: one warp of each CTA issues it; both CTAs get
+// the same column range.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *smem_dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(smem_u32(smem_dst)), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// D (+)= A[smem] * B[smem]^T over the pair (issued by rank 0 only).
+__device__ __forceinline__ void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D (+)= A[tmem] * B[smem]^T over the pair (issued by rank 0 only).
+__device__ __forceinline__ void mma_bf16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on this CTA's `bar` when the pair MMAs issued so far complete.
+__device__ __forceinline__ void mma_commit_pair(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+        ::"r"(smem_u32(bar))
+        : "memory");
+}
+
+// The same, arriving on the barrier at `bar`'s offset in both CTAs.
+__device__ __forceinline__ void mma_commit_pair_both(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;"
+        ::"r"(smem_u32(bar)), "h"((uint16_t)3)
+        : "memory");
+}
+
+// Tiled loads into this CTA's shared memory whose completion is signalled on
+// an mbarrier of either CTA of the pair (`bar` a shared::cluster address).
+__device__ __forceinline__ void tma_load_3d_pair(void *smem_dst, const CUtensorMap *map, int x,
+                                                 int y, int z, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+          "r"(z), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d_pair(void *smem_dst, const CUtensorMap *map, int x,
+                                                 int y, int z, int w, uint32_t bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+          "r"(z), "r"(w), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // Byte offset, inside a 128-byte-swizzled tile, of element `col` (bf16) of
 // row `row`.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {

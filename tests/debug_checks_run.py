@@ -30,7 +30,7 @@ from tests.helpers import compare, oracle_reference, run_gpu  # noqa: E402
 from tests.test_append_gpu import take_block  # noqa: E402
 
 GUARD_K, GUARD_V = 30.0, 1000.0
-KERNELS = ("simt", "tc", "rows")
+KERNELS = ("simt", "tc", "rows", "pairs")
 
 
 def record(name, fn):
@@ -80,7 +80,7 @@ def paged_call(case, kp, vp, table, n, **kw):
 
 def cases(kernel):
     d = 128 if kernel == "simt" else 256
-    q_len = 64 if kernel == "rows" else 8
+    q_len = 64 if kernel in ("rows", "pairs") else 8
     lens = [q_len + 300, q_len + 40, 512]
     return inputs.make_case("dbg", 3, 8, 2, d, q_len, 188, lens, 512, seed=31, outliers=True,
                             device="cuda")
@@ -105,9 +105,10 @@ def main():
             out, lse = paged_call(case, kp, vp, table, n)
             compare(out, lse, ref_o, ref_l, f"debug build, {kernel}, paged")
             assert torch.all(kp[n:] == GUARD_K) and torch.all(vp[n:] == GUARD_V)
-        record(f"{kernel}/valid paged", paged)
+        if kernel != "pairs":  # (a paged call takes the one-CTA kernel)
+            record(f"{kernel}/valid paged", paged)
 
-        if kernel != "rows":
+        if kernel not in ("rows", "pairs"):
             def append():
                 c2 = cases(kernel)
                 k_new, v_new = take_block(c2)
@@ -136,9 +137,10 @@ def main():
                 "sequence 0 read the guard page"
             compare(out[1:], lse[1:], ref_o[1:], ref_l[1:], f"debug build, {kernel}, bad page")
             assert torch.all(kp[n:] == GUARD_K) and torch.all(vp[n:] == GUARD_V)
-        record(f"{kernel}/page outside the pool", bad_page)
+        if kernel != "pairs":
+            record(f"{kernel}/page outside the pool", bad_page)
 
-        if kernel != "rows":
+        if kernel not in ("rows", "pairs"):
             def bad_page_append():
                 c4 = cases(kernel)
                 k_new, v_new = take_block(c4)

@@ -136,11 +136,16 @@ def test_plan_invariants(lib, B, q_len, Hq, Hkv, D, L, W, sms):
     units = p["num_splits"] * Hkv * p["row_tiles"] * B
     if p["kernel"] == 1:
         assert p["grid_ctas"] == units
+    elif p["kernel"] == 4:                  # persistent grid of CTA pairs over the work items
+        assert p["grid_ctas"] % 2 == 0 and 2 <= p["grid_ctas"] <= 2 * min(units, max(1, sms // 2))
+        assert D == 256 and R > 128
+        assert p["rows_per_tile"] == 2 * (128 // (Hq // Hkv)) * (Hq // Hkv)
     else:                                   # persistent grid over the work items
         assert p["kernel"] in (2, 3) and 1 <= p["grid_ctas"] <= min(units, sms)
-        # rows-major above 32 packed rows, unless the key-major items fit in
-        # one wave of the SMs or are small (8 or 16 rows)
-        assert p["kernel"] == (3 if R > 32 else 2) or (
+        # rows-major above 32 packed rows (on CTA pairs above 128 at head_dim
+        # 256), unless the key-major items fit in one wave of the SMs or are
+        # small (8 or 16 rows)
+        assert p["kernel"] == (3 if R > 32 and not (D == 256 and R > 128) else 2) or (
             p["kernel"] == 2 and (p["rows_per_tile"] <= 16 or units <= sms))
         assert p["rows_per_tile"] <= (128 if p["kernel"] == 3 else 64)
         assert p["rows_per_tile"] % (Hq // Hkv) == 0
@@ -162,6 +167,9 @@ def test_plan_kernel_choice(lib):
     d64 = swa.make_dims(1, 8, 2, 1, 64, 40)
     assert swa.swa_plan(d64, 16, 152)["kernel"] == 1            # head_dim 64: CUDA cores
     q64 = swa.swa_plan(swa.make_dims(512, 64, 8, 2, 256, 32768), 1024, 152)
+    assert q64["kernel"] == 4 and q64["row_tiles"] == 1 and q64["rows_per_tile"] == 256
+    assert q64["grid_ctas"] == 152
+    q64 = swa.swa_plan(swa.make_dims(512, 64, 8, 2, 128, 32768), 1024, 152)
     assert q64["kernel"] == 3 and q64["row_tiles"] == 2 and q64["rows_per_tile"] == 128
     q16 = swa.swa_plan(swa.make_dims(128, 16, 8, 2, 256, 4096), 188, 152)
     assert q16["kernel"] == 3 and q16["row_tiles"] == 1 and q16["rows_per_tile"] == 64
@@ -174,6 +182,11 @@ def test_plan_kernel_choice(lib):
         assert swa.swa_plan(d64, 16, 152)["kernel"] == 1
     with forced_kernel("rows"):
         assert swa.swa_plan(q1, 188, 152)["kernel"] == 3
+    with forced_kernel("pairs"):
+        p = swa.swa_plan(q1, 188, 152)
+        assert p["kernel"] == 4 and p["grid_ctas"] == 4 and p["rows_per_tile"] == 256
+        assert swa.swa_plan(swa.make_dims(1, 8, 8, 2, 128, 4096), 188, 152)["kernel"] == 3
+        assert swa.swa_plan(d64, 16, 152)["kernel"] == 1
     assert swa.swa_plan(q8, 188, 152)["kernel"] == 2  # back to the plan's choice
 
 
@@ -203,7 +216,7 @@ def test_debug_options_round_trip_and_validation(lib):
         swa.swa_set_debug_options()
     assert swa.swa_get_debug_options()["force_kernel"] == 0
     assert swa.swa_get_debug_options()["fail_launch"] == 0
-    for bad in ({"force_kernel": 4}, {"force_kernel": -1}, {"pdl": 2},
+    for bad in ({"force_kernel": 5}, {"force_kernel": -1}, {"pdl": 2},
                 {"wait_limit_cycles": -5}, {"withhold_fill": -2}, {"rows_per_item": -1},
                 {"fail_launch": -1}):
         with pytest.raises(swa.SwaError) as e:
@@ -220,7 +233,10 @@ def test_rows_per_item_override(lib):
     """The sweep override of rows per item: rounded to whole query groups,
     capped per kernel, ignored for CUDA-core plans and forced splits."""
     q64 = swa.make_dims(512, 64, 8, 2, 256, 32768)
-    assert swa.swa_plan(q64, 188, 152)["rows_per_tile"] == 128
+    assert swa.swa_plan(q64, 188, 152)["rows_per_tile"] == 256  # CTA pairs: no override
+    swa.swa_set_debug_options(rows_per_item=64)
+    assert swa.swa_plan(q64, 188, 152)["rows_per_tile"] == 256
+    swa.swa_set_debug_options()
     try:
         for want, got in ((64, 64), (32, 32), (30, 28), (3, 4), (500, 128)):
             swa.swa_set_debug_options(force_kernel="rows", rows_per_item=want)
@@ -361,7 +377,8 @@ def test_plan_few_units_prefer_small_key_major_items(lib):
         assert p["kernel"] == 2 and p["grid_ctas"] <= 152, (B, q_len, p)
     for B, q_len in ((512, 16), (512, 64), (128, 16), (64, 32), (32, 64), (64, 512)):
         p = swa.swa_plan(swa.make_dims(B, q_len, 8, 2, 256, 4096), 188, 152)
-        assert p["kernel"] == 3, (B, q_len, p)
+        # (on CTA pairs above 128 packed rows)
+        assert p["kernel"] == (4 if q_len * 4 > 128 else 3), (B, q_len, p)
     p = swa.swa_plan(swa.make_dims(64, 8, 8, 2, 256, 4096), 188, 152)
     assert p["kernel"] == 2 and p["rows_per_tile"] == 32
 

@@ -34,9 +34,10 @@ def results():
 
 
 KERNELS = ("simt", "tc", "rows")
-VALID = [f"{k}/valid contiguous" for k in KERNELS] + [f"{k}/valid paged" for k in KERNELS] + \
-        [f"{k}/valid fused append" for k in ("simt", "tc")]
-INVALID = [f"{k}/seq_len past the cache" for k in KERNELS] + \
+# the CTA-pair kernel reads contiguous caches only
+VALID = [f"{k}/valid contiguous" for k in KERNELS + ("pairs",)] + \
+        [f"{k}/valid paged" for k in KERNELS] + [f"{k}/valid fused append" for k in ("simt", "tc")]
+INVALID = [f"{k}/seq_len past the cache" for k in KERNELS + ("pairs",)] + \
           [f"{k}/page outside the pool" for k in KERNELS] + \
           [f"{k}/fused append into a page outside the pool" for k in ("simt", "tc")]
 

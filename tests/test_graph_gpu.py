@@ -81,8 +81,9 @@ def _replay_and_check(g, case, out, lse, what, before=None):
     ("window_vs_full_w4096", 0, "plan", 1),
     # the single-stream verify block split in five: key-major tensor-core + merge
     ("single_stream", 5, "plan", 2),
-    # the same with the rows-major tensor-core kernel
+    # the same with the rows-major tensor-core kernel, and on CTA pairs
     ("single_stream", 3, "rows", 3),
+    ("single_stream", 3, "pairs", 4),
     # a 64-sequence batch split in two
     ("batched", 2, "plan", 2),
 ])

@@ -49,6 +49,8 @@ CASES = [
     ("tc", lambda d: inputs.single_stream(device=d), 5, 2, "merge kernel launch"),
     ("rows", _q64, 0, 1, "tensor-core kernel launch"),
     ("rows", _q64, 3, 2, "merge kernel launch"),
+    ("pairs", _q64, 0, 1, "tensor-core kernel launch"),
+    ("pairs", _q64, 3, 2, "merge kernel launch"),
 ]
 
 

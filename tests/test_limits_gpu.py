@@ -61,7 +61,7 @@ def test_largest_row_block(kernel):
 
 
 @pytest.mark.parametrize("Hq,Hkv,q_len", [(64, 1, 8), (48, 4, 3), (48, 4, 1), (12, 1, 17)])
-@pytest.mark.parametrize("kernel", ["plan", "simt", "tc", "rows"])
+@pytest.mark.parametrize("kernel", ["plan", "simt", "tc", "rows", "pairs"])
 def test_large_and_odd_query_groups(Hq, Hkv, q_len, kernel):
     """G = 64 and G = 12 query heads per KV head, head_dim 128 and 256."""
     for D in (128, 256):
@@ -76,7 +76,7 @@ def test_large_and_odd_query_groups(Hq, Hkv, q_len, kernel):
         compare(out3, lse3, ref_o, ref_l, f"G={Hq // Hkv} q{q_len} D{D} {kernel}, 3 splits")
 
 
-@pytest.mark.parametrize("kernel", ["simt", "tc", "rows"])
+@pytest.mark.parametrize("kernel", ["simt", "tc", "rows", "pairs"])
 def test_sequences_with_no_visible_key(kernel):
     """seq_len 0 (nothing cached) and rows entirely before position 0: every
     such row gives out = 0 and lse = -inf; the other sequences are exact."""

@@ -26,12 +26,13 @@ def _built():
     yield
 
 
-@pytest.fixture(params=["simt", "tc", "rows"])
+@pytest.fixture(params=["simt", "tc", "rows", "pairs"])
 def kernel(request):
     """Runs the test once per kernel: the CUDA-core chunk kernel, the
-    key-major tensor-core kernel and the rows-major tensor-core kernel
-    (shapes the tensor-core kernels do not cover, head_dim 64, fall back to
-    the CUDA-core kernel)."""
+    key-major tensor-core kernel, the rows-major tensor-core kernel and its
+    CTA-pair form (shapes a tensor-core kernel does not cover fall back:
+    head_dim 64 to the CUDA-core kernel, head_dim 128 under "pairs" to the
+    one-CTA rows-major kernel)."""
     with forced_kernel(request.param):
         yield request.param
 

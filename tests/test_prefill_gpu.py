@@ -24,7 +24,7 @@ def _built():
     yield
 
 
-@pytest.fixture(params=["simt", "tc", "rows"])
+@pytest.fixture(params=["simt", "tc", "rows", "pairs"])
 def kernel(request):
     with forced_kernel(request.param):
         yield request.param
@@ -44,13 +44,14 @@ def test_prefill_chunk(D, q_len, window, splits, kernel):
     compare(out, lse, ref_o, ref_l, f"prefill D{D} q{q_len} W{window} {splits} splits {kernel}")
 
 
+@pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("q_len", [128, 512])
-def test_prefill_count_probe(q_len, kernel):
+def test_prefill_count_probe(q_len, D, kernel):
     """K = 0: lse = ln |K(p)| for every row, with |K(p)| = min(W, p + 1) near
     the start of the sequence and W further on."""
     window = 188
     lens = [q_len, q_len + 50]
-    case = inputs.make_case("count", 2, 8, 2, 128, q_len, window, lens, 1024, seed=7,
+    case = inputs.make_case("count", 2, 8, 2, D, q_len, window, lens, 1024, seed=7,
                             device="cuda")
     case.k_cache.zero_()
     _, lse = run_gpu(case)

@@ -49,6 +49,9 @@ def _many():
     ("tc", "single_stream", 0, 3),            # K of the first tile of a split plan
     ("rows", "single_stream", 0, 0),          # rows-major kernel, first K tile
     ("rows", "single_stream", 3, 0),          # rows-major kernel, last V tile
+    ("pairs", "single_stream", 0, 0),         # CTA pairs: rank 0's half of the first K tile
+    ("pairs", "single_stream", 3, 0),         # rank 0's half of the last V tile (rank 1 zeroes its own)
+    ("pairs", "many", 5, 0),                  # mid-item, several items per pair
 ])
 def test_withheld_copy_runs_out_and_reports(kernel, name, fill, splits):
     case = {"tiny_q8": lambda: inputs.tiny(8, device="cuda"),
