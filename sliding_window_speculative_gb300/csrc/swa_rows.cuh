@@ -425,19 +425,27 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
                     tmem_wait_ld();
                     float m4[4] = {NEG_INF, NEG_INF, NEG_INF, NEG_INF};
                     if (ca == 0 && cb == 63) {
+                        const uint64_t sc2 = f2_pack(sc, sc);
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) {
-                            const float x = __uint_as_float(sraw[c]) * sc;
-                            sraw[c] = __float_as_uint(x);
-                            m4[c & 3] = fmaxf(m4[c & 3], x);
+                        for (int c = 0; c < 64; c += 2) {
+                            float x0, x1;
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(sraw[c]), __uint_as_float(sraw[c + 1])),
+                                             sc2),
+                                      x0, x1);
+                            sraw[c] = __float_as_uint(x0);
+                            sraw[c + 1] = __float_as_uint(x1);
+                            m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], x0, x1);
                         }
                     } else {
 #pragma unroll
-                        for (int c = 0; c < 64; ++c) {
-                            const float x =
+                        for (int c = 0; c < 64; c += 2) {
+                            const float x0 =
                                 (c >= ca && c <= cb) ? __uint_as_float(sraw[c]) * sc : NEG_INF;
-                            sraw[c] = __float_as_uint(x);
-                            m4[c & 3] = fmaxf(m4[c & 3], x);
+                            const float x1 =
+                                (c + 1 >= ca && c + 1 <= cb) ? __uint_as_float(sraw[c + 1]) * sc : NEG_INF;
+                            sraw[c] = __float_as_uint(x0);
+                            sraw[c + 1] = __float_as_uint(x1);
+                            m4[(c >> 1) & 3] = fmax3(m4[(c >> 1) & 3], x0, x1);
                         }
                     }
                     // the pair's common tile maximum (one exchange per tile, buffers
@@ -478,20 +486,31 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
                     // P = 2^(s - m_ref) for this half's keys into the S buffer's TMEM
                     // columns: P_hi (bf16 truncation) in 0..63, P_lo (the rest,
                     // rounded) in 64..127, two keys per column, even key low
+                    // (pairs of keys through packed fp32 arithmetic)
                     {
                         uint32_t phi[32], plo[32];
-                        float ls0 = 0.f, ls1 = 0.f;
+                        const uint64_t m2 = f2_pack(mref, mref);
+                        uint64_t ls2 = f2_pack(0.f, 0.f);
 #pragma unroll
                         for (int c2 = 0; c2 < 32; ++c2) {
-                            const float p0 = fast_exp2(__uint_as_float(sraw[2 * c2]) - mref);
-                            const float p1 = fast_exp2(__uint_as_float(sraw[2 * c2 + 1]) - mref);
-                            ls0 += p0;
-                            ls1 += p1;
+                            float d0, d1;
+                            f2_unpack(f2_sub(f2_pack(__uint_as_float(sraw[2 * c2]),
+                                                     __uint_as_float(sraw[2 * c2 + 1])),
+                                             m2),
+                                      d0, d1);
+                            const float p0 = fast_exp2(d0), p1 = fast_exp2(d1);
+                            const uint64_t p2 = f2_pack(p0, p1);
+                            ls2 = f2_add(ls2, p2);
                             const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
                             phi[c2] = __byte_perm(u0, u1, 0x7632);
-                            plo[c2] = pack_bf16x2(p0 - __uint_as_float(u0 & 0xffff0000u),
-                                                  p1 - __uint_as_float(u1 & 0xffff0000u));
+                            float l0, l1;
+                            f2_unpack(f2_sub(p2, f2_pack(__uint_as_float(u0 & 0xffff0000u),
+                                                         __uint_as_float(u1 & 0xffff0000u))),
+                                      l0, l1);
+                            plo[c2] = pack_bf16x2(l0, l1);
                         }
+                        float ls0, ls1;
+                        f2_unpack(ls2, ls0, ls1);
                         lsum += ls0 + ls1;
                         tmem_st32(tl + sb * 128 + (kh >> 1), phi);
                         tmem_st32(tl + sb * 128 + 64 + (kh >> 1), plo);
@@ -531,22 +550,25 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
                         wlive[s2] = rr < it.rows;
                         wrow[s2] = (((size_t)it.b * P.q_len + i2) * P.Hq + (size_t)it.h * P.G + gg2) * D;
                     }
-#pragma unroll 1
-                    for (int c0 = 0; c0 < DH; c0 += 32) {
-                        uint32_t o[32];
-                        tmem_ld32(oc + c0, o);
+                    // (the next chunk's TMEM load is in flight meanwhile)
+                    uint32_t o[2][32];
+                    tmem_ld32(oc, o[0]);
+#pragma unroll
+                    for (int c = 0; c < DH / 32; ++c) {
                         tmem_wait_ld();
+                        if (c + 1 < DH / 32) tmem_ld32(oc + 32 * (c + 1), o[(c + 1) & 1]);
+                        const uint32_t *oo = o[c & 1];
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             uint4 w;
-                            w.x = pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv,
-                                              __uint_as_float(o[8 * q4 + 1]) * inv);
-                            w.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv,
-                                              __uint_as_float(o[8 * q4 + 3]) * inv);
-                            w.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv,
-                                              __uint_as_float(o[8 * q4 + 5]) * inv);
-                            w.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv,
-                                              __uint_as_float(o[8 * q4 + 7]) * inv);
+                            w.x = pack_bf16x2(__uint_as_float(oo[8 * q4 + 0]) * inv,
+                                              __uint_as_float(oo[8 * q4 + 1]) * inv);
+                            w.y = pack_bf16x2(__uint_as_float(oo[8 * q4 + 2]) * inv,
+                                              __uint_as_float(oo[8 * q4 + 3]) * inv);
+                            w.z = pack_bf16x2(__uint_as_float(oo[8 * q4 + 4]) * inv,
+                                              __uint_as_float(oo[8 * q4 + 5]) * inv);
+                            w.w = pack_bf16x2(__uint_as_float(oo[8 * q4 + 6]) * inv,
+                                              __uint_as_float(oo[8 * q4 + 7]) * inv);
                             *reinterpret_cast<uint4 *>(stg + lane * 64 +
                                                        ((q4 ^ ((lane >> 1) & 3)) << 4)) = w;
                         }
@@ -557,7 +579,7 @@ __global__ void __launch_bounds__(AP ? kRowsThreads + 32 : kRowsThreads, 1)
                             const uint4 w = *reinterpret_cast<const uint4 *>(
                                 stg + rr * 64 + ((wc ^ ((rr >> 1) & 3)) << 4));
                             if (wlive[s2])
-                                *reinterpret_cast<uint4 *>(P.out + wrow[s2] + half * DH + c0 + wc * 8) = w;
+                                *reinterpret_cast<uint4 *>(P.out + wrow[s2] + half * DH + 32 * c + wc * 8) = w;
                         }
                         __syncwarp();
                     }

@@ -1148,8 +1148,13 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
                         tmem_load<CWH>(tl + sb * N + r0 + c * CWH, raw + c * CWH);
                     tmem_wait_ld();
                     if (ra <= 0 && rb >= HN) {
+                        // (pairs of rows through packed fp32 arithmetic)
+                        const uint64_t sc2 = f2_pack(P.qk_scale, P.qk_scale);
 #pragma unroll
-                        for (int r = 0; r < HN; ++r) v[r] = __uint_as_float(raw[r]) * P.qk_scale;
+                        for (int r = 0; r < HN; r += 2)
+                            f2_unpack(f2_mul(f2_pack(__uint_as_float(raw[r]), __uint_as_float(raw[r + 1])),
+                                             sc2),
+                                      v[r], v[r + 1]);
                     } else {
 #pragma unroll
                         for (int r = 0; r < HN; ++r)
@@ -1256,16 +1261,27 @@ __global__ void __launch_bounds__(AP ? kTcThreads + 32 : kTcThreads, 1)
                 // (P_hi + P_lo within 2^-16 of P).  Row r0 + r of the tile; r0
                 // is a multiple of 8, so the row's swizzle phase is r & 7.
                 uint8_t *pt = ps + pb * C::P_BUF + p_key + r0 * 128;
+                // (pairs of rows through packed fp32 arithmetic)
 #pragma unroll
-                for (int r = 0; r < HN; ++r) {
-                    const float p = fast_exp2(v[r] - mref[r]);
-                    const uint32_t bits = __float_as_uint(p);
-                    const float lo = p - __uint_as_float(bits & 0xffff0000u);
-                    const uint32_t sw = (p_chunk ^ (uint32_t)(r & 7)) << 4;
-                    *reinterpret_cast<uint16_t *>(pt + r * 128 + sw) = (uint16_t)(bits >> 16);
-                    *reinterpret_cast<uint16_t *>(pt + (N + r) * 128 + sw) =
-                        __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-                    lrow[r] += p;
+                for (int r = 0; r < HN; r += 2) {
+                    float d0, d1;
+                    f2_unpack(f2_sub(f2_pack(v[r], v[r + 1]), f2_pack(mref[r], mref[r + 1])), d0, d1);
+                    const float p0 = fast_exp2(d0), p1 = fast_exp2(d1);
+                    const uint64_t p2 = f2_pack(p0, p1);
+                    f2_unpack(f2_add(f2_pack(lrow[r], lrow[r + 1]), p2), lrow[r], lrow[r + 1]);
+                    const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+                    float lo0, lo1;
+                    f2_unpack(f2_sub(p2, f2_pack(__uint_as_float(b0 & 0xffff0000u),
+                                                 __uint_as_float(b1 & 0xffff0000u))),
+                              lo0, lo1);
+                    const uint32_t sw0 = (p_chunk ^ (uint32_t)(r & 7)) << 4;
+                    const uint32_t sw1 = (p_chunk ^ (uint32_t)((r + 1) & 7)) << 4;
+                    *reinterpret_cast<uint16_t *>(pt + r * 128 + sw0) = (uint16_t)(b0 >> 16);
+                    *reinterpret_cast<uint16_t *>(pt + (r + 1) * 128 + sw1) = (uint16_t)(b1 >> 16);
+                    *reinterpret_cast<uint16_t *>(pt + (N + r) * 128 + sw0) =
+                        __bfloat16_as_ushort(__float2bfloat16_rn(lo0));
+                    *reinterpret_cast<uint16_t *>(pt + (N + r + 1) * 128 + sw1) =
+                        __bfloat16_as_ushort(__float2bfloat16_rn(lo1));
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&bars[C::B_PFULL + pb]);

@@ -356,6 +356,42 @@ __device__ __forceinline__ void tma_load_4d_pair(void *smem_dst, const CUtensorM
         : "memory");
 }
 
+// ------------------------------------------------- packed fp32 pairs (f32x2)
+// Two fp32 values in one 64-bit register pair, operated on by one
+// instruction each (round to nearest, as the scalar forms).
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t v;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+    return v;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// The largest of three floats in one instruction (a NaN operand is ignored,
+// as fmaxf does).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Byte offset, inside a 128-byte-swizzled tile, of element `col` (bf16) of
 // row `row`.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col) {
