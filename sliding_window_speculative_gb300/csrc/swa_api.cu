@@ -308,12 +308,20 @@ Plan make_plan_with(const swa_dims *d, int32_t window, int num_sms, int force, b
 // 22.8; q32 8 sequences 13.3 / 12.0, 32: 14.7 / 14.0, 64 (256 items): 17.4 /
 // 23.4; q64 4 sequences 13.3 / 11.8, 16: 14.4 / 13.8, 32 (256 items): 16.6 /
 // 22.7; a 512-token prefill chunk of one sequence 13.6 / 12.1.
+//
+// Against the CTA-pair kernel (above 128 rows) the key-major plan wins only
+// when it cuts the rows into 8- or 16-row items.  Measured on GB300, W188,
+// us, key-major / pairs: q64 one sequence 7.6 / 11.0 (16-row items), 4
+// sequences 11.5 / 11.2, 8: 11.7 / 11.3, 16: 12.9 / 11.5; a 512-token
+// prefill chunk, one sequence 11.7 / 11.3, two 12.9 / 11.5.
 Plan make_plan(const swa_dims *d, int32_t window, int num_sms, bool pairs_ok) {
     const int force = forced_kernel();
     Plan p = make_plan_with(d, window, num_sms, force, pairs_ok);
     if (force == 0 && p.kernel >= 3) {
         const Plan k = make_plan_with(d, window, num_sms, 2, pairs_ok);
-        if (k.kernel == 2 && (k.rows_per_tile <= 16 || k.items <= (long long)num_sms)) return k;
+        const bool small_items = k.rows_per_tile <= 16;
+        const bool one_wave = k.items <= (long long)num_sms;
+        if (k.kernel == 2 && (small_items || (p.kernel == 3 && one_wave))) return k;
     }
     return p;
 }

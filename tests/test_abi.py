@@ -348,12 +348,12 @@ def test_paged_verify_rejects_bad_tables(lib):
 
 
 def test_plan_prefill_chunk_reads_row_windows(lib):
-    # a 512-row prefill chunk at W = 188: a row tile's rows see W + 15 keys
-    # (key-major, 64-row items: 16 draft rows each, one wave of the SMs) or
-    # W + 31 (rows-major, 128 rows), so no split although the whole span is
-    # 699 keys; at W = 4096 the row tiles' windows are split to reach the SMs
+    # a 512-row prefill chunk at W = 188: an item's rows see W + 63 keys (CTA
+    # pairs, 256 rows) or W + 31 (one-CTA rows-major, 128 rows), so no split
+    # although the whole span is 699 keys; at W = 4096 the row tiles'
+    # windows are split to reach the SMs
     p = swa.swa_plan(swa.make_dims(1, 512, 8, 2, 256, 4096), 188, 152)
-    assert p["kernel"] == 2 and p["row_tiles"] == 32 and p["num_splits"] == 1
+    assert p["kernel"] == 4 and p["row_tiles"] == 8 and p["num_splits"] == 1
     with forced_kernel("rows"):
         p = swa.swa_plan(swa.make_dims(1, 512, 8, 2, 256, 4096), 188, 152)
         assert p["kernel"] == 3 and p["row_tiles"] == 16 and p["num_splits"] == 1
@@ -370,11 +370,15 @@ def test_plan_few_units_prefer_small_key_major_items(lib):
         p = swa.swa_plan(swa.make_dims(B, q_len, 8, 2, 256, 4096), 188, 152)
         assert p["kernel"] == 2 and p["rows_per_tile"] == rows, (B, q_len, p)
         assert p["grid_ctas"] <= 152
-    # more than 32 rows: the key-major kernel while its items (up to 64 rows)
-    # fit in one wave of the SMs, else the rows-major kernel
-    for B, q_len in ((16, 16), (64, 16), (8, 32), (32, 32), (4, 64), (16, 64), (1, 512)):
+    # 33..128 rows: the key-major kernel while its items (up to 64 rows) fit
+    # in one wave of the SMs, else the rows-major kernel; above 128 rows the
+    # CTA pairs unless the key-major items are small
+    for B, q_len in ((16, 16), (64, 16), (8, 32), (32, 32), (1, 64), (2, 64)):
         p = swa.swa_plan(swa.make_dims(B, q_len, 8, 2, 256, 4096), 188, 152)
         assert p["kernel"] == 2 and p["grid_ctas"] <= 152, (B, q_len, p)
+    for B, q_len in ((4, 64), (16, 64), (1, 512), (2, 512)):
+        p = swa.swa_plan(swa.make_dims(B, q_len, 8, 2, 256, 4096), 188, 152)
+        assert p["kernel"] == 4, (B, q_len, p)
     for B, q_len in ((512, 16), (512, 64), (128, 16), (64, 32), (32, 64), (64, 512)):
         p = swa.swa_plan(swa.make_dims(B, q_len, 8, 2, 256, 4096), 188, 152)
         # (on CTA pairs above 128 packed rows)
