@@ -55,6 +55,11 @@ constexpr int kPairSlots = 4;
 struct PairMaps {
     CUtensorMap vh_atoms[4];  // 4D boxes of 16, 8, 4, 2 atoms
     CUtensorMap vh_atom;      // 3D box of one atom (rows past the cache are zero-filled)
+    // out [B * q_len rows][Hq][D] as 3D (x = head dim, y = query head, z = row),
+    // a box of 32 dims x G heads x 32 / G rows (one softmax warp's 32 packed
+    // rows), 64-byte swizzled: valid when out_ok (G divides 32)
+    CUtensorMap out;
+    int out_ok;
 };
 
 template <int D, int NT>
@@ -74,7 +79,9 @@ struct PairCfg {
     // half row sums [quadrant][half][lane]
     static constexpr int XM_OFF = (META_OFF + kTcMetaItems * (int)sizeof(TcItem) + 15) & ~15;
     static constexpr int XL_OFF = XM_OFF + 2 * 4 * 2 * 32 * 4;
-    static constexpr int STG_OFF = (XL_OFF + 4 * 2 * 32 * 4 + 15) & ~15;  // 16-byte stores
+    // (1024-byte aligned: the 64-byte swizzle of the output's tensor store
+    // follows the shared-memory address)
+    static constexpr int STG_OFF = (XL_OFF + 4 * 2 * 32 * 4 + 1023) & ~1023;
     static constexpr int STG_NEED = 8 * 2048;  // output staging, 2 KB per softmax warp
     static constexpr int BAR_OFF = STG_OFF + STG_NEED;
     // ring full / empty [NT], rank 1's own landing of a V half to zero [NT],
@@ -706,6 +713,12 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                     // bank conflicts), then stored as 8 rows x 64 B per instruction
                     const float inv = ltot > 0.f ? __frcp_rn(ltot) : 0.f;
                     uint8_t *stg = sm + C::STG_OFF + (warp - 2) * 2048;
+                    // the warp's 32 rows all in the item and starting a query row:
+                    // each staged chunk leaves in one tensor store, so the warp does
+                    // not wait on the output's global stores
+                    const int rw0 = it.row0 + quad * 32;
+                    const bool tma_out = PM.out_ok && quad * 32 + 31 < it.rows && rw0 % P.G == 0;
+                    const int oy = it.h * P.G, oz = it.b * P.q_len + rw0 / P.G;
                     const int wr = lane >> 2, wc = lane & 3;  // write-back row (+ 8 s), chunk
                     size_t wrow[4];
                     bool wlive[4];
@@ -725,6 +738,9 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                         tmem_wait_ld();
                         if (c + 1 < DH / 32) tmem_ld32(oc + 32 * (c + 1), o[(c + 1) & 1]);
                         const uint32_t *oo = o[c & 1];
+                        // the staging buffer's previous tensor store has read it
+                        if (lane == 0) bulk_wait_read();
+                        __syncwarp();
 #pragma unroll
                         for (int q4 = 0; q4 < 4; ++q4) {
                             uint4 w;
@@ -738,6 +754,15 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                                               __uint_as_float(oo[8 * q4 + 7]) * inv);
                             *reinterpret_cast<uint4 *>(stg + lane * 64 +
                                                        ((q4 ^ ((lane >> 1) & 3)) << 4)) = w;
+                        }
+                        if (tma_out) {
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                tma_store_3d(&PM.out, half * DH + 32 * c, oy, oz, stg);
+                                bulk_commit();
+                            }
+                            continue;
                         }
                         __syncwarp();
 #pragma unroll
@@ -780,6 +805,7 @@ __global__ void __launch_bounds__(kPairThreads, 1)
                 if (lane == 0) mbar_arrive_cluster_relaxed(ofree0);
             }
             (void)ok;
+            if (lane == 0) bulk_wait_all();  // this warp's output stores complete
         }
     }
 

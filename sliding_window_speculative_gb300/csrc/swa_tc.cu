@@ -279,6 +279,20 @@ cudaError_t tc_launch(const TcLaunch &L, cudaStream_t stream, char *err, size_t 
                 return cudaErrorInvalidValue;
             }
         }
+        if (P.G <= 32 && 32 % P.G == 0) {
+            cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)P.Hq, (cuuint64_t)P.B * P.q_len};
+            cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)P.Hq * D * 2};
+            cuuint32_t box[3] = {32, (cuuint32_t)P.G, (cuuint32_t)(32 / P.G)};
+            cuuint32_t es[3] = {1, 1, 1};
+            CUresult r = g_encode(&pm.out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, P.out, dims, strides,
+                                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS) {
+                snprintf(err, errlen, "cuTensorMapEncodeTiled(out) failed: %d", (int)r);
+                return cudaErrorInvalidValue;
+            }
+            pm.out_ok = 1;
+        }
         return launch_pairs<256>(L, maps, pm, stream);
     }
     if (L.rows_major) {
